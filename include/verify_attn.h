@@ -1,0 +1,195 @@
+/*
+ * verify_attn.h - C ABI of the GB300 (sm_103a) target-verify attention library.
+ *
+ * The operation (sglang PR 36330 digest, "Motivation" and "Key code excerpts"):
+ * speculative decoding's target-verify step runs a short multi-token query
+ * (1-4 draft tokens per sequence, a GQA group of query heads per KV head,
+ * head_dim 256) causally over a long paged KV cache (page size 16, FP8 E4M3
+ * with per-tensor k/v descale, or BF16). The work of each (sequence, KV head)
+ * is split across KV segments and the per-segment partial results are merged
+ * by a log-sum-exp segment reduction (same digest, "Implementation breakdown"
+ * item 1: the main kernel plus its "reduce segments" kernel).
+ *
+ * For sequence b with L = cu_seqlens_q[b+1] - cu_seqlens_q[b] draft tokens and
+ * S = seqused_k[b] cached tokens (S counts the draft tokens too: the digest's
+ * call passes seq_lens + max_q_len), query head h of draft token t reads KV
+ * head h / (Hq/Hkv) and sees keys [0, S - L + t]:
+ *
+ *   out[cu[b]+t, h, :] = softmax(softmax_scale * k_descale * q . K^T) (v_descale * V)
+ *
+ * A row whose token sees no key (S - L + t < 0) is written as 0.
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor argument is a va_tensor: a DEVICE pointer plus shape and
+ *    strides counted in elements. The library never keeps a pointer after the
+ *    call returns and never frees caller memory.
+ *  - Launches are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream). No entry point synchronises, reads device memory from
+ *    the host, or depends on device values for its launch shape: only the
+ *    host integers max_seqlen_q / max_seqlen_k (upper bounds) size the grid.
+ *  - Errors are returned as va_status before anything is launched; nothing
+ *    aborts or throws across the ABI. VA_ERR_CUDA reports a failed launch or
+ *    allocation (the CUDA error is left for cudaGetLastError to inspect).
+ *  - Device-side preconditions (seqused_k[b] <= block_table width * 16,
+ *    0 <= cu_seqlens_q deltas <= max_seqlen_q, cu_seqlens_q[B] <= total_q,
+ *    block-table entries < num_blocks) are the caller's. Violations never
+ *    cause an out-of-bounds access (lengths are clamped, bad page ids read as
+ *    zeros) but the affected output rows are unspecified.
+ */
+#ifndef VERIFY_ATTN_H
+#define VERIFY_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. FP8_E4M3 is OCP E4M3 "FN" (torch.float8_e4m3fn). */
+typedef enum va_dtype {
+  VA_BF16 = 0,
+  VA_FP8_E4M3 = 1,
+  VA_INT32 = 2,
+  VA_FP32 = 3
+} va_dtype;
+
+/* A strided view of device memory. Strides are in elements. */
+typedef struct va_tensor {
+  void* data;
+  int32_t dtype;      /* va_dtype */
+  int32_t ndim;       /* 1..4 */
+  int64_t shape[4];
+  int64_t stride[4];
+} va_tensor;
+
+typedef enum va_status {
+  VA_OK = 0,
+  VA_ERR_NULL = 1,         /* a required pointer or descriptor is NULL */
+  VA_ERR_SHAPE = 2,        /* shapes disagree with each other */
+  VA_ERR_DTYPE = 3,        /* an element type is not the one required */
+  VA_ERR_UNSUPPORTED = 4,  /* well-formed but outside what the kernels cover */
+  VA_ERR_WORKSPACE = 5,    /* caller workspace missing or too small */
+  VA_ERR_CUDA = 6,         /* a CUDA runtime call or launch failed */
+  VA_ERR_LAYOUT = 7        /* a stride or alignment the kernels cannot read */
+} va_status;
+
+/* Launch plan chosen by the host heuristic (pure host arithmetic). */
+typedef struct va_plan {
+  int32_t tile_keys;       /* keys per pipeline tile of the main kernel */
+  int32_t num_splits;      /* CTAs of the main kernel; each takes an equal share
+                              of the batch's key tiles (its KV segments) */
+  int32_t max_rows;        /* packed rows per (sequence, KV head) = G * max_seqlen_q */
+  int32_t num_work;        /* B * Hkv (sequence, KV head) pairs */
+  int32_t kernel;          /* main-kernel variant the launch will use */
+  int32_t reserved;
+  int64_t workspace_bytes; /* scratch the split-KV partials need */
+} va_plan;
+
+/*
+ * verify_attn - the operation described above.
+ *
+ * q            [total_q, Hq, 256] BF16; innermost stride 1, rows 16-byte aligned.
+ * k_cache      [num_blocks, 16, Hkv, 256] FP8_E4M3 or BF16; innermost stride 1,
+ * v_cache      the other strides multiples of 16 bytes. Same dtype and shape.
+ *              Token-major pages with the heads of a token interleaved
+ *              (sglang PR 36330 digest, unit test: key/value shape
+ *              (num_blocks, block_size, num_kv_heads, head_size)).
+ * block_table  [B, W] INT32, logical page -> physical page, W*16 >= max_seqlen_k.
+ *              Only the first ceil(seqused_k[b]/16) entries of row b are read.
+ * cu_seqlens_q [B+1] INT32 contiguous, prefix sums of the draft-token counts.
+ * seqused_k    [B] INT32 contiguous, cached tokens per sequence incl. drafts.
+ * max_seqlen_q host upper bound of the draft-token counts; 1 <= max_seqlen_q
+ *              and (Hq/Hkv) * max_seqlen_q <= 64.
+ * max_seqlen_k host upper bound of seqused_k (the digest passes
+ *              page_table.shape[1] * page_size; sglang PR 30105 digest,
+ *              "Key code excerpts").
+ * softmax_scale  multiplies the logits (head_dim ** -0.5 in the pages).
+ * k_descale, v_descale  [1] FP32 device scalars or NULL (= 1.0): the
+ *              dequantised value is stored value * descale (sglang PR 34517
+ *              digest, "Key code excerpts": qk *= sm_scale * k_scale).
+ * out          [total_q, Hq, 256] BF16, written in place (round to nearest
+ *              even from fp32); may not alias any input.
+ * stream       cudaStream_t.
+ *
+ * Scratch: a per-device workspace owned by the library, grown (cudaMalloc) on
+ * demand and kept until process exit. Because growing allocates, make the
+ * first call with the largest shape before capturing a CUDA graph, or use
+ * verify_attn_ex with a caller workspace. Calls that share the library
+ * workspace must be ordered on one stream (concurrent streams race on it).
+ */
+va_status verify_attn(const va_tensor* q, const va_tensor* k_cache, const va_tensor* v_cache,
+                      const va_tensor* block_table, const va_tensor* cu_seqlens_q,
+                      const va_tensor* seqused_k, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                      float softmax_scale, const va_tensor* k_descale,
+                      const va_tensor* v_descale, va_tensor* out, void* stream);
+
+/*
+ * verify_attn_ex - verify_attn with a caller-owned workspace and an optional
+ * forced split count. Not on the pages: it exists so a caller can own all
+ * memory (graph capture, allocator integration) and so tests can force the
+ * number of KV segments.
+ *
+ * workspace        device pointer, 256-byte aligned, at least
+ *                  verify_attn_workspace_size(...) bytes for the same shapes
+ *                  and num_splits; NULL with workspace_bytes == 0 is valid only
+ *                  when that size is 0.
+ * num_splits       0 = the heuristic's choice; > 0 forces the main kernel's
+ *                  CTA count (clamped to the number of key tiles it could have).
+ * The workspace holds no state between calls.
+ */
+va_status verify_attn_ex(const va_tensor* q, const va_tensor* k_cache, const va_tensor* v_cache,
+                         const va_tensor* block_table, const va_tensor* cu_seqlens_q,
+                         const va_tensor* seqused_k, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                         float softmax_scale, const va_tensor* k_descale,
+                         const va_tensor* v_descale, va_tensor* out, void* workspace,
+                         size_t workspace_bytes, int32_t num_splits, void* stream);
+
+/*
+ * verify_attn_check - validation only: the same checks verify_attn runs before
+ * launching, as a pure host function (no CUDA call; device pointers are only
+ * tested for NULL and alignment). Turns the shape gate of sglang PR 36330
+ * digest ("Key code excerpts", aiter_backend.py) and the rejections of sglang
+ * PR 34517 digest ("Implementation breakdown": can_handle) into status codes.
+ */
+va_status verify_attn_check(const va_tensor* q, const va_tensor* k_cache, const va_tensor* v_cache,
+                            const va_tensor* block_table, const va_tensor* cu_seqlens_q,
+                            const va_tensor* seqused_k, int32_t max_seqlen_q,
+                            int32_t max_seqlen_k, const va_tensor* k_descale,
+                            const va_tensor* v_descale, const va_tensor* out);
+
+/*
+ * verify_attn_plan - the host launch heuristic as a pure function (no CUDA
+ * call). Picks the tile size and the number of KV segments (main-kernel CTAs)
+ * from the batch, the KV-length bound and the SM count, so that short-query
+ * batches fill every SM (sglang PR 36330 digest, "Implementation breakdown"
+ * item 1: 8-64 segments for CU parallelism; sglang PR 30105 digest,
+ * "Implementation breakdown" item 3: split-KV restores occupancy for short
+ * queries).
+ *
+ * num_sms        SMs of the target device (> 0).
+ * force_splits   0 = heuristic; > 0 = this many (clamped as in verify_attn_ex).
+ * Returns VA_ERR_NULL if plan is NULL, VA_ERR_UNSUPPORTED for arguments out
+ * of range.
+ */
+va_status verify_attn_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
+                           int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t kv_dtype,
+                           int32_t num_sms, int32_t force_splits, va_plan* plan);
+
+/*
+ * verify_attn_workspace_size - bytes of workspace verify_attn_ex needs for
+ * these shapes on the current device with num_splits (0 = heuristic). Queries
+ * the current device's SM count (a CUDA call); returns 0 on error.
+ */
+size_t verify_attn_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
+                                  int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t kv_dtype,
+                                  int32_t num_splits);
+
+/* Static, NUL-terminated name of a status code. */
+const char* verify_attn_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_ATTN_H */

@@ -1,0 +1,208 @@
+"""Python binding of the verify-attention C-ABI library (``include/verify_attn.h``).
+
+Argument marshalling only: torch tensors become ``va_tensor`` descriptors
+(device pointer, dtype code, shape, strides) and the call goes to the native
+library, which runs every step in its own CUDA kernels. There is no Python or
+CPU fallback: if the library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libverify_attn.so")
+
+VA_BF16, VA_FP8_E4M3, VA_INT32, VA_FP32 = 0, 1, 2, 3
+VA_OK = 0
+STATUS_NAMES = {0: "VA_OK", 1: "VA_ERR_NULL", 2: "VA_ERR_SHAPE", 3: "VA_ERR_DTYPE",
+                4: "VA_ERR_UNSUPPORTED", 5: "VA_ERR_WORKSPACE", 6: "VA_ERR_CUDA",
+                7: "VA_ERR_LAYOUT"}
+
+_DTYPES = {torch.bfloat16: VA_BF16, torch.float8_e4m3fn: VA_FP8_E4M3,
+           torch.int32: VA_INT32, torch.float32: VA_FP32}
+
+# Every symbol include/verify_attn.h declares.
+EXPORTS = ("verify_attn", "verify_attn_ex", "verify_attn_check", "verify_attn_plan",
+           "verify_attn_workspace_size", "verify_attn_status_string")
+
+
+class VaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class VaPlan(ctypes.Structure):
+    _fields_ = [("tile_keys", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+                ("max_rows", ctypes.c_int32), ("num_work", ctypes.c_int32),
+                ("kernel", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64)]
+
+
+class VerifyAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} "
+                         f"({_lib().verify_attn_status_string(status).decode()})")
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"native library not built: {LIB_PATH} is missing "
+                               "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+        lib = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER(VaTensor)
+        tens = [P] * 6 + [ctypes.c_int32, ctypes.c_int32]
+        lib.verify_attn.argtypes = tens + [ctypes.c_float, P, P, P, ctypes.c_void_p]
+        lib.verify_attn.restype = ctypes.c_int32
+        lib.verify_attn_ex.argtypes = tens + [ctypes.c_float, P, P, P, ctypes.c_void_p,
+                                              ctypes.c_size_t, ctypes.c_int32, ctypes.c_void_p]
+        lib.verify_attn_ex.restype = ctypes.c_int32
+        lib.verify_attn_check.argtypes = tens + [P, P, P]
+        lib.verify_attn_check.restype = ctypes.c_int32
+        lib.verify_attn_plan.argtypes = [ctypes.c_int32] * 8 + [ctypes.POINTER(VaPlan)]
+        lib.verify_attn_plan.restype = ctypes.c_int32
+        lib.verify_attn_workspace_size.argtypes = [ctypes.c_int32] * 7
+        lib.verify_attn_workspace_size.restype = ctypes.c_size_t
+        lib.verify_attn_status_string.argtypes = [ctypes.c_int32]
+        lib.verify_attn_status_string.restype = ctypes.c_char_p
+        _LIB = lib
+    return _LIB
+
+
+def library():
+    """The loaded ctypes library (raises if it was not built)."""
+    return _lib()
+
+
+def desc(t: Optional[torch.Tensor]):
+    """va_tensor descriptor of a torch tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    if t.dim() > 4:
+        raise ValueError("at most 4 dimensions")
+    d = VaTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else 0
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _ref(d):
+    return None if d is None else ctypes.byref(d)
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, k_descale, v_descale, out):
+    ds = [desc(x) for x in (q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
+                            k_descale, v_descale, out)]
+    return ds, [_ref(d) for d in ds]
+
+
+def verify_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q: int,
+                max_seqlen_k: int, softmax_scale: float, k_descale=None, v_descale=None,
+                out=None, stream=None):
+    """Target-verify attention (see include/verify_attn.h). Returns ``out``."""
+    if out is None:
+        out = torch.empty_like(q)
+    ds, r = _args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, k_descale,
+                  v_descale, out)
+    with torch.cuda.device(q.device):
+        s = _lib().verify_attn(r[0], r[1], r[2], r[3], r[4], r[5], int(max_seqlen_q),
+                               int(max_seqlen_k), float(softmax_scale), r[6], r[7], r[8],
+                               ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if s != VA_OK:
+        raise VerifyAttnError(s, "verify_attn")
+    return out
+
+
+def verify_attn_ex(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q: int,
+                   max_seqlen_k: int, softmax_scale: float, k_descale=None, v_descale=None,
+                   out=None, workspace: Optional[torch.Tensor] = None, num_splits: int = 0,
+                   stream=None):
+    """verify_attn with a caller workspace (a uint8 device tensor) and a forced
+    split count (0 = heuristic). Allocates the workspace with torch if None."""
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        n = workspace_size(q, k_cache, seqused_k, max_seqlen_q, max_seqlen_k, num_splits)
+        workspace = torch.empty(n + 256, dtype=torch.uint8, device=q.device)
+    addr = workspace.data_ptr()
+    off = (-addr) % 256
+    ds, r = _args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, k_descale,
+                  v_descale, out)
+    with torch.cuda.device(q.device):
+        s = _lib().verify_attn_ex(r[0], r[1], r[2], r[3], r[4], r[5], int(max_seqlen_q),
+                                  int(max_seqlen_k), float(softmax_scale), r[6], r[7], r[8],
+                                  ctypes.c_void_p(addr + off), workspace.numel() - off,
+                                  int(num_splits),
+                                  ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if s != VA_OK:
+        raise VerifyAttnError(s, "verify_attn_ex")
+    return out
+
+
+def check(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q: int,
+          max_seqlen_k: int, k_descale=None, v_descale=None, out=None) -> int:
+    """Host-only validation; returns the va_status code (no CUDA call)."""
+    ds, r = _args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, k_descale,
+                  v_descale, out)
+    return int(_lib().verify_attn_check(r[0], r[1], r[2], r[3], r[4], r[5], int(max_seqlen_q),
+                                        int(max_seqlen_k), r[6], r[7], r[8]))
+
+
+def plan(num_seqs, num_kv_heads, num_q_heads, max_seqlen_q, max_seqlen_k, kv_dtype, num_sms,
+         force_splits=0) -> dict:
+    """The host launch heuristic (pure function). Raises on an error status."""
+    p = VaPlan()
+    code = VA_FP8_E4M3 if kv_dtype in ("fp8_e4m3", VA_FP8_E4M3, torch.float8_e4m3fn) else VA_BF16
+    s = _lib().verify_attn_plan(int(num_seqs), int(num_kv_heads), int(num_q_heads),
+                                int(max_seqlen_q), int(max_seqlen_k), code, int(num_sms),
+                                int(force_splits), ctypes.byref(p))
+    if s != VA_OK:
+        raise VerifyAttnError(s, "verify_attn_plan")
+    return {f: getattr(p, f) for f, _ in VaPlan._fields_ if f != "reserved"}
+
+
+def workspace_size(q, k_cache, seqused_k, max_seqlen_q, max_seqlen_k, num_splits=0) -> int:
+    code = _DTYPES[k_cache.dtype]
+    with torch.cuda.device(q.device):
+        n = _lib().verify_attn_workspace_size(int(seqused_k.shape[0]), int(k_cache.shape[2]),
+                                              int(q.shape[1]), int(max_seqlen_q),
+                                              int(max_seqlen_k), code, int(num_splits))
+    if n == 0:
+        raise VerifyAttnError(4, "verify_attn_workspace_size")
+    return int(n)
+
+
+def run_workload(w, out=None, stream=None, **kw):
+    """verify_attn on a ``workloads.Workload`` whose tensors are on the GPU."""
+    return verify_attn(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q, w.seqused_k,
+                       w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale, w.k_descale,
+                       w.v_descale, out=out, stream=stream, **kw)
+
+
+def run_workload_ex(w, out=None, workspace=None, num_splits=0, stream=None):
+    return verify_attn_ex(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q, w.seqused_k,
+                          w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale, w.k_descale,
+                          w.v_descale, out=out, workspace=workspace, num_splits=num_splits,
+                          stream=stream)

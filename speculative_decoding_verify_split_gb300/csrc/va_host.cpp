@@ -1,0 +1,363 @@
+// Host side of the C ABI (include/verify_attn.h): argument validation, the
+// split heuristic, the library-owned workspace and the kernel launches.
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/verify_attn.h"
+#include "va_internal.h"
+
+#define VA_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using namespace va;
+
+constexpr int kMaxDevices = 64;
+
+struct Shapes {
+  int64_t total_q, hq, hkv, num_blocks, num_seqs, width;
+  int32_t kv_dtype;
+};
+
+int64_t numel(const va_tensor* t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_size(int32_t dt) {
+  switch (dt) {
+    case VA_BF16: return 2;
+    case VA_FP8_E4M3: return 1;
+    case VA_INT32: return 4;
+    case VA_FP32: return 4;
+    default: return 0;
+  }
+}
+
+bool dims_ok(const va_tensor* t, int ndim) {
+  if (t->ndim != ndim) return false;
+  for (int i = 0; i < ndim; ++i)
+    if (t->shape[i] < 0 || t->stride[i] < 0) return false;
+  return true;
+}
+
+// Strides of all but the innermost dimension, in bytes, are multiples of 16
+// and the innermost stride is 1.
+bool rows_16b(const va_tensor* t) {
+  const int es = elem_size(t->dtype);
+  if (t->stride[t->ndim - 1] != 1) return false;
+  for (int i = 0; i < t->ndim - 1; ++i)
+    if ((t->stride[i] * es) % 16 != 0) return false;
+  return true;
+}
+
+va_status check_descale(const va_tensor* t) {
+  if (!t) return VA_OK;
+  if (t->ndim < 0 || t->ndim > 4) return VA_ERR_SHAPE;
+  if (t->dtype != VA_FP32) return VA_ERR_DTYPE;
+  for (int i = 0; i < t->ndim; ++i)
+    if (t->shape[i] < 0) return VA_ERR_SHAPE;
+  if (numel(t) != 1) return VA_ERR_SHAPE;
+  if (!t->data) return VA_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(t->data) & 3u) != 0) return VA_ERR_LAYOUT;
+  return VA_OK;
+}
+
+va_status validate(const va_tensor* q, const va_tensor* k, const va_tensor* v,
+                   const va_tensor* bt, const va_tensor* cu, const va_tensor* su,
+                   int32_t max_seqlen_q, int32_t max_seqlen_k, const va_tensor* kd,
+                   const va_tensor* vd, const va_tensor* out, Shapes* sh) {
+  if (!q || !k || !v || !bt || !cu || !su || !out) return VA_ERR_NULL;
+  if (!dims_ok(q, 3) || !dims_ok(k, 4) || !dims_ok(v, 4) || !dims_ok(bt, 2) || !dims_ok(cu, 1) ||
+      !dims_ok(su, 1) || !dims_ok(out, 3))
+    return VA_ERR_SHAPE;
+  if (q->dtype != VA_BF16 || out->dtype != VA_BF16) return VA_ERR_DTYPE;
+  if (k->dtype != VA_FP8_E4M3 && k->dtype != VA_BF16) return VA_ERR_DTYPE;
+  if (v->dtype != k->dtype) return VA_ERR_DTYPE;
+  if (bt->dtype != VA_INT32 || cu->dtype != VA_INT32 || su->dtype != VA_INT32) return VA_ERR_DTYPE;
+
+  // Shape gate (sglang PR 36330 digest, aiter_backend.py excerpt): head size
+  // 256, page size 16, Hk == Hv; Hq % Hkv == 0 (same digest, review notes).
+  if (q->shape[2] != kHeadDim || k->shape[3] != kHeadDim) return VA_ERR_UNSUPPORTED;
+  if (k->shape[1] != kPageSize) return VA_ERR_UNSUPPORTED;
+  for (int i = 0; i < 4; ++i)
+    if (v->shape[i] != k->shape[i]) return VA_ERR_SHAPE;
+  for (int i = 0; i < 3; ++i)
+    if (out->shape[i] != q->shape[i]) return VA_ERR_SHAPE;
+  const int64_t hq = q->shape[1], hkv = k->shape[2];
+  if (hq < 1 || hkv < 1) return VA_ERR_SHAPE;
+  if (hq % hkv != 0) return VA_ERR_SHAPE;
+  const int64_t B = su->shape[0];
+  if (cu->shape[0] != B + 1 || bt->shape[0] != B) return VA_ERR_SHAPE;
+  if (max_seqlen_q < 1 || max_seqlen_k < 0) return VA_ERR_UNSUPPORTED;
+  if ((hq / hkv) * (int64_t)max_seqlen_q > kMaxRows) return VA_ERR_UNSUPPORTED;
+  if (B > 0 && bt->shape[1] * kPageSize < (int64_t)max_seqlen_k) return VA_ERR_SHAPE;
+  if (q->shape[0] > INT32_MAX || k->shape[0] > INT32_MAX || B * hkv > INT32_MAX / 2 ||
+      bt->shape[1] > INT32_MAX / kPageSize)
+    return VA_ERR_UNSUPPORTED;
+
+  // Layout: innermost stride 1, 16-byte rows (what 16-byte vector and bulk
+  // copies need), contiguous index vectors.
+  if (!rows_16b(q) || !rows_16b(out) || !rows_16b(k) || !rows_16b(v)) return VA_ERR_LAYOUT;
+  if (cu->stride[0] != 1 || su->stride[0] != 1) return VA_ERR_LAYOUT;
+
+  const bool has_q = numel(q) > 0;
+  if (has_q && (!q->data || !out->data)) return VA_ERR_NULL;
+  if (numel(k) > 0 && (!k->data || !v->data)) return VA_ERR_NULL;
+  if (!cu->data) return VA_ERR_NULL;
+  if (B > 0 && !su->data) return VA_ERR_NULL;
+  if (numel(bt) > 0 && !bt->data) return VA_ERR_NULL;
+  if ((q->data && !aligned16(q->data)) || (out->data && !aligned16(out->data)) ||
+      (k->data && !aligned16(k->data)) || (v->data && !aligned16(v->data)))
+    return VA_ERR_LAYOUT;
+  va_status s = check_descale(kd);
+  if (s != VA_OK) return s;
+  s = check_descale(vd);
+  if (s != VA_OK) return s;
+
+  sh->total_q = q->shape[0];
+  sh->hq = hq;
+  sh->hkv = hkv;
+  sh->num_blocks = k->shape[0];
+  sh->num_seqs = B;
+  sh->width = bt->shape[1];
+  sh->kv_dtype = k->dtype;
+  return VA_OK;
+}
+
+va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t max_k, int32_t kv_dtype,
+                    int32_t num_sms, int32_t force, va_plan* plan) {
+  if (!plan) return VA_ERR_NULL;
+  if (B < 0 || hkv < 1 || hq < 1 || hq % hkv != 0 || max_q < 1 || max_k < 0 || num_sms < 1)
+    return VA_ERR_UNSUPPORTED;
+  if (kv_dtype != VA_FP8_E4M3 && kv_dtype != VA_BF16) return VA_ERR_UNSUPPORTED;
+  const int64_t G = hq / hkv;
+  if (G * max_q > kMaxRows) return VA_ERR_UNSUPPORTED;
+  const int tile = kSimtTileKeys;
+  const int64_t J = B * hkv;
+  const int64_t tiles_bound = J * ((max_k + tile - 1) / tile);
+  if (tiles_bound > INT32_MAX / 2) return VA_ERR_UNSUPPORTED;
+  // Heuristic: every SM gets one CTA (the main kernel keeps one CTA per SM),
+  // but no CTA gets fewer than kMinTiles tiles of the upper-bound workload,
+  // so small batches do not pay a merge for nothing.
+  constexpr int64_t kMinTiles = 4;
+  int64_t splits;
+  if (force > 0) {
+    splits = force;
+    if (splits > tiles_bound) splits = tiles_bound;
+  } else {
+    splits = (tiles_bound + kMinTiles - 1) / kMinTiles;
+    if (splits > num_sms) splits = num_sms;
+  }
+  if (splits < 1) splits = 1;
+  std::memset(plan, 0, sizeof(*plan));
+  plan->tile_keys = tile;
+  plan->num_splits = (int32_t)splits;
+  plan->max_rows = (int32_t)(G * max_q);
+  plan->num_work = (int32_t)J;
+  plan->kernel = kKernelSimt;
+  plan->workspace_bytes = (int64_t)workspace_layout(J, splits, G * max_q).total;
+  return VA_OK;
+}
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// Current device's state, initialised once (SM count, kernel attributes).
+// Caller holds g_mu.
+va_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return VA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return VA_ERR_UNSUPPORTED;
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return VA_ERR_CUDA;
+    if (prepare_main_simt() != cudaSuccess) return VA_ERR_CUDA;
+    st.ready = true;
+  }
+  *out = &st;
+  return VA_OK;
+}
+
+va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, const va_tensor* bt,
+                 const va_tensor* cu, const va_tensor* su, int32_t max_q, int32_t max_k,
+                 float scale, const va_tensor* kd, const va_tensor* vd, va_tensor* out,
+                 const Shapes& sh, const va_plan& plan, void* ws, size_t ws_bytes,
+                 cudaStream_t stream) {
+  if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;  // no output rows
+  if ((size_t)plan.workspace_bytes > ws_bytes || !ws) return VA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return VA_ERR_WORKSPACE;
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const uint16_t*>(q->data);
+  p.q_s0 = q->stride[0];
+  p.q_s1 = q->stride[1];
+  p.k = k->data;
+  p.k_s0 = k->stride[0];
+  p.k_s1 = k->stride[1];
+  p.k_s2 = k->stride[2];
+  p.v = v->data;
+  p.v_s0 = v->stride[0];
+  p.v_s1 = v->stride[1];
+  p.v_s2 = v->stride[2];
+  p.block_table = static_cast<const int32_t*>(bt->data);
+  p.bt_s0 = bt->stride[0];
+  p.bt_s1 = bt->stride[1];
+  p.bt_width = (int32_t)sh.width;
+  p.cu_q = static_cast<const int32_t*>(cu->data);
+  p.seqused_k = static_cast<const int32_t*>(su->data);
+  p.k_descale = kd ? static_cast<const float*>(kd->data) : nullptr;
+  p.v_descale = vd ? static_cast<const float*>(vd->data) : nullptr;
+  p.out = static_cast<uint16_t*>(out->data);
+  p.o_s0 = out->stride[0];
+  p.o_s1 = out->stride[1];
+  p.num_seqs = (int32_t)sh.num_seqs;
+  p.hq = (int32_t)sh.hq;
+  p.hkv = (int32_t)sh.hkv;
+  p.group = (int32_t)(sh.hq / sh.hkv);
+  p.num_blocks = (int32_t)sh.num_blocks;
+  p.total_q = (int32_t)sh.total_q;
+  p.max_seqlen_q = max_q;
+  p.max_seqlen_k = max_k;
+  p.kv_fp8 = sh.kv_dtype == VA_FP8_E4M3 ? 1 : 0;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.tile_keys = plan.tile_keys;
+  p.num_splits = plan.num_splits;
+  p.max_rows = plan.max_rows;
+  p.num_work = plan.num_work;
+  const WorkspaceLayout lay = workspace_layout(plan.num_work, plan.num_splits, plan.max_rows);
+  char* base = static_cast<char*>(ws);
+  p.ws_meta = reinterpret_cast<int32_t*>(base + lay.meta_off);
+  p.ws_ml = reinterpret_cast<float*>(base + lay.ml_off);
+  p.ws_acc = reinterpret_cast<float*>(base + lay.acc_off);
+  if (launch_main_simt(p, stream) != cudaSuccess) return VA_ERR_CUDA;
+  if (launch_merge(p, stream) != cudaSuccess) return VA_ERR_CUDA;
+  return VA_OK;
+}
+
+}  // namespace
+
+VA_EXPORT va_status verify_attn_check(const va_tensor* q, const va_tensor* k_cache,
+                                      const va_tensor* v_cache, const va_tensor* block_table,
+                                      const va_tensor* cu_seqlens_q, const va_tensor* seqused_k,
+                                      int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                      const va_tensor* k_descale, const va_tensor* v_descale,
+                                      const va_tensor* out) {
+  Shapes sh;
+  return validate(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
+                  max_seqlen_k, k_descale, v_descale, out, &sh);
+}
+
+VA_EXPORT va_status verify_attn_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
+                                     int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t kv_dtype,
+                                     int32_t num_sms, int32_t force_splits, va_plan* plan) {
+  return make_plan(num_seqs, num_kv_heads, num_q_heads, max_seqlen_q, max_seqlen_k, kv_dtype,
+                   num_sms, force_splits, plan);
+}
+
+VA_EXPORT size_t verify_attn_workspace_size(int32_t num_seqs, int32_t num_kv_heads,
+                                            int32_t num_q_heads, int32_t max_seqlen_q,
+                                            int32_t max_seqlen_k, int32_t kv_dtype,
+                                            int32_t num_splits) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  if (device_state(&st) != VA_OK) return 0;
+  va_plan plan;
+  if (make_plan(num_seqs, num_kv_heads, num_q_heads, max_seqlen_q, max_seqlen_k, kv_dtype, st->sms,
+                num_splits, &plan) != VA_OK)
+    return 0;
+  return (size_t)plan.workspace_bytes;
+}
+
+VA_EXPORT va_status verify_attn_ex(const va_tensor* q, const va_tensor* k_cache,
+                                   const va_tensor* v_cache, const va_tensor* block_table,
+                                   const va_tensor* cu_seqlens_q, const va_tensor* seqused_k,
+                                   int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
+                                   const va_tensor* k_descale, const va_tensor* v_descale,
+                                   va_tensor* out, void* workspace, size_t workspace_bytes,
+                                   int32_t num_splits, void* stream) {
+  Shapes sh;
+  va_status s = validate(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
+                         max_seqlen_k, k_descale, v_descale, out, &sh);
+  if (s != VA_OK) return s;
+  if (num_splits < 0) return VA_ERR_UNSUPPORTED;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* st = nullptr;
+    s = device_state(&st);
+    if (s != VA_OK) return s;
+    sms = st->sms;
+  }
+  va_plan plan;
+  s = make_plan(sh.num_seqs, sh.hkv, sh.hq, max_seqlen_q, max_seqlen_k, sh.kv_dtype, sms,
+                num_splits, &plan);
+  if (s != VA_OK) return s;
+  return launch(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
+                max_seqlen_k, softmax_scale, k_descale, v_descale, out, sh, plan, workspace,
+                workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+VA_EXPORT va_status verify_attn(const va_tensor* q, const va_tensor* k_cache,
+                                const va_tensor* v_cache, const va_tensor* block_table,
+                                const va_tensor* cu_seqlens_q, const va_tensor* seqused_k,
+                                int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
+                                const va_tensor* k_descale, const va_tensor* v_descale,
+                                va_tensor* out, void* stream) {
+  Shapes sh;
+  va_status s = validate(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
+                         max_seqlen_k, k_descale, v_descale, out, &sh);
+  if (s != VA_OK) return s;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  s = device_state(&st);
+  if (s != VA_OK) return s;
+  va_plan plan;
+  s = make_plan(sh.num_seqs, sh.hkv, sh.hq, max_seqlen_q, max_seqlen_k, sh.kv_dtype, st->sms, 0,
+                &plan);
+  if (s != VA_OK) return s;
+  if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;
+  if ((size_t)plan.workspace_bytes > st->ws_bytes) {
+    // Grow only. cudaFree waits for work already queued on the old buffer.
+    if (st->ws) cudaFree(st->ws);
+    st->ws = nullptr;
+    st->ws_bytes = 0;
+    if (cudaMalloc(&st->ws, (size_t)plan.workspace_bytes) != cudaSuccess) {
+      st->ws = nullptr;
+      return VA_ERR_CUDA;
+    }
+    st->ws_bytes = (size_t)plan.workspace_bytes;
+  }
+  return launch(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
+                max_seqlen_k, softmax_scale, k_descale, v_descale, out, sh, plan, st->ws,
+                st->ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+VA_EXPORT const char* verify_attn_status_string(int32_t status) {
+  switch (status) {
+    case VA_OK: return "VA_OK";
+    case VA_ERR_NULL: return "VA_ERR_NULL: a required pointer or descriptor is NULL";
+    case VA_ERR_SHAPE: return "VA_ERR_SHAPE: tensor shapes disagree";
+    case VA_ERR_DTYPE: return "VA_ERR_DTYPE: wrong element type";
+    case VA_ERR_UNSUPPORTED: return "VA_ERR_UNSUPPORTED: outside what the kernels cover";
+    case VA_ERR_WORKSPACE: return "VA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case VA_ERR_CUDA: return "VA_ERR_CUDA: a CUDA call or launch failed";
+    case VA_ERR_LAYOUT: return "VA_ERR_LAYOUT: unsupported stride or alignment";
+    default: return "unknown va_status";
+  }
+}

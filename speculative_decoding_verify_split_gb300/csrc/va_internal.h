@@ -1,0 +1,72 @@
+// Internal launch parameters shared by the host library and the kernels.
+// Not part of the C ABI (include/verify_attn.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace va {
+
+constexpr int kHeadDim = 256;
+constexpr int kPageSize = 16;
+constexpr int kMaxRows = 64;  // G * max_seqlen_q packed rows per (sequence, KV head)
+
+// Everything a kernel needs, by value. Strides are in elements.
+struct Params {
+  const uint16_t* q;  // bf16 bits
+  int64_t q_s0, q_s1;
+  const void* k;
+  int64_t k_s0, k_s1, k_s2;
+  const void* v;
+  int64_t v_s0, v_s1, v_s2;
+  const int32_t* block_table;
+  int64_t bt_s0, bt_s1;
+  int32_t bt_width;
+  const int32_t* cu_q;
+  const int32_t* seqused_k;
+  const float* k_descale;  // nullable
+  const float* v_descale;  // nullable
+  uint16_t* out;           // bf16 bits
+  int64_t o_s0, o_s1;
+  int32_t num_seqs, hq, hkv, group, num_blocks, total_q, max_seqlen_q, max_seqlen_k;
+  int32_t kv_fp8;
+  float scale_log2;  // softmax_scale * log2(e)
+
+  // Split-KV decomposition: one stream of key tiles over all work items
+  // j = b * hkv + kvh, cut into num_splits equal ranges (one per CTA).
+  int32_t tile_keys, num_splits, max_rows, num_work;
+  int32_t* ws_meta;  // [num_work + 1]: first tile of each work item, then the total
+  float* ws_ml;      // [pieces][max_rows][2]: running max (log2 units), row sum
+  float* ws_acc;     // [pieces][max_rows][256]: unnormalised output rows
+};
+
+// Workspace layout. pieces = num_work + num_splits: a work item split over
+// CTAs c0..c1 stores the partial of CTA c at piece j + c, which is unique
+// because consecutive work items share at most one CTA.
+struct WorkspaceLayout {
+  size_t meta_off, ml_off, acc_off, total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WorkspaceLayout workspace_layout(int64_t num_work, int64_t num_splits, int64_t max_rows) {
+  WorkspaceLayout w;
+  const int64_t pieces = num_work + num_splits;
+  w.meta_off = 0;
+  w.ml_off = align_up(sizeof(int32_t) * (size_t)(num_work + 1), 256);
+  w.acc_off = w.ml_off + align_up(sizeof(float) * 2 * (size_t)(pieces * max_rows), 256);
+  w.total = w.acc_off + align_up(sizeof(float) * kHeadDim * (size_t)(pieces * max_rows), 256);
+  return w;
+}
+
+// Main-kernel variants.
+enum Kernel : int32_t { kKernelSimt = 0 };
+constexpr int kSimtTileKeys = 32;
+
+cudaError_t prepare_main_simt();  // once per device: opt in to its shared memory
+cudaError_t launch_main_simt(const Params& p, cudaStream_t stream);
+cudaError_t launch_merge(const Params& p, cudaStream_t stream);
+
+}  // namespace va

@@ -1,0 +1,133 @@
+// Device helpers for the split-KV decomposition shared by the main and merge
+// kernels: per-sequence lengths (clamped so no access leaves its buffer), the
+// key-tile count of each (sequence, KV head) work item, and the mapping from a
+// global key tile to the CTA whose equal share contains it.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "va_internal.h"
+
+namespace va {
+
+// Draft tokens of sequence b, clamped to [0, max_seqlen_q] and to the rows of q.
+__device__ __forceinline__ int seq_q_len(const Params& p, int b) {
+  const int a = p.cu_q[b];
+  const int e = p.cu_q[b + 1];
+  int L = e - a;
+  L = L < 0 ? 0 : L;
+  L = L > p.max_seqlen_q ? p.max_seqlen_q : L;
+  if (a < 0) return 0;
+  const int room = p.total_q - a;
+  return L > room ? (room < 0 ? 0 : room) : L;
+}
+
+// Cached tokens of sequence b, clamped to what its block-table row can address.
+__device__ __forceinline__ int seq_kv_len(const Params& p, int b) {
+  int S = p.seqused_k[b];
+  S = S < 0 ? 0 : S;
+  const int cap = p.bt_width * kPageSize;
+  return S > cap ? cap : S;
+}
+
+// Key tiles of work item j (b = j / hkv). A sequence without draft tokens
+// needs no work.
+__device__ __forceinline__ int work_tiles(const Params& p, int j) {
+  const int b = j / p.hkv;
+  if (seq_q_len(p, b) == 0) return 0;
+  return (seq_kv_len(p, b) + p.tile_keys - 1) / p.tile_keys;
+}
+
+// First global tile of CTA c when N tiles are cut into G equal ranges.
+__device__ __forceinline__ long long split_begin(long long N, int c, int G) {
+  return (N * (long long)c) / G;
+}
+
+// The CTA whose range contains tile x (0 <= x < N): the largest c with
+// split_begin(c) <= x, i.e. c*N < (x+1)*G.
+__device__ __forceinline__ int split_of(long long x, long long N, int G) {
+  return (int)(((x + 1) * (long long)G - 1) / N);
+}
+
+// Block-wide exclusive scan of one value per thread (NT threads, NT % 32 == 0).
+// Returns the exclusive prefix; *total receives the block sum. Uses 32 slots
+// of shared scratch; contains __syncthreads.
+template <int NT>
+__device__ __forceinline__ long long block_exclusive_scan(long long v, long long* scratch,
+                                                          long long* total) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = lane < NT / 32 ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    scratch[lane] = w;
+  }
+  __syncthreads();
+  const long long base = warp > 0 ? scratch[warp - 1] : 0;
+  *total = scratch[NT / 32 - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+// Scans the tile counts of all work items. When write_meta, stores the first
+// tile of every item in ws_meta and the total at ws_meta[num_work]. Returns
+// the total tile count N.
+template <int NT>
+__device__ long long scan_work(const Params& p, long long* scratch, bool write_meta) {
+  long long running = 0;
+  for (int base = 0; base < p.num_work; base += NT) {
+    const int j = base + (int)threadIdx.x;
+    const long long v = j < p.num_work ? work_tiles(p, j) : 0;
+    long long tot;
+    const long long ex = block_exclusive_scan<NT>(v, scratch, &tot);
+    if (write_meta && j < p.num_work) p.ws_meta[j] = (int32_t)(running + ex);
+    running += tot;
+  }
+  if (write_meta && threadIdx.x == 0) p.ws_meta[p.num_work] = (int32_t)running;
+  return running;
+}
+
+// Finds the work item containing global tile x (0 <= x < N) and its first
+// tile. Every thread gets the answer.
+template <int NT>
+__device__ void find_work(const Params& p, long long x, long long* scratch, int* s_j,
+                          long long* s_ts, int* out_j, long long* out_ts) {
+  long long running = 0;
+  for (int base = 0; base < p.num_work; base += NT) {
+    const int j = base + (int)threadIdx.x;
+    const long long v = j < p.num_work ? work_tiles(p, j) : 0;
+    long long tot;
+    const long long ex = block_exclusive_scan<NT>(v, scratch, &tot);
+    const long long s = running + ex;
+    if (j < p.num_work && v > 0 && s <= x && x < s + v) {
+      *s_j = j;
+      *s_ts = s;
+    }
+    running += tot;
+  }
+  __syncthreads();
+  *out_j = *s_j;
+  *out_ts = *s_ts;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+}  // namespace va

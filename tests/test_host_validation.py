@@ -1,0 +1,119 @@
+"""Host-only checks of the boundary: the validation matrix (each shape gate
+of the pages turned into a status code) and the split heuristic. No CUDA
+call is made: verify_attn_check and verify_attn_plan are pure host code."""
+import pytest
+import torch
+
+import speculative_decoding_verify_split_gb300 as va
+from speculative_decoding_verify_split_gb300.build import build_library
+from speculative_decoding_verify_split_gb300.workloads import make_workload
+
+OK, NULL, SHAPE, DTYPE, UNSUP, WS, CUDA, LAYOUT = range(8)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build_library()
+
+
+def _args(w, **over):
+    a = dict(q=w.q, k_cache=w.k_cache, v_cache=w.v_cache, block_table=w.block_table,
+             cu_seqlens_q=w.cu_seqlens_q, seqused_k=w.seqused_k, max_seqlen_q=w.max_seqlen_q,
+             max_seqlen_k=w.max_seqlen_k, k_descale=w.k_descale, v_descale=w.v_descale,
+             out=torch.empty_like(w.q))
+    a.update(over)
+    return a
+
+
+@pytest.fixture(scope="module")
+def w():
+    return make_workload([4, 2], [100, 37], 16, 1, "fp8_e4m3", seed=1, k_descale=1.0, v_descale=2.0)
+
+
+def test_valid(w):
+    assert va.check(**_args(w)) == OK
+
+
+def test_valid_bf16_and_gqa():
+    w2 = make_workload([2, 3], [50, 70], 32, 2, "bf16", seed=2)
+    assert va.check(**_args(w2)) == OK
+
+
+def test_null_descriptor(w):
+    assert va.check(**_args(w, q=None)) == NULL
+    assert va.check(**_args(w, out=None)) == NULL
+    assert va.check(**_args(w, block_table=None)) == NULL
+
+
+def test_dtypes(w):
+    assert va.check(**_args(w, q=w.q.view(torch.int16).to(torch.int32))) == DTYPE
+    assert va.check(**_args(w, v_cache=w.v_cache.to(torch.bfloat16))) == DTYPE
+    assert va.check(**_args(w, block_table=w.block_table.float())) == DTYPE
+    assert va.check(**_args(w, k_descale=torch.ones(1, dtype=torch.int32))) == DTYPE
+
+
+def test_head_dim_and_page_size_are_gated(w):
+    k = w.k_cache[..., :128].contiguous()
+    assert va.check(**_args(w, k_cache=k, v_cache=k)) == UNSUP
+    k8 = w.k_cache.reshape(-1, 8, 1, 256)
+    assert va.check(**_args(w, k_cache=k8, v_cache=k8)) == UNSUP
+    q = w.q[..., :128].contiguous()
+    assert va.check(**_args(w, q=q, out=torch.empty_like(q))) == UNSUP
+
+
+def test_head_ratio(w):
+    q = torch.zeros(w.q.shape[0], 12, 256, dtype=torch.bfloat16)
+    k = torch.zeros(4, 16, 8, 256, dtype=torch.float8_e4m3fn)
+    assert va.check(**_args(w, q=q, out=torch.empty_like(q), k_cache=k, v_cache=k)) == SHAPE
+
+
+def test_row_budget(w):
+    assert va.check(**_args(w, max_seqlen_q=5)) == UNSUP      # 16 * 5 > 64
+    assert va.check(**_args(w, max_seqlen_q=0)) == UNSUP
+    assert va.check(**_args(w, max_seqlen_k=-1)) == UNSUP
+
+
+def test_shapes(w):
+    assert va.check(**_args(w, cu_seqlens_q=w.cu_seqlens_q[:2])) == SHAPE
+    assert va.check(**_args(w, block_table=w.block_table[:1])) == SHAPE
+    assert va.check(**_args(w, max_seqlen_k=w.block_table.shape[1] * 16 + 1)) == SHAPE
+    assert va.check(**_args(w, out=torch.empty(w.q.shape[0], 8, 256, dtype=torch.bfloat16))) == SHAPE
+    assert va.check(**_args(w, v_descale=torch.ones(2))) == SHAPE
+
+
+def test_layout(w):
+    big = torch.zeros(w.q.shape[0], w.q.shape[1], 512, dtype=torch.bfloat16)
+    q_strided = big[..., ::2]
+    assert va.check(**_args(w, q=q_strided, out=torch.empty_like(w.q))) == LAYOUT
+    q_padded = big[..., :256]                       # head stride 512: still 16-byte rows
+    assert va.check(**_args(w, q=q_padded, out=torch.empty_like(w.q))) == OK
+    odd = torch.zeros(w.q.numel() + 1, dtype=torch.bfloat16)[1:].view(w.q.shape)
+    assert va.check(**_args(w, q=odd, out=torch.empty_like(w.q))) == LAYOUT
+
+
+def test_plan_fills_the_sms():
+    p = va.plan(16, 1, 16, 4, 131072, "fp8_e4m3", 152)
+    assert p["num_splits"] == 152 and p["max_rows"] == 64 and p["num_work"] == 16
+    assert p["workspace_bytes"] >= (16 + 152) * 64 * 256 * 4
+
+
+def test_plan_small_batches_use_few_splits():
+    p = va.plan(1, 1, 16, 2, 16, "fp8_e4m3", 152)
+    assert p["num_splits"] == 1
+    p = va.plan(2, 1, 16, 4, 1024, "fp8_e4m3", 152)
+    assert 1 <= p["num_splits"] <= 152
+    assert p["num_splits"] * 4 * p["tile_keys"] >= 2 * 1024 - 4 * p["tile_keys"]
+
+
+def test_plan_force_and_clamp():
+    assert va.plan(2, 1, 16, 4, 1024, "fp8_e4m3", 152, force_splits=7)["num_splits"] == 7
+    tiles = 2 * (1024 // 32)
+    assert va.plan(2, 1, 16, 4, 1024, "fp8_e4m3", 152, force_splits=10**6)["num_splits"] == tiles
+    assert va.plan(3, 1, 16, 4, 0, "fp8_e4m3", 152)["num_splits"] == 1
+
+
+def test_plan_rejects():
+    for bad in [(1, 1, 16, 5, 100, "fp8_e4m3", 152), (1, 3, 16, 1, 100, "fp8_e4m3", 152),
+                (1, 1, 16, 1, 100, "fp8_e4m3", 0), (1, 1, 16, 0, 100, "bf16", 152)]:
+        with pytest.raises(va.VerifyAttnError):
+            va.plan(*bad)
