@@ -1,0 +1,387 @@
+#!/usr/bin/env python
+"""Benchmark of target-verify attention (split-KV main kernel + segment merge).
+
+One step = one verify_attn call over the whole batch of the long-context FP8
+verify workload (16 sequences, 4 draft tokens, kv_len U[65536, 131072],
+16 query heads per KV head, head_dim 256, page 16, FP8 E4M3 KV), inputs
+resident in HBM. The inputs (~0.8 GB) exceed the 129 MB L2, so no flush is
+needed between steps.
+
+Prints one JSON line. ``value`` = algorithmic bytes (K+V read once per KV
+head, plus Q and out) of all ranks / max-over-ranks time, in GB/s.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+Multi-GPU runs are independent replicas (the operation has no exchange step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify-attn µs/call and achieved HBM GB/s (fraction of ~8 TB/s) on 1 GB300"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+MAIN_KERNEL = "va_main_simt_kernel"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long_context_fp8")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def env_int(name, default):
+    v = os.environ.get(name)
+    return int(v) if v is not None else default
+
+
+def peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verify_split_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per main-kernel launch from a committed ncu summary, only if
+    it was taken on the kernel sources as they are now."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(p) as f:
+            recs = json.load(f)
+    except Exception:
+        return None
+    sha = kernel_source_sha()
+    for r in recs:
+        if r.get("workload") == workload and r.get("kernel_source_sha") == sha:
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_id), "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def gpu_identifier(torch, dev):
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return dev
+
+
+def workload_config(w, name, world):
+    return {"workload": name, "num_seqs": w.num_seqs, "q_lens": sorted(set(w.q_lens)),
+            "kv_len_range": [min(w.kv_lens), max(w.kv_lens)], "kv_tokens": sum(w.kv_lens),
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": 256,
+            "page_size": 16, "kv_dtype": w.kv_dtype, "algorithmic_bytes": w.algorithmic_bytes(),
+            "l2": "inputs exceed the 129 MB L2; no flush between steps",
+            "parallelism": f"replicas x{world}", "seed": 0}
+
+
+def cpu_baseline(w_cpu, seconds):
+    """The fp64 oracle as it stands, on sequences of the workload in order,
+    until `seconds` of wall time have passed (at least one sequence)."""
+    from oracle.attention_fp64 import oracle_from_torch
+    done, nbytes = [], 0
+    e = 1 if w_cpu.kv_dtype == "fp8_e4m3" else 2
+    t0 = time.perf_counter()
+    c0 = time.process_time()
+    for b in range(w_cpu.num_seqs):
+        oracle_from_torch(w_cpu, [b])
+        done.append(b)
+        nbytes += (w_cpu.kv_lens[b] * w_cpu.num_kv_heads * 256 * 2 * e
+                   + 2 * w_cpu.q_lens[b] * w_cpu.num_q_heads * 256 * 2)
+        if time.perf_counter() - t0 >= seconds:
+            break
+    wall = time.perf_counter() - t0
+    cpu = time.process_time() - c0
+    return {"value": nbytes / wall / 1e9, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle", "cpu_time_over_wall": round(cpu / wall, 2),
+            "sample": f"{len(done)} of {w_cpu.num_seqs} sequences ({sum(w_cpu.kv_lens[b] for b in done)} "
+                      f"keys), fp64 numpy, {wall:.1f} s wall"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = env_int("RANK", 0), env_int("WORLD_SIZE", 1), env_int("LOCAL_RANK", 0)
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        from speculative_decoding_verify_split_gb300.build import build_library
+        build_library()
+    if world > 1:
+        dist.barrier()
+    import speculative_decoding_verify_split_gb300 as va
+    from speculative_decoding_verify_split_gb300.workloads import named_workload
+
+    w = named_workload(args.workload, seed=0, value_device=str(dev)).to(dev)
+    alg = w.algorithmic_bytes()
+    out = torch.empty_like(w.q)
+    n_ws = va.workspace_size(w.q, w.k_cache, w.seqused_k, w.max_seqlen_q, w.max_seqlen_k)
+    ws = torch.empty(n_ws + 256, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev_mid=None):
+        va.run_workload_ex(w, out=out, workspace=ws, stream=stream, event_after_main=ev_mid)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_identifier(torch, local))
+    sampler.start()
+    time.sleep(0.3)
+    K = args.steps
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in e1:
+        e.record(stream)
+    ev_a = torch.cuda.Event(enable_timing=True)
+    ev_b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev_a.record(stream)
+    for i in range(K):
+        e0[i].record(stream)
+        step(e1[i])
+    ev_b.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = ev_a.elapsed_time(ev_b)
+    main_ms = statistics.mean(e0[i].elapsed_time(e1[i]) for i in range(K))
+    # keep the GPU busy a little longer so the clock sampler sees the load
+    t_end = time.time() + 1.0
+    while time.time() < t_end:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+    clocks = sampler.stop()
+
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = alg * world / (total_ms / 1e3) / 1e9
+
+    # End to end through the public API with host buffers: every step copies
+    # all inputs from pinned host memory and reads the output back.
+    host = {k: getattr(w, k).cpu().pin_memory() for k in
+            ("q", "k_cache", "v_cache", "block_table", "cu_seqlens_q", "seqused_k")}
+    for k in ("k_descale", "v_descale"):
+        if getattr(w, k) is not None:
+            host[k] = getattr(w, k).cpu().pin_memory()
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k, t in host.items():
+            getattr(w, k).copy_(t, non_blocking=True)
+        va.run_workload(w, out=out, stream=stream)
+        out_host.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    E = max(args.e2e_steps, 3)
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    ea.record(stream)
+    for _ in range(E):
+        e2e_step()
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb) / E
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peak, peak_src = peak_hbm()
+    achieved = alg / (main_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w, args.workload, world),
+        "us_per_call": round(ms_per_step * 1e3, 2),
+        "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "main_kernel_us": round(main_ms * 1e3, 2),
+        "roofline": {"bound": "hbm", "kernel": MAIN_KERNEL, "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_src} (HBM copy bandwidth)",
+                     "traffic": recorded_traffic(args.workload),
+                     "bytes_per_launch": alg},
+        "e2e": {"value": round(alg * world / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        w_cpu = w.to("cpu")
+        line["cpu_baseline"] = cpu_baseline(w_cpu, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle on the host cores: each step is one sequence of the workload's
+    shape (its q_len and heads), with the KV length capped so the whole run
+    stays within a few minutes."""
+    rank = env_int("RANK", 0)
+    if rank != 0:
+        return
+    from oracle.attention_fp64 import oracle_from_torch
+    from speculative_decoding_verify_split_gb300.workloads import make_workload, workload_structure
+
+    st = workload_structure(args.workload, 0)
+    q_lens, kv_lens = st["q_lens"], st["kv_lens"]
+    e = 1 if st["kv_dtype"] == "fp8_e4m3" else 2
+
+    def sample(b, cap, seed):
+        S = min(kv_lens[b], cap)
+        w = make_workload([q_lens[b]], [S], st["Hq"], st["Hkv"], st["kv_dtype"], seed=seed)
+        nbytes = S * st["Hkv"] * 256 * 2 * e + 2 * q_lens[b] * st["Hq"] * 256 * 2
+        return w, nbytes
+
+    # calibrate the cap so that all steps fit in about two minutes
+    w, nb = sample(0, 4096, 1000)
+    t = time.perf_counter()
+    oracle_from_torch(w)
+    rate = nb / (time.perf_counter() - t)
+    budget = max(0.05, min(20.0, 120.0 / (args.steps + args.warmup)))
+    cap = int(max(256, min(max(kv_lens), budget * rate / (st["Hkv"] * 512 * e))))
+
+    times, nbytes_total = [], 0
+    for i in range(args.warmup + args.steps):
+        b = i % len(kv_lens)
+        w, nb = sample(b, cap, 2000 + i)
+        t = time.perf_counter()
+        oracle_from_torch(w)
+        dt = time.perf_counter() - t
+        if i >= args.warmup:
+            times.append(dt)
+            nbytes_total += nb
+    total = sum(times)
+    value = nbytes_total / total / 1e9
+    cores = len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "num_seqs": len(q_lens), "q_len": q_lens[0],
+                       "num_q_heads": st["Hq"], "num_kv_heads": st["Hkv"], "head_dim": 256,
+                       "page_size": 16, "kv_dtype": st["kv_dtype"]},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step one sequence of the workload's shape with kv_len "
+                                       f"capped at {cap}"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -136,6 +136,9 @@ va_status verify_attn(const va_tensor* q, const va_tensor* k_cache, const va_ten
  *                  when that size is 0.
  * num_splits       0 = the heuristic's choice; > 0 forces the main kernel's
  *                  CTA count (clamped to the number of key tiles it could have).
+ * event_after_main NULL, or a cudaEvent_t recorded on `stream` between the
+ *                  main and the merge kernel (lets a caller time the main
+ *                  kernel alone with CUDA events on the launching stream).
  * The workspace holds no state between calls.
  */
 va_status verify_attn_ex(const va_tensor* q, const va_tensor* k_cache, const va_tensor* v_cache,
@@ -143,7 +146,8 @@ va_status verify_attn_ex(const va_tensor* q, const va_tensor* k_cache, const va_
                          const va_tensor* seqused_k, int32_t max_seqlen_q, int32_t max_seqlen_k,
                          float softmax_scale, const va_tensor* k_descale,
                          const va_tensor* v_descale, va_tensor* out, void* workspace,
-                         size_t workspace_bytes, int32_t num_splits, void* stream);
+                         size_t workspace_bytes, int32_t num_splits, void* event_after_main,
+                         void* stream);
 
 /*
  * verify_attn_check - validation only: the same checks verify_attn runs before

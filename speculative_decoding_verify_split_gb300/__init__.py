@@ -65,7 +65,8 @@ def _lib():
         lib.verify_attn.argtypes = tens + [ctypes.c_float, P, P, P, ctypes.c_void_p]
         lib.verify_attn.restype = ctypes.c_int32
         lib.verify_attn_ex.argtypes = tens + [ctypes.c_float, P, P, P, ctypes.c_void_p,
-                                              ctypes.c_size_t, ctypes.c_int32, ctypes.c_void_p]
+                                              ctypes.c_size_t, ctypes.c_int32, ctypes.c_void_p,
+                                              ctypes.c_void_p]
         lib.verify_attn_ex.restype = ctypes.c_int32
         lib.verify_attn_check.argtypes = tens + [P, P, P]
         lib.verify_attn_check.restype = ctypes.c_int32
@@ -112,6 +113,14 @@ def _stream_handle(stream, device) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _event_handle(ev) -> int:
+    if ev is None:
+        return 0
+    if ev.cuda_event == 0:      # torch creates the CUDA event lazily
+        ev.record()
+    return int(ev.cuda_event)
+
+
 def _args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, k_descale, v_descale, out):
     ds = [desc(x) for x in (q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
                             k_descale, v_descale, out)]
@@ -138,9 +147,11 @@ def verify_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_s
 def verify_attn_ex(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q: int,
                    max_seqlen_k: int, softmax_scale: float, k_descale=None, v_descale=None,
                    out=None, workspace: Optional[torch.Tensor] = None, num_splits: int = 0,
-                   stream=None):
+                   stream=None, event_after_main=None):
     """verify_attn with a caller workspace (a uint8 device tensor) and a forced
-    split count (0 = heuristic). Allocates the workspace with torch if None."""
+    split count (0 = heuristic). Allocates the workspace with torch if None.
+    ``event_after_main`` (a torch.cuda.Event) is recorded between the two
+    kernels when given."""
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
@@ -154,7 +165,7 @@ def verify_attn_ex(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, ma
         s = _lib().verify_attn_ex(r[0], r[1], r[2], r[3], r[4], r[5], int(max_seqlen_q),
                                   int(max_seqlen_k), float(softmax_scale), r[6], r[7], r[8],
                                   ctypes.c_void_p(addr + off), workspace.numel() - off,
-                                  int(num_splits),
+                                  int(num_splits), ctypes.c_void_p(_event_handle(event_after_main)),
                                   ctypes.c_void_p(_stream_handle(stream, q.device)))
     if s != VA_OK:
         raise VerifyAttnError(s, "verify_attn_ex")
@@ -201,8 +212,9 @@ def run_workload(w, out=None, stream=None, **kw):
                        w.v_descale, out=out, stream=stream, **kw)
 
 
-def run_workload_ex(w, out=None, workspace=None, num_splits=0, stream=None):
+def run_workload_ex(w, out=None, workspace=None, num_splits=0, stream=None,
+                    event_after_main=None):
     return verify_attn_ex(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q, w.seqused_k,
                           w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale, w.k_descale,
                           w.v_descale, out=out, workspace=workspace, num_splits=num_splits,
-                          stream=stream)
+                          stream=stream, event_after_main=event_after_main)

@@ -198,7 +198,7 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
                  const va_tensor* cu, const va_tensor* su, int32_t max_q, int32_t max_k,
                  float scale, const va_tensor* kd, const va_tensor* vd, va_tensor* out,
                  const Shapes& sh, const va_plan& plan, void* ws, size_t ws_bytes,
-                 cudaStream_t stream) {
+                 cudaEvent_t ev_mid, cudaStream_t stream) {
   if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;  // no output rows
   if ((size_t)plan.workspace_bytes > ws_bytes || !ws) return VA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return VA_ERR_WORKSPACE;
@@ -246,6 +246,7 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
   p.ws_ml = reinterpret_cast<float*>(base + lay.ml_off);
   p.ws_acc = reinterpret_cast<float*>(base + lay.acc_off);
   if (launch_main_simt(p, stream) != cudaSuccess) return VA_ERR_CUDA;
+  if (ev_mid && cudaEventRecord(ev_mid, stream) != cudaSuccess) return VA_ERR_CUDA;
   if (launch_merge(p, stream) != cudaSuccess) return VA_ERR_CUDA;
   return VA_OK;
 }
@@ -290,7 +291,7 @@ VA_EXPORT va_status verify_attn_ex(const va_tensor* q, const va_tensor* k_cache,
                                    int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
                                    const va_tensor* k_descale, const va_tensor* v_descale,
                                    va_tensor* out, void* workspace, size_t workspace_bytes,
-                                   int32_t num_splits, void* stream) {
+                                   int32_t num_splits, void* event_after_main, void* stream) {
   Shapes sh;
   va_status s = validate(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
                          max_seqlen_k, k_descale, v_descale, out, &sh);
@@ -310,7 +311,8 @@ VA_EXPORT va_status verify_attn_ex(const va_tensor* q, const va_tensor* k_cache,
   if (s != VA_OK) return s;
   return launch(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
                 max_seqlen_k, softmax_scale, k_descale, v_descale, out, sh, plan, workspace,
-                workspace_bytes, static_cast<cudaStream_t>(stream));
+                workspace_bytes, static_cast<cudaEvent_t>(event_after_main),
+                static_cast<cudaStream_t>(stream));
 }
 
 VA_EXPORT va_status verify_attn(const va_tensor* q, const va_tensor* k_cache,
@@ -345,7 +347,7 @@ VA_EXPORT va_status verify_attn(const va_tensor* q, const va_tensor* k_cache,
   }
   return launch(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
                 max_seqlen_k, softmax_scale, k_descale, v_descale, out, sh, plan, st->ws,
-                st->ws_bytes, static_cast<cudaStream_t>(stream));
+                st->ws_bytes, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 VA_EXPORT const char* verify_attn_status_string(int32_t status) {
