@@ -40,8 +40,11 @@ __global__ void __launch_bounds__(kHeadDim) va_merge_kernel(const Params p) {
   const int c1 = split_of(ts + nt - 1, N, p.num_splits);
   if (c0 == c1) return;  // one CTA held the whole item and wrote it
 
+  // CTAs with an empty range (possible when there are more CTAs than tiles)
+  // wrote no partial and are skipped.
   float M = -INFINITY;
   for (int c = c0; c <= c1; ++c) {
+    if (split_begin(N, c, p.num_splits) == split_begin(N, c + 1, p.num_splits)) continue;
     const int64_t piece = (int64_t)j + c;
     M = fmaxf(M, p.ws_ml[(piece * p.max_rows + r) * 2]);
   }
@@ -51,6 +54,7 @@ __global__ void __launch_bounds__(kHeadDim) va_merge_kernel(const Params p) {
   }
   float num = 0.f, den = 0.f;
   for (int c = c0; c <= c1; ++c) {
+    if (split_begin(N, c, p.num_splits) == split_begin(N, c + 1, p.num_splits)) continue;
     const int64_t piece = (int64_t)j + c;
     const float m = p.ws_ml[(piece * p.max_rows + r) * 2];
     const float l = p.ws_ml[(piece * p.max_rows + r) * 2 + 1];
