@@ -189,6 +189,41 @@ size_t verify_attn_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_
                                   int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t kv_dtype,
                                   int32_t num_splits);
 
+/*
+ * verify_attn_noalloc - verify_attn for callers that cannot allocate device
+ * memory. The pages have no counterpart; this is a library addition.
+ *
+ * Who needs it: code that must not call cudaMalloc when it runs attention,
+ * e.g. a serving runtime that sized its GPU memory pool at start-up and
+ * forbids later allocations (cudaMalloc synchronises the device and
+ * fragments the pool), or an allocator callback that must not re-enter the
+ * allocator. verify_attn would grow its workspace with cudaMalloc;
+ * verify_attn_ex needs the caller to allocate one.
+ *
+ * Arguments, layouts, results and errors are those of verify_attn. The
+ * split-KV partials go to a fixed array of VERIFY_ATTN_NOALLOC_SCRATCH_BYTES
+ * compiled into the library; every GPU that loads the library holds that
+ * array until the process exits. Nothing is allocated or freed by this call.
+ *  - Returns VA_ERR_WORKSPACE, before launching anything, when the shapes
+ *    need more partial storage than the array holds (it needs about
+ *    (B*Hkv + SMs) * (Hq/Hkv) * max_seqlen_q KiB).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *    that first call before any stream capture.
+ *  - Every call on a device shares the one array and leaves its contents
+ *    behind. Nothing in it needs to start at zero, but calls that overlap on
+ *    the GPU (different streams, or different host threads) race on it:
+ *    order them on one stream.
+ */
+#define VERIFY_ATTN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+va_status verify_attn_noalloc(const va_tensor* q, const va_tensor* k_cache,
+                              const va_tensor* v_cache, const va_tensor* block_table,
+                              const va_tensor* cu_seqlens_q, const va_tensor* seqused_k,
+                              int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
+                              const va_tensor* k_descale, const va_tensor* v_descale,
+                              va_tensor* out, void* stream);
+
 /* Static, NUL-terminated name of a status code. */
 const char* verify_attn_status_string(int32_t status);
 

@@ -28,7 +28,10 @@ _DTYPES = {torch.bfloat16: VA_BF16, torch.float8_e4m3fn: VA_FP8_E4M3,
 
 # Every symbol include/verify_attn.h declares.
 EXPORTS = ("verify_attn", "verify_attn_ex", "verify_attn_check", "verify_attn_plan",
-           "verify_attn_workspace_size", "verify_attn_status_string")
+           "verify_attn_workspace_size", "verify_attn_status_string", "verify_attn_noalloc")
+
+# Size of the library's built-in partials array used by verify_attn_noalloc.
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class VaTensor(ctypes.Structure):
@@ -74,6 +77,8 @@ def _lib():
         lib.verify_attn_plan.restype = ctypes.c_int32
         lib.verify_attn_workspace_size.argtypes = [ctypes.c_int32] * 7
         lib.verify_attn_workspace_size.restype = ctypes.c_size_t
+        lib.verify_attn_noalloc.argtypes = tens + [ctypes.c_float, P, P, P, ctypes.c_void_p]
+        lib.verify_attn_noalloc.restype = ctypes.c_int32
         lib.verify_attn_status_string.argtypes = [ctypes.c_int32]
         lib.verify_attn_status_string.restype = ctypes.c_char_p
         _LIB = lib
@@ -169,6 +174,27 @@ def verify_attn_ex(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, ma
                                   ctypes.c_void_p(_stream_handle(stream, q.device)))
     if s != VA_OK:
         raise VerifyAttnError(s, "verify_attn_ex")
+    return out
+
+
+def verify_attn_noalloc(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
+                        max_seqlen_q: int, max_seqlen_k: int, softmax_scale: float,
+                        k_descale=None, v_descale=None, out=None, stream=None):
+    """verify_attn for callers that cannot allocate device memory: the
+    split-KV partials live in an array built into the library
+    (NOALLOC_SCRATCH_BYTES per GPU), so the call itself allocates nothing.
+    ``out`` must be given by such callers (here it is created with torch only
+    when omitted). Calls that overlap on the GPU share that array and race."""
+    if out is None:
+        out = torch.empty_like(q)
+    ds, r = _args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, k_descale,
+                  v_descale, out)
+    with torch.cuda.device(q.device):
+        s = _lib().verify_attn_noalloc(r[0], r[1], r[2], r[3], r[4], r[5], int(max_seqlen_q),
+                                       int(max_seqlen_k), float(softmax_scale), r[6], r[7], r[8],
+                                       ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if s != VA_OK:
+        raise VerifyAttnError(s, "verify_attn_noalloc")
     return out
 
 

@@ -7,21 +7,13 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/verify_attn.h"
-#include "va_internal.h"
+#include "va_host_impl.h"
 
-#define VA_EXPORT extern "C" __attribute__((visibility("default")))
-
-namespace {
+namespace va_host_impl {
 
 using namespace va;
 
 constexpr int kMaxDevices = 64;
-
-struct Shapes {
-  int64_t total_q, hq, hkv, num_blocks, num_seqs, width;
-  int32_t kv_dtype;
-};
 
 int64_t numel(const va_tensor* t) {
   int64_t n = 1;
@@ -174,12 +166,12 @@ struct DeviceState {
   size_t ws_bytes = 0;
 };
 
-std::mutex g_mu;
-DeviceState g_dev[kMaxDevices];
+static std::mutex g_mu;
+static DeviceState g_dev[kMaxDevices];
 
 // Current device's state, initialised once (SM count, kernel attributes).
 // Caller holds g_mu.
-va_status device_state(DeviceState** out) {
+static va_status device_state(DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return VA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return VA_ERR_UNSUPPORTED;
@@ -251,7 +243,17 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
   return VA_OK;
 }
 
-}  // namespace
+va_status current_device_sms(int* sms) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  const va_status s = device_state(&st);
+  if (s == VA_OK) *sms = st->sms;
+  return s;
+}
+
+}  // namespace va_host_impl
+
+using namespace va_host_impl;
 
 VA_EXPORT va_status verify_attn_check(const va_tensor* q, const va_tensor* k_cache,
                                       const va_tensor* v_cache, const va_tensor* block_table,
