@@ -33,7 +33,7 @@ METRIC = "verify-attn µs/call and achieved HBM GB/s (fraction of ~8 TB/s) on 1 
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-MAIN_KERNEL = "va_main_simt_kernel"
+MAIN_KERNEL = {"fp8_e4m3": "va_main_tc_fp8_kernel", "bf16": "va_main_simt_kernel"}
 
 
 def parse():
@@ -299,7 +299,7 @@ def run_ours(args):
         "us_per_call": round(ms_per_step * 1e3, 2),
         "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "main_kernel_us": round(main_ms * 1e3, 2),
-        "roofline": {"bound": "hbm", "kernel": MAIN_KERNEL, "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": MAIN_KERNEL[w.kv_dtype], "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_src} (HBM copy bandwidth)",
                      "traffic": recorded_traffic(args.workload),

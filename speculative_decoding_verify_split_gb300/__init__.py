@@ -161,7 +161,7 @@ def verify_attn_ex(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, ma
         out = torch.empty_like(q)
     if workspace is None:
         n = workspace_size(q, k_cache, seqused_k, max_seqlen_q, max_seqlen_k, num_splits)
-        workspace = torch.empty(n + 256, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(n + 256, dtype=torch.uint8, device=q.device)
     addr = workspace.data_ptr()
     off = (-addr) % 256
     ds, r = _args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, k_descale,
@@ -196,6 +196,13 @@ def verify_attn_noalloc(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_
     if s != VA_OK:
         raise VerifyAttnError(s, "verify_attn_noalloc")
     return out
+
+
+def workspace_status(workspace: torch.Tensor) -> int:
+    """Sticky error bits the kernels set in a caller workspace (0 = no bounded
+    wait ever timed out). Reads device memory, so it synchronises."""
+    off = (-workspace.data_ptr()) % 256
+    return int(workspace[off:off + 4].view(torch.int32).item())
 
 
 def check(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q: int,

@@ -132,7 +132,10 @@ va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t m
   if (kv_dtype != VA_FP8_E4M3 && kv_dtype != VA_BF16) return VA_ERR_UNSUPPORTED;
   const int64_t G = hq / hkv;
   if (G * max_q > kMaxRows) return VA_ERR_UNSUPPORTED;
-  const int tile = kSimtTileKeys;
+  // FP8 pages go to the tensor-core kernel (64-key tiles); BF16 pages to the
+  // CUDA-core kernel (32-key tiles).
+  const bool tc = kv_dtype == VA_FP8_E4M3;
+  const int tile = tc ? kTcTileKeys : kSimtTileKeys;
   const int64_t J = B * hkv;
   const int64_t tiles_bound = J * ((max_k + tile - 1) / tile);
   if (tiles_bound > INT32_MAX / 2) return VA_ERR_UNSUPPORTED;
@@ -154,9 +157,45 @@ va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t m
   plan->num_splits = (int32_t)splits;
   plan->max_rows = (int32_t)(G * max_q);
   plan->num_work = (int32_t)J;
-  plan->kernel = kKernelSimt;
+  plan->kernel = tc ? kKernelTcFp8 : kKernelSimt;
   plan->workspace_bytes = (int64_t)workspace_layout(J, splits, G * max_q).total;
   return VA_OK;
+}
+
+// cuTensorMapEncodeTiled, fetched through the runtime so that the library
+// does not link the driver library (it must load on machines without one).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 4-D map over an FP8 cache [num_blocks, 16, Hkv, 256] (bytes): box = one
+// page of one KV head, half the head dim (16 tokens x 128 bytes), 128-byte
+// swizzle, so each box lands as eight 1 KB swizzle atoms.
+static bool make_kv_map(CUtensorMap* m, const va_tensor* t, int64_t nb, int64_t hkv) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)kPageSize, (cuuint64_t)nb};
+  cuuint64_t strides[3] = {(cuuint64_t)t->stride[2], (cuuint64_t)t->stride[1], (cuuint64_t)t->stride[0]};
+  cuuint32_t box[4] = {128, 1, (cuuint32_t)kPageSize, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, t->data, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct DeviceState {
@@ -180,6 +219,7 @@ static va_status device_state(DeviceState** out) {
     if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return VA_ERR_CUDA;
     if (prepare_main_simt() != cudaSuccess) return VA_ERR_CUDA;
+    if (prepare_main_tc() != cudaSuccess) return VA_ERR_CUDA;
     st.ready = true;
   }
   *out = &st;
@@ -237,7 +277,15 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
   p.ws_meta = reinterpret_cast<int32_t*>(base + lay.meta_off);
   p.ws_ml = reinterpret_cast<float*>(base + lay.ml_off);
   p.ws_acc = reinterpret_cast<float*>(base + lay.acc_off);
-  if (launch_main_simt(p, stream) != cudaSuccess) return VA_ERR_CUDA;
+  p.ws_status = reinterpret_cast<int32_t*>(base + lay.status_off);
+  if (plan.kernel == kKernelTcFp8 && sh.num_blocks > 0) {
+    CUtensorMap tm_k, tm_v;
+    if (!make_kv_map(&tm_k, k, sh.num_blocks, sh.hkv) || !make_kv_map(&tm_v, v, sh.num_blocks, sh.hkv))
+      return VA_ERR_LAYOUT;
+    if (launch_main_tc_fp8(p, tm_k, tm_v, stream) != cudaSuccess) return VA_ERR_CUDA;
+  } else {
+    if (launch_main_simt(p, stream) != cudaSuccess) return VA_ERR_CUDA;
+  }
   if (ev_mid && cudaEventRecord(ev_mid, stream) != cudaSuccess) return VA_ERR_CUDA;
   if (launch_merge(p, stream) != cudaSuccess) return VA_ERR_CUDA;
   return VA_OK;
@@ -345,6 +393,7 @@ VA_EXPORT va_status verify_attn(const va_tensor* q, const va_tensor* k_cache,
       st->ws = nullptr;
       return VA_ERR_CUDA;
     }
+    if (cudaMemset(st->ws, 0, (size_t)plan.workspace_bytes) != cudaSuccess) return VA_ERR_CUDA;
     st->ws_bytes = (size_t)plan.workspace_bytes;
   }
   return launch(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,

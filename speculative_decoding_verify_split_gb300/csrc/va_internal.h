@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace va {
@@ -37,6 +38,7 @@ struct Params {
   // Split-KV decomposition: one stream of key tiles over all work items
   // j = b * hkv + kvh, cut into num_splits equal ranges (one per CTA).
   int32_t tile_keys, num_splits, max_rows, num_work;
+  int32_t* ws_status;  // sticky error bits (a bounded wait timed out); never cleared by kernels
   int32_t* ws_meta;  // [num_work + 1]: first tile of each work item, then the total
   float* ws_ml;      // [pieces][max_rows][2]: running max (log2 units), row sum
   float* ws_acc;     // [pieces][max_rows][256]: unnormalised output rows
@@ -46,7 +48,7 @@ struct Params {
 // CTAs c0..c1 stores the partial of CTA c at piece j + c, which is unique
 // because consecutive work items share at most one CTA.
 struct WorkspaceLayout {
-  size_t meta_off, ml_off, acc_off, total;
+  size_t status_off, meta_off, ml_off, acc_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -54,19 +56,24 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline WorkspaceLayout workspace_layout(int64_t num_work, int64_t num_splits, int64_t max_rows) {
   WorkspaceLayout w;
   const int64_t pieces = num_work + num_splits;
-  w.meta_off = 0;
-  w.ml_off = align_up(sizeof(int32_t) * (size_t)(num_work + 1), 256);
+  w.status_off = 0;
+  w.meta_off = 256;
+  w.ml_off = w.meta_off + align_up(sizeof(int32_t) * (size_t)(num_work + 1), 256);
   w.acc_off = w.ml_off + align_up(sizeof(float) * 2 * (size_t)(pieces * max_rows), 256);
   w.total = w.acc_off + align_up(sizeof(float) * kHeadDim * (size_t)(pieces * max_rows), 256);
   return w;
 }
 
 // Main-kernel variants.
-enum Kernel : int32_t { kKernelSimt = 0 };
+enum Kernel : int32_t { kKernelSimt = 0, kKernelTcFp8 = 1 };
 constexpr int kSimtTileKeys = 32;
+constexpr int kTcTileKeys = 64;
 
 cudaError_t prepare_main_simt();  // once per device: opt in to its shared memory
 cudaError_t launch_main_simt(const Params& p, cudaStream_t stream);
 cudaError_t launch_merge(const Params& p, cudaStream_t stream);
+cudaError_t prepare_main_tc();
+cudaError_t launch_main_tc_fp8(const Params& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                               cudaStream_t stream);
 
 }  // namespace va

@@ -193,3 +193,15 @@ def test_out_of_range_page_ids_do_not_fault():
     w.block_table[0, 1] = 10**6
     wg = to_gpu(w)
     run_gpu(wg)
+
+
+def test_no_bounded_wait_timed_out():
+    """The tensor-core kernel bounds every wait; a timeout sets a status bit in
+    the workspace. None may be set on a normal run."""
+    w = to_gpu(make_workload([4, 3, 2, 4], [9000, 2500, 900, 70], 16, 1, "fp8_e4m3", seed=18))
+    n = va.workspace_size(w.q, w.k_cache, w.seqused_k, w.max_seqlen_q, w.max_seqlen_k)
+    ws = torch.zeros(n + 256, dtype=torch.uint8, device="cuda")
+    for splits in (0, 3, 40):
+        va.run_workload_ex(w, out=torch.empty_like(w.q), workspace=ws, num_splits=splits)
+    torch.cuda.synchronize()
+    assert va.workspace_status(ws) == 0

@@ -107,8 +107,9 @@ def test_plan_small_batches_use_few_splits():
 
 def test_plan_force_and_clamp():
     assert va.plan(2, 1, 16, 4, 1024, "fp8_e4m3", 152, force_splits=7)["num_splits"] == 7
-    tiles = 2 * (1024 // 32)
-    assert va.plan(2, 1, 16, 4, 1024, "fp8_e4m3", 152, force_splits=10**6)["num_splits"] == tiles
+    for dt in ("fp8_e4m3", "bf16"):
+        p = va.plan(2, 1, 16, 4, 1024, dt, 152, force_splits=10**6)
+        assert p["num_splits"] == 2 * (1024 // p["tile_keys"])
     assert va.plan(3, 1, 16, 4, 0, "fp8_e4m3", 152)["num_splits"] == 1
 
 
