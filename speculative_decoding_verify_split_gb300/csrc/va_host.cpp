@@ -132,10 +132,8 @@ va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t m
   if (kv_dtype != VA_FP8_E4M3 && kv_dtype != VA_BF16) return VA_ERR_UNSUPPORTED;
   const int64_t G = hq / hkv;
   if (G * max_q > kMaxRows) return VA_ERR_UNSUPPORTED;
-  // FP8 pages go to the tensor-core kernel (64-key tiles); BF16 pages to the
-  // CUDA-core kernel (32-key tiles).
-  const bool tc = kv_dtype == VA_FP8_E4M3;
-  const int tile = tc ? kTcTileKeys : kSimtTileKeys;
+  // Tensor-core kernel: 64-key tiles for FP8 pages, 32-key tiles for BF16.
+  const int tile = kv_dtype == VA_FP8_E4M3 ? kTcTileKeys : kTcTileKeysBf16;
   const int64_t J = B * hkv;
   const int64_t tiles_bound = J * ((max_k + tile - 1) / tile);
   if (tiles_bound > INT32_MAX / 2) return VA_ERR_UNSUPPORTED;
@@ -157,7 +155,7 @@ va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t m
   plan->num_splits = (int32_t)splits;
   plan->max_rows = (int32_t)(G * max_q);
   plan->num_work = (int32_t)J;
-  plan->kernel = tc ? kKernelTcFp8 : kKernelSimt;
+  plan->kernel = kKernelTc;
   plan->workspace_bytes = (int64_t)workspace_layout(J, splits, G * max_q).total;
   return VA_OK;
 }
@@ -183,17 +181,21 @@ static EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// 4-D map over an FP8 cache [num_blocks, 16, Hkv, 256] (bytes): box = one
-// page of one KV head, half the head dim (16 tokens x 128 bytes), 128-byte
-// swizzle, so each box lands as eight 1 KB swizzle atoms.
+// 4-D map over a cache [num_blocks, 16, Hkv, 256]: box = one page of one KV
+// head, 128 bytes of the head dim (16 tokens x 128 bytes), 128-byte swizzle,
+// so each box lands as two 1 KB swizzle atoms.
 static bool make_kv_map(CUtensorMap* m, const va_tensor* t, int64_t nb, int64_t hkv) {
   EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
+  const int64_t es_bytes = elem_size(t->dtype);
   cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)kPageSize, (cuuint64_t)nb};
-  cuuint64_t strides[3] = {(cuuint64_t)t->stride[2], (cuuint64_t)t->stride[1], (cuuint64_t)t->stride[0]};
-  cuuint32_t box[4] = {128, 1, (cuuint32_t)kPageSize, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)(t->stride[2] * es_bytes), (cuuint64_t)(t->stride[1] * es_bytes),
+                           (cuuint64_t)(t->stride[0] * es_bytes)};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / es_bytes), 1, (cuuint32_t)kPageSize, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, t->data, dims, strides, box, es,
+  const CUtensorMapDataType dt =
+      es_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  return fn(m, dt, 4, t->data, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -218,7 +220,6 @@ static va_status device_state(DeviceState** out) {
   if (!st.ready) {
     if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return VA_ERR_CUDA;
-    if (prepare_main_simt() != cudaSuccess) return VA_ERR_CUDA;
     if (prepare_main_tc() != cudaSuccess) return VA_ERR_CUDA;
     st.ready = true;
   }
@@ -278,14 +279,14 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
   p.ws_ml = reinterpret_cast<float*>(base + lay.ml_off);
   p.ws_acc = reinterpret_cast<float*>(base + lay.acc_off);
   p.ws_status = reinterpret_cast<int32_t*>(base + lay.status_off);
-  if (plan.kernel == kKernelTcFp8 && sh.num_blocks > 0) {
-    CUtensorMap tm_k, tm_v;
+  CUtensorMap tm_k, tm_v;
+  std::memset(&tm_k, 0, sizeof(tm_k));
+  std::memset(&tm_v, 0, sizeof(tm_v));
+  if (sh.num_blocks > 0) {  // an empty cache has no page to load
     if (!make_kv_map(&tm_k, k, sh.num_blocks, sh.hkv) || !make_kv_map(&tm_v, v, sh.num_blocks, sh.hkv))
       return VA_ERR_LAYOUT;
-    if (launch_main_tc_fp8(p, tm_k, tm_v, stream) != cudaSuccess) return VA_ERR_CUDA;
-  } else {
-    if (launch_main_simt(p, stream) != cudaSuccess) return VA_ERR_CUDA;
   }
+  if (launch_main_tc(p, tm_k, tm_v, stream) != cudaSuccess) return VA_ERR_CUDA;
   if (ev_mid && cudaEventRecord(ev_mid, stream) != cudaSuccess) return VA_ERR_CUDA;
   if (launch_merge(p, stream) != cudaSuccess) return VA_ERR_CUDA;
   return VA_OK;

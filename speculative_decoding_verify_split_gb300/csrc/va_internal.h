@@ -64,16 +64,14 @@ inline WorkspaceLayout workspace_layout(int64_t num_work, int64_t num_splits, in
   return w;
 }
 
-// Main-kernel variants.
-enum Kernel : int32_t { kKernelSimt = 0, kKernelTcFp8 = 1 };
-constexpr int kSimtTileKeys = 32;
-constexpr int kTcTileKeys = 64;
+// Main kernel (tensor cores) and its key-tile sizes.
+enum Kernel : int32_t { kKernelTc = 1 };
+constexpr int kTcTileKeys = 64;      // FP8 KV
+constexpr int kTcTileKeysBf16 = 32;  // BF16 KV
 
-cudaError_t prepare_main_simt();  // once per device: opt in to its shared memory
-cudaError_t launch_main_simt(const Params& p, cudaStream_t stream);
 cudaError_t launch_merge(const Params& p, cudaStream_t stream);
-cudaError_t prepare_main_tc();
-cudaError_t launch_main_tc_fp8(const Params& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                               cudaStream_t stream);
+cudaError_t prepare_main_tc();  // once per device: opt in to its shared memory
+cudaError_t launch_main_tc(const Params& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                           cudaStream_t stream);
 
 }  // namespace va

@@ -1,34 +1,40 @@
-// Split-KV main kernel on the 5th-generation tensor cores (tcgen05, sm_103a),
-// FP8 E4M3 KV cache.
+// Split-KV main kernel on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
 // Same decomposition and partial format as the CUDA-core kernel: one CTA per
-// SM takes an equal share of the batch's 64-key tiles, and for every
+// SM takes an equal share of the batch's key tiles, and for every
 // (sequence, KV head) in its share packs all G query heads x L draft tokens
 // (<= 64 rows) into one M=64 tile, so each KV page is read from HBM once per
 // KV head (sglang PR 30105 digest, "Implementation breakdown" item 2; sglang
 // PR 34517 digest, "Motivation": one KV load shared by the heads of a group).
 //
-// The FP8 pages stay FP8 all the way into the tensor cores (kind::f8f6f4):
-//  * S = Q K^T: Q (bf16) is scaled per row by a power of two 2^e (exact) and
-//    split into two e4m3 terms, Qh = e4m3(Q 2^e) and Ql = e4m3(Q 2^e - Qh);
-//    both MMAs accumulate into the same fp32 TMEM tile, so the logits carry
-//    the product (Qh + Ql) K, about 2^-8 relative to Q, with K exact.
-//  * O += P V: P = 2^(s - m_ref + 8) <= 2^8.3 is split the same way into
-//    e4m3 hi and lo terms; V is the MN-major B operand read straight from the
-//    TMA-staged page.
-// The k/v descales fold into the logit scale and the output scale.
+// KV pages are TMA-loaded as 128-byte-swizzled boxes (16 tokens x 128 bytes
+// of one KV head) into a 5-stage ring and fed to the tensor cores as they are:
+//  * FP8 E4M3 cache, kind::f8f6f4, 64-key tiles. Q (bf16) is scaled per row
+//    by an exact power of two 2^e and split into two e4m3 terms,
+//    Qh = e4m3(Q 2^e), Ql = e4m3(Q 2^e - Qh); both MMAs accumulate into the
+//    same fp32 TMEM tile, so the logits carry (Qh + Ql) K with K exact. P is
+//    split the same way into e4m3 hi/lo terms. K and V are never dequantised.
+//  * BF16 cache, kind::f16, 32-key tiles; Q and P in bf16.
+// V is the MN-major B operand of O += P V. The k/v descales fold into the
+// logit scale and the output scale.
 //
-// Roles (256 threads):
-//  warp 0     TMA producer: block-table walk (32 page ids per lane load),
-//             two 128-byte-swizzled 2 KB boxes per page for K and for V into
-//             a 5-stage ring.
-//  warp 1     TMEM owner and MMA issuer (one thread).
-//  warps 4-7  softmax: thread (quadrant q, lane t) owns row 16q + (t & 15)
-//             and half (t >> 4) of each tile's keys and of O's columns.
-// Online softmax in log2 units keeps a per-row reference m_ref; it moves (and
-// O, l are rescaled in TMEM) only when a tile's max exceeds it by > 0.3, so
-// rescaling is rare. Waits are bounded in time: on a timeout the kernel sets
-// the workspace status word, stops issuing work and frees its TMEM.
+// Roles (384 threads):
+//  warp 0      TMA producer: block-table walk (32 page ids per lane load).
+//  warp 1      TMEM owner and MMA issuer (one thread). QK^T runs up to two
+//              tiles ahead of P V through four S buffers in TMEM.
+//  warps 4-11  softmax, two warps per TMEM lane quadrant (same SMSP, so they
+//              hide each other's latency). Warp w owns packed rows
+//              16(w%4) .. +15 (the M=64 accumulator puts them in TMEM lanes
+//              32(w%4) .. +15), half kh = (w-4)/4 of each tile's keys and of
+//              O's columns; lane bit 4 splits that half again. The two warps
+//              of a quadrant exchange row maxima through shared memory.
+// Online softmax in log2 units keeps a per-row reference m_ref and computes
+// P = 2^(s - m_ref + 6) <= 2^8.5; m_ref moves (and O, l are rescaled in
+// TMEM) only when a tile's max exceeds it by more than 2.5, so rescales are
+// rare. Waits are bounded in time and warp-uniform: on a timeout the kernel
+// sets the workspace status word, stops issuing work, drains and frees its
+// TMEM.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -40,23 +46,45 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kT = kTcTileKeys;  // 64 keys per tile
+template <bool FP8>
+struct Cfg {
+  static constexpr int kT = FP8 ? kTcTileKeys : kTcTileKeysBf16;  // keys per tile
+  static constexpr int kEsize = FP8 ? 1 : 2;                       // bytes per KV element
+  static constexpr int kChunks = kHeadDim * kEsize / 128;          // 128-byte d chunks (2 or 4)
+  static constexpr int kRegion = kT * 128;                         // one d chunk of a K or V tile
+  static constexpr int kTensorBytes = kChunks * kRegion;           // K (or V) tile
+  static constexpr int kStageBytes = 2 * kTensorBytes;             // 32 KB either way
+  static constexpr int kPagesPerTile = kT / kPageSize;
+  static constexpr int kPageBytes = kChunks * 2048;                // one page of one tensor
+  static constexpr int kQParts = FP8 ? 2 : 1;                      // hi/lo e4m3, or bf16
+  static constexpr int kQPart = kChunks * 64 * 128;
+  static constexpr int kPParts = FP8 ? 2 : 1;
+  static constexpr int kPPart = 64 * kT * kEsize;                  // 64 rows x 64 bytes
+  static constexpr int kKeysPerStep = 32 / kEsize;                 // PV keys per MMA (32 bytes)
+  static constexpr int kQuarter = kT / 4;                          // keys per thread per tile
+  static constexpr uint32_t kFmt = FP8 ? 0u : 1u;                  // e4m3 / bf16
+  static constexpr uint32_t kIdQK = instr_desc(kFmt, kFmt, false, kT, 64);
+  static constexpr uint32_t kIdPV = instr_desc(kFmt, kFmt, true, kHeadDim, 64);
+};
+
 constexpr int kStages = 5;
-constexpr int kThreads = 256;
-constexpr int kStageBytes = 32768;  // K: 2 halves x 64 keys x 128 B; V: same
-constexpr int kQPart = 16384;       // 2 halves x 64 rows x 128 B
-constexpr int kPPart = 4096;        // 64 rows x 64 B, no swizzle
-constexpr int kOffQ = kStages * kStageBytes;
-constexpr int kOffP = kOffQ + 2 * kQPart;
-constexpr int kOffBar = kOffP + 4 * kPPart;
-constexpr int kSmemBytes = kOffBar + 512 + 1024;
+constexpr int kSBufs = 4;
+constexpr int kPvLag = 2;
+constexpr int kThreads = 384;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kOffQ = kStages * 32768;
+constexpr int kOffP = kOffQ + 32768;
+constexpr int kOffX = kOffP + 16384;  // row-max exchange: [2 parity][2 kh][64 rows] floats
+constexpr int kOffBar = kOffX + 1024;
+constexpr int kSmemBytes = kOffBar + 1024 + 1024;
 
 constexpr uint32_t kColO = 0;    // 256 fp32 columns
-constexpr uint32_t kColS = 256;  // two 64-column S tiles
+constexpr uint32_t kColS = 256;  // four S tiles
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint32_t kIdQK = instr_desc(0, 0, false, kT, 64);     // e4m3 x e4m3, M=64, N=64
-constexpr uint32_t kIdPV = instr_desc(0, 0, true, kHeadDim, 64);  // B (V) MN-major, N=256
+constexpr float kPShift = 6.f;    // P = 2^(s - m_ref + kPShift)
+constexpr float kHeadroom = 1.f;  // m_ref = tile max + kHeadroom when it moves
+constexpr float kOvershoot = 2.5f;  // move only if the tile max > m_ref + kOvershoot
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -66,16 +94,18 @@ enum : int {
   kBarFullV = kBarFullK + kStages,
   kBarEmpty = kBarFullV + kStages,
   kBarSFull = kBarEmpty + kStages,
-  kBarSFree = kBarSFull + 2,
-  kBarPFull = kBarSFree + 2,
+  kBarSFree = kBarSFull + kSBufs,
+  kBarPFull = kBarSFree + kSBufs,
   kBarPFree = kBarPFull + 2,
   kBarQFull = kBarPFree + 2,
   kBarQFree,
   kBarOFull,
   kBarOFree,
   kBarDrain,
-  kNumBars
+  kBarX,  // four row-exchange barriers, one per TMEM lane quadrant
+  kNumBars = kBarX + 4
 };
+static_assert(8 * kNumBars + 16 + 34 * 8 <= 1024, "barrier area");
 
 struct Piece {
   int j, b, kvh, S, L, q0, R, nt, lt0, lt1;
@@ -123,7 +153,7 @@ __device__ __forceinline__ float2 unpack_fp8x2(uint32_t v) {
   return __half22float2(__half2(h));
 }
 
-// p (two fp32 values, p.x first) -> e4m3 hi and lo bytes, via f16x2.
+// p (two fp32 values, a first) -> e4m3 hi and lo bytes, via f16x2.
 __device__ __forceinline__ void split_p(float a, float b, uint32_t& hi, uint32_t& lo) {
   const __half2 h = __floats2half2_rn(a, b);
   const __nv_fp8x2_storage_t h8 = __nv_cvt_halfraw2_to_fp8x2(__half2_raw(h), __NV_SATFINITE, __NV_E4M3);
@@ -134,9 +164,37 @@ __device__ __forceinline__ void split_p(float a, float b, uint32_t& hi, uint32_t
   lo = (uint32_t)l8;
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
+}
+
+// S values of this thread: columns [col, col + n) for lanes 0-15 of the warp,
+// [col + n, col + 2n) for lanes 16-31, n = keys per thread.
+template <int N>
+__device__ __forceinline__ void tmem_ld_s(uint32_t taddr, uint32_t (&r)[N]);
+template <>
+__device__ __forceinline__ void tmem_ld_s<16>(uint32_t taddr, uint32_t (&r)[16]) {
+  tmem_ld_16x32bx2_x16<16>(taddr, r);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_s<8>(uint32_t taddr, uint32_t (&r)[8]) {
+  tmem_ld_16x32bx2_x8<8>(taddr, r);
+}
+
+template <bool FP8>
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (FP8)
+    mma_f8f6f4(d, a, b, idesc, acc);
+  else
+    mma_f16(d, a, b, idesc, acc);
+}
+
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
-    va_main_tc_fp8_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v) {
+    va_main_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v) {
+  using C = Cfg<FP8>;
+  constexpr int kT = C::kT;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -146,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   long long* scratch = reinterpret_cast<long long*>(sm + kOffBar + 8 * kNumBars + 16);  // 32 slots
   long long* s_ts = scratch + 32;
   int* s_j = reinterpret_cast<int*>(scratch + 33);
+  float* xch = reinterpret_cast<float*>(sm + kOffX);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -153,6 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c = blockIdx.x;
   const uint32_t sbase = smem_addr(sm);
   auto bar = [&](int i) { return smem_addr(&bars[i]); };
+
+  // The merge kernel is a programmatic dependent: let it be scheduled now; it
+  // waits for this grid's completion before reading the workspace.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---- work range (all threads) -------------------------------------------------
   const long long N = scan_work<kThreads>(p, scratch, c == 0);
@@ -164,23 +227,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   find_work<kThreads>(p, t0, scratch, s_j, s_ts, &j_first, &ts_first);
 
   // ---- setup --------------------------------------------------------------------
+  constexpr uint32_t kSwWarps = kSoftmaxThreads / 32;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarFullK + s), 1);
       mbar_init(bar(kBarFullV + s), 1);
       mbar_init(bar(kBarEmpty + s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
-      mbar_init(bar(kBarSFree + i), 4);
-      mbar_init(bar(kBarPFull + i), 4);
+      mbar_init(bar(kBarSFree + i), kSwWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarPFull + i), kSwWarps);
       mbar_init(bar(kBarPFree + i), 1);
     }
-    mbar_init(bar(kBarQFull), 4);
+    mbar_init(bar(kBarQFull), kSwWarps);
     mbar_init(bar(kBarQFree), 1);
     mbar_init(bar(kBarOFull), 1);
-    mbar_init(bar(kBarOFree), 4);
+    mbar_init(bar(kBarOFree), kSwWarps);
     mbar_init(bar(kBarDrain), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(kBarX + i), 64);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -188,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == 0 && lane == 0 && p.num_blocks > 0) {
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
@@ -218,37 +285,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const int pg0 = lt * (kT / kPageSize);
-        if (win < 0 || pg0 + 3 >= win + 32) {
+        const int pg0 = lt * C::kPagesPerTile;
+        if (win < 0 || pg0 + C::kPagesPerTile > win + 32) {
           win = pg0;
           const int pg = win + lane;
           my_page = pg < npages ? bt_row[(int64_t)pg * p.bt_s1] : -1;
         }
         uint32_t nvalid = 0;
-        int ids[4];
+        int ids[C::kPagesPerTile];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < C::kPagesPerTile; ++i) {
           ids[i] = __shfl_sync(0xffffffffu, my_page, pg0 + i - win);
           const bool v = (pg0 + i) < npages && (unsigned)ids[i] < (unsigned)p.num_blocks;
           ids[i] = v ? ids[i] : -1;
           nvalid += v ? 1u : 0u;
         }
         if (lane == 0) {
-          const uint32_t kst = sbase + s * kStageBytes;
-          const uint32_t vst = kst + kStageBytes / 2;
-          mbar_arrive_expect_tx(bar(kBarFullK + s), nvalid * 4096u);
+          const uint32_t kst = sbase + s * C::kStageBytes;
+          const uint32_t vst = kst + C::kTensorBytes;
+          mbar_arrive_expect_tx(bar(kBarFullK + s), nvalid * (uint32_t)C::kPageBytes);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < C::kPagesPerTile; ++i) {
             if (ids[i] < 0) continue;
-            tma_load_4d(kst + i * 2048, &tm_k, 0, pc.kvh, 0, ids[i], bar(kBarFullK + s));
-            tma_load_4d(kst + 8192 + i * 2048, &tm_k, 128, pc.kvh, 0, ids[i], bar(kBarFullK + s));
+#pragma unroll
+            for (int ch = 0; ch < C::kChunks; ++ch)
+              tma_load_4d(kst + ch * C::kRegion + i * 2048, &tm_k, ch * (128 / C::kEsize), pc.kvh, 0,
+                          ids[i], bar(kBarFullK + s));
           }
-          mbar_arrive_expect_tx(bar(kBarFullV + s), nvalid * 4096u);
+          mbar_arrive_expect_tx(bar(kBarFullV + s), nvalid * (uint32_t)C::kPageBytes);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < C::kPagesPerTile; ++i) {
             if (ids[i] < 0) continue;
-            tma_load_4d(vst + i * 2048, &tm_v, 0, pc.kvh, 0, ids[i], bar(kBarFullV + s));
-            tma_load_4d(vst + 8192 + i * 2048, &tm_v, 128, pc.kvh, 0, ids[i], bar(kBarFullV + s));
+#pragma unroll
+            for (int ch = 0; ch < C::kChunks; ++ch)
+              tma_load_4d(vst + ch * C::kRegion + i * 2048, &tm_v, ch * (128 / C::kEsize), pc.kvh, 0,
+                          ids[i], bar(kBarFullV + s));
           }
         }
         __syncwarp();
@@ -265,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ======================= MMA issuer ===========================================
     if (lane == 0) {
-      const uint32_t qh = sbase + kOffQ, ql = qh + kQPart;
+      const uint32_t qbase = sbase + kOffQ;
       int it = 0, piece_idx = 0;
       int j = j_first;
       long long ts = ts_first;
@@ -291,15 +362,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_or_fail(kBarFullV + s, (x / kStages) & 1, 8)) return;
           if (x == first && piece_idx > 0 && !wait_or_fail(kBarOFree, (piece_idx - 1) & 1, 16)) return;
           tc_fence_after();
-          const uint32_t vst = sbase + s * kStageBytes + kStageBytes / 2;
+          const uint32_t vst = sbase + s * C::kStageBytes + C::kTensorBytes;
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            const uint32_t pbuf = sbase + kOffP + (pb * 2 + part) * kPPart;
+          for (int part = 0; part < C::kPParts; ++part) {
+            const uint32_t pbuf = sbase + kOffP + (pb * 2 + part) * C::kPPart;
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
+            for (int kk = 0; kk < kT / C::kKeysPerStep; ++kk) {
               const uint64_t a = smem_desc(pbuf + kk * 256, 128, 512, kLayoutNone);
-              const uint64_t bdesc = smem_desc(vst + kk * 4096, 8192, 1024, kLayoutSw128);
-              mma_f8f6f4(tmem + kColO, a, bdesc, kIdPV, (x == first && part == 0 && kk == 0) ? 0u : 1u);
+              const uint64_t bdesc = smem_desc(vst + kk * (C::kKeysPerStep / 8) * 1024, C::kRegion,
+                                               1024, kLayoutSw128);
+              mma<FP8>(tmem + kColO, a, bdesc, C::kIdPV, (x == first && part == 0 && kk == 0) ? 0u : 1u);
             }
           }
           mma_commit(bar(kBarPFree + pb));
@@ -309,27 +381,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < ntile && ok; ++i) {
           const int cur = first + i;
           const int s = cur % kStages;
-          const int b = cur & 1;
+          const int b = cur & (kSBufs - 1);
           if (!wait_or_fail(kBarFullK + s, (cur / kStages) & 1, 32)) break;
-          if (cur >= 2 && !wait_or_fail(kBarSFree + b, ((cur - 2) >> 1) & 1, 64)) break;
+          if (cur >= kSBufs && !wait_or_fail(kBarSFree + b, ((cur - kSBufs) / kSBufs) & 1, 64)) break;
           tc_fence_after();
-          const uint32_t kst = sbase + s * kStageBytes;
+          const uint32_t kst = sbase + s * C::kStageBytes;
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            const uint32_t qb = part ? ql : qh;
+          for (int part = 0; part < C::kQParts; ++part) {
+            const uint32_t qb = qbase + part * C::kQPart;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint32_t off = (uint32_t)((k >> 2) * 8192 + (k & 3) * 32);
-              const uint64_t a = smem_desc(qb + off, 16, 1024, kLayoutSw128);
-              const uint64_t bdesc = smem_desc(kst + off, 16, 1024, kLayoutSw128);
-              mma_f8f6f4(tmem + kColS + b * kT, a, bdesc, kIdQK, (part | k) ? 1u : 0u);
+            for (int k = 0; k < 4 * C::kChunks; ++k) {
+              const uint32_t qoff = (uint32_t)((k >> 2) * 8192 + (k & 3) * 32);
+              const uint32_t koff = (uint32_t)((k >> 2) * C::kRegion + (k & 3) * 32);
+              const uint64_t a = smem_desc(qb + qoff, 16, 1024, kLayoutSw128);
+              const uint64_t bdesc = smem_desc(kst + koff, 16, 1024, kLayoutSw128);
+              mma<FP8>(tmem + kColS + b * kT, a, bdesc, C::kIdQK, (part | k) ? 1u : 0u);
             }
           }
           mma_commit(bar(kBarSFull + b));
           if (i == ntile - 1) mma_commit(bar(kBarQFree));
-          if (i > 0) issue_pv(cur - 1);
+          if (i >= kPvLag) issue_pv(cur - kPvLag);
         }
-        if (ok) issue_pv(first + ntile - 1);
+        for (int x = first + (ntile > kPvLag ? ntile - kPvLag : 0); ok && x < first + ntile; ++x)
+          issue_pv(x);
         it = first + ntile;
         ++piece_idx;
       }
@@ -340,23 +414,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ======================= softmax / epilogue ===================================
-    const int q = warp & 3;
-    const int hf = lane >> 4;
-    const int r = 16 * q + (lane & 15);
+    const int q = warp & 3;              // TMEM lane quadrant
+    const int kh = (warp - 4) >> 2;      // which half of the keys / O columns
+    const int sub = lane >> 4;           // which quarter within that half
+    const int rl = lane & 15;
+    const int r = 16 * q + rl;           // packed row
+    const int qtr = 2 * kh + sub;        // quarter 0..3
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const float kd = p.k_descale ? *p.k_descale : 1.0f;
     const float vd = p.v_descale ? *p.v_descale : 1.0f;
     const float cscale = p.scale_log2 * kd;
     const int G = p.group;
-    unsigned char* qhi = sm + kOffQ;
-    unsigned char* qlo = qhi + kQPart;
-    int it = 0, piece_idx = 0;
+    unsigned char* qs = sm + kOffQ;
+    int it = 0, piece_idx = 0, xpar = 0;
     int j = j_first;
     long long ts = ts_first;
     Piece pc;
     bool ok = true;
     // Every lane waits; the outcome is made warp-uniform so that a timeout can
     // never split the warp in front of a .sync.aligned tcgen05 instruction.
+    // (Both warps of a quadrant see the same barriers, so both fail together.)
     auto wait_or_fail = [&](int b, uint32_t par, int code) {
       if (!ok) return false;
       const bool got = __all_sync(0xffffffffu, mbar_wait(bar(b), par, abort_flag, kWaitLimitNs));
@@ -366,56 +443,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return ok;
     };
+    // Row-wide combine of a per-thread value: lanes t and t^16 share a row in
+    // this warp, the partner warp of the quadrant holds the other half. The
+    // exchange goes through shared memory (double-buffered by round parity)
+    // and a per-quadrant mbarrier that all 64 threads arrive on, so waits stay
+    // bounded and both warps give up together.
+    auto exchange = [&](float v, bool is_max) {
+      v = is_max ? fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16)) : v + __shfl_xor_sync(0xffffffffu, v, 16);
+      if (sub == 0) xch[(xpar * 2 + kh) * 64 + r] = v;
+      mbar_arrive(bar(kBarX + q));
+      if (!wait_or_fail(kBarX + q, (uint32_t)xpar, 8192)) return v;
+      const float other = xch[(xpar * 2 + (kh ^ 1)) * 64 + r];
+      xpar ^= 1;
+      return is_max ? fmaxf(v, other) : v + other;
+    };
+    auto row_max = [&](float v) { return exchange(v, true); };
+    auto row_sum = [&](float v) { return exchange(v, false); };
     while (ok && next_piece(p, t0, t1, j, ts, pc)) {
-      // -- Q tile: per-row power-of-two scale, e4m3 hi/lo split, swizzled store
+      // -- Q tile into the swizzled K-major A operand; this thread: d [64 qtr, +64)
       if (piece_idx > 0 && !wait_or_fail(kBarQFree, (piece_idx - 1) & 1, 128)) break;
       const bool row_ok = r < pc.R;
       const int tq = row_ok ? r / G : 0;
       const int gq = row_ok ? r - tq * G : 0;
       float rs = 0.f;
       {
-        uint4 raw[16];
-        const uint16_t* src = p.q + (int64_t)(pc.q0 + tq) * p.q_s0 + (int64_t)(pc.kvh * G + gq) * p.q_s1 + 128 * hf;
-        float amax = 0.f;
+        uint4 raw[8];  // 64 bf16
+        const uint16_t* src = p.q + (int64_t)(pc.q0 + tq) * p.q_s0 + (int64_t)(pc.kvh * G + gq) * p.q_s1 + 64 * qtr;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i)
           raw[i] = row_ok ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0, 0, 0, 0);
-          const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+        if constexpr (FP8) {
+          float amax = 0.f;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            amax = fmaxf(amax, fabsf(__uint_as_float(w4[k] << 16)));
-            amax = fmaxf(amax, fabsf(__uint_as_float(w4[k] & 0xFFFF0000u)));
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              amax = fmaxf(amax, fabsf(__uint_as_float(w4[k] << 16)));
+              amax = fmaxf(amax, fabsf(__uint_as_float(w4[k] & 0xFFFF0000u)));
+            }
           }
-        }
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
-        int e = 0;
-        if (amax > 0.f && amax < INFINITY) {
-          const int E = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
-          e = 7 - E;
-          e = e < -120 ? -120 : (e > 120 ? 120 : e);
-        }
-        const float up = __uint_as_float((uint32_t)(e + 127) << 23);
-        const float down = __uint_as_float((uint32_t)(127 - e) << 23);
-        rs = row_ok ? cscale * down : 0.f;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {  // 16 d values -> 16 bytes hi, 16 bytes lo
-          uint32_t hw[4], lw[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint4 a = raw[2 * cc + (k >> 1)];
-            const uint32_t wa = (k & 1) ? a.z : a.x;
-            const uint32_t wb = (k & 1) ? a.w : a.y;
-            const float x0 = __uint_as_float(wa << 16) * up, x1 = __uint_as_float(wa & 0xFFFF0000u) * up;
-            const float x2 = __uint_as_float(wb << 16) * up, x3 = __uint_as_float(wb & 0xFFFF0000u) * up;
-            const uint32_t h01 = pack_fp8x2(x0, x1), h23 = pack_fp8x2(x2, x3);
-            const float2 f01 = unpack_fp8x2(h01), f23 = unpack_fp8x2(h23);
-            const uint32_t l01 = pack_fp8x2(x0 - f01.x, x1 - f01.y), l23 = pack_fp8x2(x2 - f23.x, x3 - f23.y);
-            hw[k] = h01 | (h23 << 16);
-            lw[k] = l01 | (l23 << 16);
+          amax = row_max(amax);
+          if (!ok) break;
+          int e = 0;
+          if (amax > 0.f && amax < INFINITY) {
+            const int E = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+            e = 7 - E;
+            e = e < -120 ? -120 : (e > 120 ? 120 : e);
           }
-          const int off = hf * 8192 + r * 128 + ((cc ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(qhi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(qlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          const float up = __uint_as_float((uint32_t)(e + 127) << 23);
+          const float down = __uint_as_float((uint32_t)(127 - e) << 23);
+          rs = row_ok ? cscale * down : 0.f;
+          unsigned char* qhi = qs;
+          unsigned char* qlo = qs + C::kQPart;
+          // d [64 qtr, +64) = region kh (128 bytes per row), 16-byte pieces 4 sub .. 4 sub + 3
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint4 a = raw[2 * cc + (k >> 1)];
+              const uint32_t wa = (k & 1) ? a.z : a.x;
+              const uint32_t wb = (k & 1) ? a.w : a.y;
+              const float x0 = __uint_as_float(wa << 16) * up, x1 = __uint_as_float(wa & 0xFFFF0000u) * up;
+              const float x2 = __uint_as_float(wb << 16) * up, x3 = __uint_as_float(wb & 0xFFFF0000u) * up;
+              const uint32_t h01 = pack_fp8x2(x0, x1), h23 = pack_fp8x2(x2, x3);
+              const float2 f01 = unpack_fp8x2(h01), f23 = unpack_fp8x2(h23);
+              const uint32_t l01 = pack_fp8x2(x0 - f01.x, x1 - f01.y), l23 = pack_fp8x2(x2 - f23.x, x3 - f23.y);
+              hw[k] = h01 | (h23 << 16);
+              lw[k] = l01 | (l23 << 16);
+            }
+            const int piece16 = 4 * sub + cc;
+            const int off = kh * 8192 + r * 128 + ((piece16 ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(qhi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(qlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+        } else {
+          rs = row_ok ? cscale : 0.f;
+          // d [64 qtr, +64) = one whole 128-byte region (qtr), eight 16-byte pieces
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int off = qtr * 8192 + r * 128 + ((i ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(qs + off) = raw[i];
+          }
         }
       }
       fence_proxy_async_smem();
@@ -429,118 +539,132 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int first = it;
       for (int lt = pc.lt0; lt < pc.lt1; ++lt, ++it) {
         const int cur = it;
-        const int b = cur & 1;
+        const int b = cur & (kSBufs - 1);
+        const int pb = cur & 1;
         const int s = cur % kStages;
-        if (!wait_or_fail(kBarSFull + b, (cur >> 1) & 1, 256)) break;
+        if (!wait_or_fail(kBarSFull + b, (cur / kSBufs) & 1, 256)) break;
         tc_fence_after();
-        uint32_t sr[32];
-        tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kColS + b * kT, sr);
+        uint32_t sr[C::kQuarter];
+        tmem_ld_s<C::kQuarter>(tmem + lane_base + kColS + b * kT + kh * (kT / 2), sr);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarSFree + b));
 
-        float x[32];
-        const int key0 = lt * kT + 32 * hf;
+        float x[C::kQuarter];
+        const int key0 = lt * kT + C::kQuarter * qtr;
         const bool tail = lt * kT + kT - 1 > pc.S - pc.L;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < C::kQuarter; ++i) {
           x[i] = __uint_as_float(sr[i]) * rs;
           if (tail && key0 + i > vis_end) x[i] = -INFINITY;
         }
-        float tmax = x[0];
+        float tmax = -INFINITY;
 #pragma unroll
-        for (int i = 1; i < 32; ++i) tmax = fmaxf(tmax, x[i]);
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+        for (int i = 0; i < C::kQuarter; i += 2) tmax = fmaxf(tmax, fmaxf(x[i], x[i + 1]));
+        tmax = row_max(tmax);
+        if (!ok) break;
 
-        // P buffer b was last read by PV(cur - 2)
-        if (cur >= 2 && !wait_or_fail(kBarPFree + b, ((cur - 2) >> 1) & 1, 512)) break;
+        // P buffer pb was last read by PV(cur - 2)
+        if (cur >= 2 && !wait_or_fail(kBarPFree + pb, ((cur - 2) >> 1) & 1, 512)) break;
 
-        const bool need = tmax > m_ref + 0.3f;
-        const float m_new = need ? tmax + 0.5f : m_ref;
+        const bool need = tmax > m_ref + kOvershoot;
+        const float m_new = need ? tmax + kHeadroom : m_ref;
         const bool rescale = need && (m_ref != -INFINITY) && (cur > first);
-        const float alpha = rescale ? exp2f(m_ref - m_new) : 1.f;
+        const float alpha = rescale ? ex2(m_ref - m_new) : 1.f;
         if (__any_sync(0xffffffffu, rescale)) {
-          // O holds earlier tiles of this piece: wait for PV(cur - 1), scale rows in TMEM
+          // O holds earlier tiles of this piece: wait for PV(cur - 1), scale my
+          // 64 columns of my row in TMEM
           if (!wait_or_fail(kBarPFree + ((cur - 1) & 1), ((cur - 1) >> 1) & 1, 1024)) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < 2; ++k) {
             uint32_t o[32];
-            const uint32_t ta = tmem + lane_base + kColO + 32 * k;
-            tmem_ld_16x32bx2_x32<128>(ta, o);
+            const uint32_t ta = tmem + lane_base + kColO + 128 * kh + 32 * k;
+            tmem_ld_16x32bx2_x32<64>(ta, o);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st_16x32bx2_x32<128>(ta, o);
+            tmem_st_16x32bx2_x32<64>(ta, o);
           }
           tmem_wait_st();
         }
         l *= alpha;
         m_ref = m_new;
 
-        // P = 2^(x - m_ref + 8), split into e4m3 hi/lo, K-major no-swizzle layout
-        const float mref8 = m_ref - 8.f;
+        // P = 2^(x - m_ref + kPShift) into the K-major no-swizzle A operand:
+        // row r, keys [kQuarter qtr, +kQuarter) = 16 bytes = core-matrix column qtr
+        const float mref_s = m_ref - kPShift;
         const bool live = m_ref != -INFINITY;
-        uint32_t ph[8], pl[8];
-        float lsum = 0.f;
+        const int off0 = (r >> 3) * 512 + qtr * 128 + (r & 7) * 16;
+        float ls0 = 0.f, ls1 = 0.f;
+        if constexpr (FP8) {
+          uint32_t ph[4], pl[4];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = live ? exp2f(x[2 * i] - mref8) : 0.f;
-          const float bb = live ? exp2f(x[2 * i + 1] - mref8) : 0.f;
-          lsum += a + bb;
-          uint32_t h2, l2;
-          split_p(a, bb, h2, l2);
-          if (i & 1) {
-            ph[i >> 1] |= h2 << 16;
-            pl[i >> 1] |= l2 << 16;
-          } else {
-            ph[i >> 1] = h2;
-            pl[i >> 1] = l2;
+          for (int i = 0; i < 8; ++i) {
+            const float a = live ? ex2(x[2 * i] - mref_s) : 0.f;
+            const float bb = live ? ex2(x[2 * i + 1] - mref_s) : 0.f;
+            ls0 += a;
+            ls1 += bb;
+            uint32_t h2, l2;
+            split_p(a, bb, h2, l2);
+            if (i & 1) {
+              ph[i >> 1] |= h2 << 16;
+              pl[i >> 1] |= l2 << 16;
+            } else {
+              ph[i >> 1] = h2;
+              pl[i >> 1] = l2;
+            }
           }
+          *reinterpret_cast<uint4*>(sm + kOffP + (pb * 2 + 0) * C::kPPart + off0) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+          *reinterpret_cast<uint4*>(sm + kOffP + (pb * 2 + 1) * C::kPPart + off0) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        } else {
+          uint32_t pw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float a = live ? ex2(x[2 * i] - mref_s) : 0.f;
+            const float bb = live ? ex2(x[2 * i + 1] - mref_s) : 0.f;
+            ls0 += a;
+            ls1 += bb;
+            pw[i] = pack_bf16x2(a, bb);
+          }
+          *reinterpret_cast<uint4*>(sm + kOffP + (pb * 2) * C::kPPart + off0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         }
-        l += lsum;
-        {
-          unsigned char* pbh = sm + kOffP + (b * 2 + 0) * kPPart;
-          unsigned char* pbl = sm + kOffP + (b * 2 + 1) * kPPart;
-          const int off0 = (r >> 3) * 512 + (2 * hf) * 128 + (r & 7) * 16;
-          *reinterpret_cast<uint4*>(pbh + off0) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-          *reinterpret_cast<uint4*>(pbh + off0 + 128) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
-          *reinterpret_cast<uint4*>(pbl + off0) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-          *reinterpret_cast<uint4*>(pbl + off0 + 128) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
-        }
+        l += ls0 + ls1;
         // last tile of the item: V rows past S (partial page, pages never loaded)
         // are zeroed so that 0 * garbage cannot reach O
         if (lt == pc.nt - 1 && (pc.S % kT) != 0) {
           if (!wait_or_fail(kBarFullV + s, (cur / kStages) & 1, 2048)) break;
           const int z0 = pc.S - lt * kT;
           const int nz = kT - z0;
-          unsigned char* vst = sm + s * kStageBytes + kStageBytes / 2;
-          for (int idx = tid - 128; idx < nz * 16; idx += 128) {
-            const int row = z0 + (idx >> 4);
-            const int h = (idx >> 3) & 1;
-            const int ch = idx & 7;
-            *reinterpret_cast<uint4*>(vst + h * 8192 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+          unsigned char* vst = sm + s * C::kStageBytes + C::kTensorBytes;
+          for (int idx = tid - 128; idx < nz * 8 * C::kChunks; idx += kSoftmaxThreads) {
+            const int row = z0 + idx / (8 * C::kChunks);
+            const int rem = idx % (8 * C::kChunks);
+            const int ch = rem >> 3;
+            const int piece16 = rem & 7;
+            *reinterpret_cast<uint4*>(vst + ch * C::kRegion + row * 128 + piece16 * 16) = make_uint4(0, 0, 0, 0);
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarPFull + b));
+        if (lane == 0) mbar_arrive(bar(kBarPFull + pb));
       }
       if (!ok) break;
 
-      // -- epilogue
+      // -- epilogue: this thread holds O[r][128 kh + 64 sub, +64)
       if (!wait_or_fail(kBarOFull, piece_idx & 1, 4096)) break;
       tc_fence_after();
-      const float lrow = l + __shfl_xor_sync(0xffffffffu, l, 16);
+      const float lrow = row_sum(l);
+      if (!ok) break;
       const float inv = lrow > 0.f ? vd / lrow : 0.f;
       const int64_t piece = (int64_t)pc.j + c;
 #pragma unroll 1
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 2; ++k) {
         uint32_t o[32];
-        tmem_ld_16x32bx2_x32<128>(tmem + lane_base + kColO + 32 * k, o);
+        tmem_ld_16x32bx2_x32<64>(tmem + lane_base + kColO + 128 * kh + 32 * k, o);
         tmem_wait_ld();
-        const int col = 128 * hf + 32 * k;
+        const int col = 128 * kh + 64 * sub + 32 * k;
         if (row_ok) {
           if (pc.direct) {
             uint16_t* dst = p.out + (int64_t)(pc.q0 + tq) * p.o_s0 + (int64_t)(pc.kvh * G + gq) * p.o_s1 + col;
@@ -548,11 +672,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int v4 = 0; v4 < 4; ++v4) {
               uint32_t w[4];
 #pragma unroll
-              for (int e2 = 0; e2 < 4; ++e2) {
-                const float y0 = __uint_as_float(o[v4 * 8 + 2 * e2]) * inv;
-                const float y1 = __uint_as_float(o[v4 * 8 + 2 * e2 + 1]) * inv;
-                w[e2] = (uint32_t)float_to_bf16_bits(y0) | ((uint32_t)float_to_bf16_bits(y1) << 16);
-              }
+              for (int e2 = 0; e2 < 4; ++e2)
+                w[e2] = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2 * e2]) * inv,
+                                    __uint_as_float(o[v4 * 8 + 2 * e2 + 1]) * inv);
               reinterpret_cast<uint4*>(dst)[v4] = make_uint4(w[0], w[1], w[2], w[3]);
             }
           } else {
@@ -565,8 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (row_ok && !pc.direct && hf == 0) {
-        p.ws_ml[(piece * p.max_rows + r) * 2 + 0] = (m_ref == -INFINITY) ? -INFINITY : m_ref - 8.f;
+      if (row_ok && !pc.direct && kh == 0 && sub == 0) {
+        p.ws_ml[(piece * p.max_rows + r) * 2 + 0] = (m_ref == -INFINITY) ? -INFINITY : m_ref - kPShift;
         p.ws_ml[(piece * p.max_rows + r) * 2 + 1] = lrow;
       }
       tc_fence_before();
@@ -582,16 +704,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+static_assert(Cfg<true>::kStageBytes == 32768 && Cfg<false>::kStageBytes == 32768, "stage size");
+static_assert(2 * Cfg<true>::kQPart == 32768 && Cfg<false>::kQPart == 32768, "Q size");
+static_assert(4 * Cfg<true>::kPPart <= 16384 && 2 * Cfg<false>::kPPart <= 16384, "P size");
+static_assert(kColS + kSBufs * Cfg<true>::kT <= kTmemCols, "TMEM columns");
+static_assert(kSmemBytes <= 232448, "shared memory");
+
 }  // namespace
 
 cudaError_t prepare_main_tc() {
-  return cudaFuncSetAttribute(va_main_tc_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(va_main_tc_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(va_main_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemBytes);
 }
 
-cudaError_t launch_main_tc_fp8(const Params& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                               cudaStream_t stream) {
-  va_main_tc_fp8_kernel<<<p.num_splits, kThreads, kSmemBytes, stream>>>(p, tm_k, tm_v);
+cudaError_t launch_main_tc(const Params& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                           cudaStream_t stream) {
+  if (p.kv_fp8)
+    va_main_tc_kernel<true><<<p.num_splits, kThreads, kSmemBytes, stream>>>(p, tm_k, tm_v);
+  else
+    va_main_tc_kernel<false><<<p.num_splits, kThreads, kSmemBytes, stream>>>(p, tm_k, tm_v);
   return cudaGetLastError();
 }
 
