@@ -3,7 +3,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/verify_attn.h"
+#include "verify_attn.h"
 #include "va_internal.h"
 
 #define VA_EXPORT extern "C" __attribute__((visibility("default")))

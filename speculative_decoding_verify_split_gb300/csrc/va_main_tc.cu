@@ -1,33 +1,38 @@
 // Split-KV main kernel on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
-// Same decomposition and partial format as the CUDA-core kernel: one CTA per
-// SM takes an equal share of the batch's key tiles, and for every
-// (sequence, KV head) in its share packs all G query heads x L draft tokens
-// (<= 64 rows) into one M=64 tile, so each KV page is read from HBM once per
-// KV head (sglang PR 30105 digest, "Implementation breakdown" item 2; sglang
-// PR 34517 digest, "Motivation": one KV load shared by the heads of a group).
+// One CTA per SM takes an equal share of the batch's 64-key tiles, and for
+// every (sequence, KV head) in its share packs all G query heads x L draft
+// tokens (<= 64 rows) into one MMA tile, so each KV page is read from HBM once
+// per KV head (sglang PR 30105 digest, "Implementation breakdown" item 2;
+// sglang PR 34517 digest, "Motivation": one KV load shared by the heads of a
+// group).
 //
 // KV pages are TMA-loaded as 128-byte-swizzled boxes (16 tokens x 128 bytes
-// of one KV head) into a 5-stage ring and fed to the tensor cores as they are:
-//  * FP8 E4M3 cache, kind::f8f6f4, 64-key tiles. Q (bf16) is scaled per row
-//    by an exact power of two 2^e and split into two e4m3 terms,
-//    Qh = e4m3(Q 2^e), Ql = e4m3(Q 2^e - Qh); both MMAs accumulate into the
-//    same fp32 TMEM tile, so the logits carry (Qh + Ql) K with K exact. P is
-//    split the same way into e4m3 hi/lo terms. K and V are never dequantised.
-//  * BF16 cache, kind::f16, 32-key tiles; Q and P in bf16.
+// of one KV head) into a 128 KB ring and fed to the tensor cores as they are.
+//  * FP8 E4M3 cache, kind::f8f6f4. Q (bf16) is scaled per row by an exact
+//    power of two 2^e and split into two e4m3 terms, Qh = e4m3(Q 2^e) and
+//    Ql = e4m3(Q 2^e - Qh); P is split the same way. The two terms are
+//    stacked in one M=128 MMA: packed row 16q + i uses A rows 32q + i (hi)
+//    and 32q + 16 + i (lo), so the hi and lo results land in lanes i and
+//    16 + i of the same TMEM lane quadrant and one lane shuffle adds them.
+//    K and V are never dequantised.
+//  * BF16 cache, kind::f16, M=64 (packed row 16q + i in lane 32q + i).
 // V is the MN-major B operand of O += P V. The k/v descales fold into the
 // logit scale and the output scale.
 //
 // Roles (384 threads):
-//  warp 0      TMA producer: block-table walk (32 page ids per lane load).
-//  warp 1      TMEM owner and MMA issuer (one thread). QK^T runs up to two
-//              tiles ahead of P V through four S buffers in TMEM.
-//  warps 4-11  softmax, two warps per TMEM lane quadrant (same SMSP, so they
-//              hide each other's latency). Warp w owns packed rows
-//              16(w%4) .. +15 (the M=64 accumulator puts them in TMEM lanes
-//              32(w%4) .. +15), half kh = (w-4)/4 of each tile's keys and of
-//              O's columns; lane bit 4 splits that half again. The two warps
-//              of a quadrant exchange row maxima through shared memory.
+//  warps 0,2,3 TMA producers (FP8: three, BF16: two, never more than the
+//              stages), tiles round-robin: block-table walk (32 page ids per
+//              lane load), one 2 KB box per lane.
+//  warp 1      TMEM owner and MMA issuer (one thread). Q K^T runs ahead of
+//              P V (two tiles for FP8, one for BF16) through four S buffers
+//              in TMEM; P has four buffers in shared memory.
+//  warps 4-11  softmax, two warps per TMEM lane quadrant q = w % 4 (both on
+//              the same SMSP). Warp half kh = (w - 4) / 4 takes keys
+//              [32 kh, 32 kh + 32) of each tile and O columns
+//              [128 kh, 128 kh + 128); lane bit 4 splits those again, so a
+//              thread owns 16 keys of one packed row. The two warps of a
+//              quadrant combine row maxima and sums through shared memory.
 // Online softmax in log2 units keeps a per-row reference m_ref and computes
 // P = 2^(s - m_ref + 6) <= 2^8.5; m_ref moves (and O, l are rescaled in
 // TMEM) only when a tile's max exceeds it by more than 2.5, so rescales are
@@ -46,58 +51,76 @@ namespace {
 
 using namespace ptx;
 
+constexpr int kT = kTcTileKeys;  // 64 keys per tile, both KV types
+
 template <bool FP8>
 struct Cfg {
-  static constexpr int kT = FP8 ? kTcTileKeys : kTcTileKeysBf16;  // keys per tile
-  static constexpr int kEsize = FP8 ? 1 : 2;                       // bytes per KV element
-  static constexpr int kChunks = kHeadDim * kEsize / 128;          // 128-byte d chunks (2 or 4)
-  static constexpr int kRegion = kT * 128;                         // one d chunk of a K or V tile
-  static constexpr int kTensorBytes = kChunks * kRegion;           // K (or V) tile
-  static constexpr int kStageBytes = 2 * kTensorBytes;             // 32 KB either way
-  static constexpr int kPagesPerTile = kT / kPageSize;
-  static constexpr int kPageBytes = kChunks * 2048;                // one page of one tensor
-  static constexpr int kQParts = FP8 ? 2 : 1;                      // hi/lo e4m3, or bf16
-  static constexpr int kQPart = kChunks * 64 * 128;
-  static constexpr int kPParts = FP8 ? 2 : 1;
-  static constexpr int kPPart = 64 * kT * kEsize;                  // 64 rows x 64 bytes
-  static constexpr int kKeysPerStep = 32 / kEsize;                 // PV keys per MMA (32 bytes)
-  static constexpr int kQuarter = kT / 4;                          // keys per thread per tile
-  static constexpr uint32_t kFmt = FP8 ? 0u : 1u;                  // e4m3 / bf16
-  static constexpr uint32_t kIdQK = instr_desc(kFmt, kFmt, false, kT, 64);
-  static constexpr uint32_t kIdPV = instr_desc(kFmt, kFmt, true, kHeadDim, 64);
+  static constexpr int kEsize = FP8 ? 1 : 2;               // bytes per KV element
+  static constexpr int kChunks = kHeadDim * kEsize / 128;  // 128-byte d chunks (2 or 4)
+  static constexpr int kRegion = kT * 128;                 // one d chunk of a K or V tile: 8 KB
+  static constexpr int kTensorBytes = kChunks * kRegion;   // K (or V) tile
+  static constexpr int kStageBytes = 2 * kTensorBytes;     // 32 KB (fp8) / 64 KB (bf16)
+  static constexpr int kStages = FP8 ? 4 : 2;              // 128 KB ring either way
+  // P V of tile i is issued after Q K^T of tile i + kPvLag; a stage holds
+  // tiles i - kPvLag .. i, so kPvLag < kStages (else Q K^T waits forever for
+  // a stage that only P V can free).
+  static constexpr int kPvLag = FP8 ? 2 : 1;
+  // TMA producer warps, tiles round-robin. A producer's wait for tile i's
+  // stage relies on its own previous wait (tile i - kProducers) to keep the
+  // stage's empty barrier within one phase of the wanted completion, which
+  // holds only while kProducers <= kStages.
+  static constexpr int kProducers = FP8 ? 3 : 2;
+  static_assert(kProducers <= kStages, "producer count exceeds the stage ring");
+  static_assert(kPvLag < kStages, "stage ring too short for the P V lag");
+  static constexpr int kPageBytes = kChunks * 2048;        // one page of one tensor
+  static constexpr int kM = FP8 ? 128 : 64;                // MMA rows
+  static constexpr int kQRegion = kM * 128;                // one 128-byte d chunk of Q
+  static constexpr int kPRowBytes = kT * kEsize;           // 64 (fp8) / 128 (bf16)
+  static constexpr int kPSbo = 8 * kPRowBytes;             // 8-row group stride, no swizzle
+  static constexpr int kPBuf = kM * kPRowBytes;            // 8 KB
+  static constexpr int kQkSteps = 4 * kChunks;             // K-steps of 32 bytes over d
+  static constexpr int kPvSteps = kT * kEsize / 32;        // K-steps of 32 bytes over keys
+  static constexpr int kKeysPerPvStep = 32 / kEsize;
+  static constexpr uint32_t kFmt = FP8 ? 0u : 1u;          // e4m3 / bf16
+  static constexpr uint32_t kIdQK = instr_desc(kFmt, kFmt, false, kT, kM);
+  static constexpr uint32_t kIdPV = instr_desc(kFmt, kFmt, true, kHeadDim, kM);
+  static_assert(kStages * kStageBytes == 131072, "ring size");
+  static_assert(kChunks * kQRegion == 32768, "Q size");
+  static_assert(kPBuf == 8192, "P buffer size");
 };
 
-constexpr int kStages = 5;
+constexpr int kPagesPerTile = kT / kPageSize;
 constexpr int kSBufs = 4;
-constexpr int kPvLag = 2;
+constexpr int kPBufs = 4;
 constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;
-constexpr int kOffQ = kStages * 32768;
+constexpr int kOffQ = 131072;
 constexpr int kOffP = kOffQ + 32768;
-constexpr int kOffX = kOffP + 16384;  // row-max exchange: [2 parity][2 kh][64 rows] floats
+constexpr int kOffX = kOffP + kPBufs * 8192;  // row exchange: [2 parity][2 kh][64 rows] floats
 constexpr int kOffBar = kOffX + 1024;
 constexpr int kSmemBytes = kOffBar + 1024 + 1024;
 
 constexpr uint32_t kColO = 0;    // 256 fp32 columns
-constexpr uint32_t kColS = 256;  // four S tiles
+constexpr uint32_t kColS = 256;  // four 64-column S tiles
 constexpr uint32_t kTmemCols = 512;
 
-constexpr float kPShift = 6.f;    // P = 2^(s - m_ref + kPShift)
-constexpr float kHeadroom = 1.f;  // m_ref = tile max + kHeadroom when it moves
+constexpr float kPShift = 6.f;      // P = 2^(s - m_ref + kPShift)
+constexpr float kHeadroom = 1.f;    // m_ref = tile max + kHeadroom when it moves
 constexpr float kOvershoot = 2.5f;  // move only if the tile max > m_ref + kOvershoot
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+constexpr int kMaxStages = 4;
 // Barrier slots (8 bytes each) after kOffBar.
 enum : int {
   kBarFullK = 0,
-  kBarFullV = kBarFullK + kStages,
-  kBarEmpty = kBarFullV + kStages,
-  kBarSFull = kBarEmpty + kStages,
+  kBarFullV = kBarFullK + kMaxStages,
+  kBarEmpty = kBarFullV + kMaxStages,
+  kBarSFull = kBarEmpty + kMaxStages,
   kBarSFree = kBarSFull + kSBufs,
   kBarPFull = kBarSFree + kSBufs,
-  kBarPFree = kBarPFull + 2,
-  kBarQFull = kBarPFree + 2,
+  kBarPFree = kBarPFull + kPBufs,
+  kBarQFull = kBarPFree + kPBufs,
   kBarQFree,
   kBarOFull,
   kBarOFree,
@@ -106,6 +129,8 @@ enum : int {
   kNumBars = kBarX + 4
 };
 static_assert(8 * kNumBars + 16 + 34 * 8 <= 1024, "barrier area");
+static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(kColS + kSBufs * kT <= kTmemCols, "TMEM columns");
 
 struct Piece {
   int j, b, kvh, S, L, q0, R, nt, lt0, lt1;
@@ -168,19 +193,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
 }
 
-// S values of this thread: columns [col, col + n) for lanes 0-15 of the warp,
-// [col + n, col + 2n) for lanes 16-31, n = keys per thread.
-template <int N>
-__device__ __forceinline__ void tmem_ld_s(uint32_t taddr, uint32_t (&r)[N]);
-template <>
-__device__ __forceinline__ void tmem_ld_s<16>(uint32_t taddr, uint32_t (&r)[16]) {
-  tmem_ld_16x32bx2_x16<16>(taddr, r);
-}
-template <>
-__device__ __forceinline__ void tmem_ld_s<8>(uint32_t taddr, uint32_t (&r)[8]) {
-  tmem_ld_16x32bx2_x8<8>(taddr, r);
-}
-
 template <bool FP8>
 __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   if constexpr (FP8)
@@ -194,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     va_main_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v) {
   using C = Cfg<FP8>;
-  constexpr int kT = C::kT;
+  constexpr int kStages = C::kStages;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -238,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarSFull + i), 1);
       mbar_init(bar(kBarSFree + i), kSwWarps);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kPBufs; ++i) {
       mbar_init(bar(kBarPFull + i), kSwWarps);
       mbar_init(bar(kBarPFree + i), 1);
     }
@@ -247,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarOFull), 1);
     mbar_init(bar(kBarOFree), kSwWarps);
     mbar_init(bar(kBarDrain), 1);
-    for (int i = 0; i < 4; ++i) mbar_init(bar(kBarX + i), 64);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(kBarX + i), 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -255,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0 && p.num_blocks > 0) {
+  if (warp == 2 && lane == 0 && p.num_blocks > 0) {
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
@@ -264,8 +276,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ======================= TMA producer =======================================
+  if (warp == 0 || (warp >= 2 && warp < 1 + C::kProducers)) {
+    // ======================= TMA producers ======================================
+    // Several warps take the tiles round-robin: one warp alone cannot issue
+    // the 2 KB page boxes fast enough to keep HBM busy. Within a warp the
+    // lanes issue the tile's boxes in parallel.
+    const int prod = warp == 0 ? 0 : warp - 1;  // 0 .. kProducers - 1
+    constexpr int kBoxes = kPagesPerTile * C::kChunks;  // boxes per tensor per tile
+    static_assert(2 * kBoxes <= 32, "one box per lane");
     int it = 0;
     int j = j_first;
     long long ts = ts_first;
@@ -277,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int win = -1;       // first page index cached in the lanes
       int my_page = -1;   // page id of page (win + lane)
       for (int lt = pc.lt0; lt < pc.lt1 && ok; ++lt, ++it) {
+        if (it % C::kProducers != prod) continue;
         const int s = it % kStages;
         const bool got = __all_sync(
             0xffffffffu, mbar_wait(bar(kBarEmpty + s), ((it / kStages) & 1) ^ 1, abort_flag, kWaitLimitNs));
@@ -285,42 +304,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const int pg0 = lt * C::kPagesPerTile;
-        if (win < 0 || pg0 + C::kPagesPerTile > win + 32) {
+        const int pg0 = lt * kPagesPerTile;
+        if (win < 0 || pg0 + kPagesPerTile > win + 32) {
           win = pg0;
           const int pg = win + lane;
           my_page = pg < npages ? bt_row[(int64_t)pg * p.bt_s1] : -1;
         }
         uint32_t nvalid = 0;
-        int ids[C::kPagesPerTile];
+        int ids[kPagesPerTile];
 #pragma unroll
-        for (int i = 0; i < C::kPagesPerTile; ++i) {
+        for (int i = 0; i < kPagesPerTile; ++i) {
           ids[i] = __shfl_sync(0xffffffffu, my_page, pg0 + i - win);
           const bool v = (pg0 + i) < npages && (unsigned)ids[i] < (unsigned)p.num_blocks;
           ids[i] = v ? ids[i] : -1;
           nvalid += v ? 1u : 0u;
         }
+        const uint32_t kst = sbase + s * C::kStageBytes;
+        const uint32_t vst = kst + C::kTensorBytes;
         if (lane == 0) {
-          const uint32_t kst = sbase + s * C::kStageBytes;
-          const uint32_t vst = kst + C::kTensorBytes;
           mbar_arrive_expect_tx(bar(kBarFullK + s), nvalid * (uint32_t)C::kPageBytes);
-#pragma unroll
-          for (int i = 0; i < C::kPagesPerTile; ++i) {
-            if (ids[i] < 0) continue;
-#pragma unroll
-            for (int ch = 0; ch < C::kChunks; ++ch)
-              tma_load_4d(kst + ch * C::kRegion + i * 2048, &tm_k, ch * (128 / C::kEsize), pc.kvh, 0,
-                          ids[i], bar(kBarFullK + s));
-          }
           mbar_arrive_expect_tx(bar(kBarFullV + s), nvalid * (uint32_t)C::kPageBytes);
+        }
+        __syncwarp();
+        if (lane < 2 * kBoxes) {  // lane -> (tensor, page, 128-byte d chunk)
+          const int tsr = lane / kBoxes, bx = lane % kBoxes;
+          const int i = bx / C::kChunks, ch = bx % C::kChunks;
+          int id = ids[0];
 #pragma unroll
-          for (int i = 0; i < C::kPagesPerTile; ++i) {
-            if (ids[i] < 0) continue;
-#pragma unroll
-            for (int ch = 0; ch < C::kChunks; ++ch)
-              tma_load_4d(vst + ch * C::kRegion + i * 2048, &tm_v, ch * (128 / C::kEsize), pc.kvh, 0,
-                          ids[i], bar(kBarFullV + s));
-          }
+          for (int u = 1; u < kPagesPerTile; ++u)
+            if (i == u) id = ids[u];
+          if (id >= 0)
+            tma_load_4d((tsr ? vst : kst) + ch * C::kRegion + i * 2048, tsr ? &tm_v : &tm_k,
+                        ch * (128 / C::kEsize), pc.kvh, 0, id, bar((tsr ? kBarFullV : kBarFullK) + s));
         }
         __syncwarp();
       }
@@ -328,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) {
       // let copies already in flight land before the CTA goes away
       for (int k = (it > kStages ? it - kStages : 0); k < it; ++k) {
+        if (k % C::kProducers != prod) continue;
         const int s = k % kStages;
         mbar_wait(bar(kBarFullK + s), (k / kStages) & 1, abort_flag, 10000000ull);
         mbar_wait(bar(kBarFullV + s), (k / kStages) & 1, abort_flag, 10000000ull);
@@ -356,23 +372,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_or_fail(kBarQFull, piece_idx & 1, 2)) break;
         tc_fence_after();
         auto issue_pv = [&](int x) {
-          const int pb = x & 1;
+          const int pb = x & (kPBufs - 1);
           const int s = x % kStages;
-          if (!wait_or_fail(kBarPFull + pb, (x >> 1) & 1, 4)) return;
+          if (!wait_or_fail(kBarPFull + pb, (x / kPBufs) & 1, 4)) return;
           if (!wait_or_fail(kBarFullV + s, (x / kStages) & 1, 8)) return;
           if (x == first && piece_idx > 0 && !wait_or_fail(kBarOFree, (piece_idx - 1) & 1, 16)) return;
           tc_fence_after();
           const uint32_t vst = sbase + s * C::kStageBytes + C::kTensorBytes;
+          const uint32_t pbuf = sbase + kOffP + pb * C::kPBuf;
 #pragma unroll
-          for (int part = 0; part < C::kPParts; ++part) {
-            const uint32_t pbuf = sbase + kOffP + (pb * 2 + part) * C::kPPart;
-#pragma unroll
-            for (int kk = 0; kk < kT / C::kKeysPerStep; ++kk) {
-              const uint64_t a = smem_desc(pbuf + kk * 256, 128, 512, kLayoutNone);
-              const uint64_t bdesc = smem_desc(vst + kk * (C::kKeysPerStep / 8) * 1024, C::kRegion,
-                                               1024, kLayoutSw128);
-              mma<FP8>(tmem + kColO, a, bdesc, C::kIdPV, (x == first && part == 0 && kk == 0) ? 0u : 1u);
-            }
+          for (int kk = 0; kk < C::kPvSteps; ++kk) {
+            const uint64_t a = smem_desc(pbuf + kk * 256, 128, C::kPSbo, kLayoutNone);
+            const uint64_t bdesc = smem_desc(vst + kk * (C::kKeysPerPvStep / 8) * 1024, C::kRegion,
+                                             1024, kLayoutSw128);
+            mma<FP8>(tmem + kColO, a, bdesc, C::kIdPV, (x == first && kk == 0) ? 0u : 1u);
           }
           mma_commit(bar(kBarPFree + pb));
           mma_commit(bar(kBarEmpty + s));
@@ -387,22 +400,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t kst = sbase + s * C::kStageBytes;
 #pragma unroll
-          for (int part = 0; part < C::kQParts; ++part) {
-            const uint32_t qb = qbase + part * C::kQPart;
-#pragma unroll
-            for (int k = 0; k < 4 * C::kChunks; ++k) {
-              const uint32_t qoff = (uint32_t)((k >> 2) * 8192 + (k & 3) * 32);
-              const uint32_t koff = (uint32_t)((k >> 2) * C::kRegion + (k & 3) * 32);
-              const uint64_t a = smem_desc(qb + qoff, 16, 1024, kLayoutSw128);
-              const uint64_t bdesc = smem_desc(kst + koff, 16, 1024, kLayoutSw128);
-              mma<FP8>(tmem + kColS + b * kT, a, bdesc, C::kIdQK, (part | k) ? 1u : 0u);
-            }
+          for (int k = 0; k < C::kQkSteps; ++k) {
+            const uint32_t qoff = (uint32_t)((k >> 2) * C::kQRegion + (k & 3) * 32);
+            const uint32_t koff = (uint32_t)((k >> 2) * C::kRegion + (k & 3) * 32);
+            const uint64_t a = smem_desc(qbase + qoff, 16, 1024, kLayoutSw128);
+            const uint64_t bdesc = smem_desc(kst + koff, 16, 1024, kLayoutSw128);
+            mma<FP8>(tmem + kColS + b * kT, a, bdesc, C::kIdQK, k ? 1u : 0u);
           }
           mma_commit(bar(kBarSFull + b));
           if (i == ntile - 1) mma_commit(bar(kBarQFree));
-          if (i >= kPvLag) issue_pv(cur - kPvLag);
+          if (i >= C::kPvLag) issue_pv(cur - C::kPvLag);
         }
-        for (int x = first + (ntile > kPvLag ? ntile - kPvLag : 0); ok && x < first + ntile; ++x)
+        for (int x = first + (ntile > C::kPvLag ? ntile - C::kPvLag : 0); ok && x < first + ntile; ++x)
           issue_pv(x);
         it = first + ntile;
         ++piece_idx;
@@ -419,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sub = lane >> 4;           // which quarter within that half
     const int rl = lane & 15;
     const int r = 16 * q + rl;           // packed row
-    const int qtr = 2 * kh + sub;        // quarter 0..3
+    const int qtr = 2 * kh + sub;        // key quarter 0..3 of a tile
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const float kd = p.k_descale ? *p.k_descale : 1.0f;
     const float vd = p.v_descale ? *p.v_descale : 1.0f;
@@ -433,7 +442,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     // Every lane waits; the outcome is made warp-uniform so that a timeout can
     // never split the warp in front of a .sync.aligned tcgen05 instruction.
-    // (Both warps of a quadrant see the same barriers, so both fail together.)
     auto wait_or_fail = [&](int b, uint32_t par, int code) {
       if (!ok) return false;
       const bool got = __all_sync(0xffffffffu, mbar_wait(bar(b), par, abort_flag, kWaitLimitNs));
@@ -446,19 +454,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Row-wide combine of a per-thread value: lanes t and t^16 share a row in
     // this warp, the partner warp of the quadrant holds the other half. The
     // exchange goes through shared memory (double-buffered by round parity)
-    // and a per-quadrant mbarrier that all 64 threads arrive on, so waits stay
-    // bounded and both warps give up together.
+    // and a per-quadrant mbarrier, so waits stay bounded and both warps give
+    // up together.
     auto exchange = [&](float v, bool is_max) {
       v = is_max ? fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16)) : v + __shfl_xor_sync(0xffffffffu, v, 16);
       if (sub == 0) xch[(xpar * 2 + kh) * 64 + r] = v;
-      mbar_arrive(bar(kBarX + q));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarX + q));
       if (!wait_or_fail(kBarX + q, (uint32_t)xpar, 8192)) return v;
       const float other = xch[(xpar * 2 + (kh ^ 1)) * 64 + r];
       xpar ^= 1;
       return is_max ? fmaxf(v, other) : v + other;
     };
-    auto row_max = [&](float v) { return exchange(v, true); };
-    auto row_sum = [&](float v) { return exchange(v, false); };
     while (ok && next_piece(p, t0, t1, j, ts, pc)) {
       // -- Q tile into the swizzled K-major A operand; this thread: d [64 qtr, +64)
       if (piece_idx > 0 && !wait_or_fail(kBarQFree, (piece_idx - 1) & 1, 128)) break;
@@ -483,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               amax = fmaxf(amax, fabsf(__uint_as_float(w4[k] & 0xFFFF0000u)));
             }
           }
-          amax = row_max(amax);
+          amax = exchange(amax, true);
           if (!ok) break;
           int e = 0;
           if (amax > 0.f && amax < INFINITY) {
@@ -494,9 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float up = __uint_as_float((uint32_t)(e + 127) << 23);
           const float down = __uint_as_float((uint32_t)(127 - e) << 23);
           rs = row_ok ? cscale * down : 0.f;
-          unsigned char* qhi = qs;
-          unsigned char* qlo = qs + C::kQPart;
-          // d [64 qtr, +64) = region kh (128 bytes per row), 16-byte pieces 4 sub .. 4 sub + 3
+          // d [64 qtr, +64) = region kh, 16-byte pieces 4 sub .. 4 sub + 3;
+          // hi to A row 32q + rl, lo to A row 32q + 16 + rl
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t hw[4], lw[4];
@@ -514,16 +520,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               lw[k] = l01 | (l23 << 16);
             }
             const int piece16 = 4 * sub + cc;
-            const int off = kh * 8192 + r * 128 + ((piece16 ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(qhi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(qlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            const int swz = (piece16 ^ (rl & 7)) << 4;
+            const int ahi = 32 * q + rl, alo = ahi + 16;
+            *reinterpret_cast<uint4*>(qs + kh * C::kQRegion + ahi * 128 + swz) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(qs + kh * C::kQRegion + alo * 128 + swz) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
         } else {
           rs = row_ok ? cscale : 0.f;
           // d [64 qtr, +64) = one whole 128-byte region (qtr), eight 16-byte pieces
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int off = qtr * 8192 + r * 128 + ((i ^ (r & 7)) << 4);
+            const int off = qtr * C::kQRegion + r * 128 + ((i ^ (r & 7)) << 4);
             *reinterpret_cast<uint4*>(qs + off) = raw[i];
           }
         }
@@ -540,64 +547,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int lt = pc.lt0; lt < pc.lt1; ++lt, ++it) {
         const int cur = it;
         const int b = cur & (kSBufs - 1);
-        const int pb = cur & 1;
+        const int pb = cur & (kPBufs - 1);
         const int s = cur % kStages;
         if (!wait_or_fail(kBarSFull + b, (cur / kSBufs) & 1, 256)) break;
         tc_fence_after();
-        uint32_t sr[C::kQuarter];
-        tmem_ld_s<C::kQuarter>(tmem + lane_base + kColS + b * kT + kh * (kT / 2), sr);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarSFree + b));
-
-        float x[C::kQuarter];
-        const int key0 = lt * kT + C::kQuarter * qtr;
-        const bool tail = lt * kT + kT - 1 > pc.S - pc.L;
+        float x[16];  // logits of keys [16 qtr, +16) of this tile, this row
+        if constexpr (FP8) {
+          // lane t reads its TMEM lane: hi (t < 16) or lo (t >= 16) partial of
+          // row 16q + rl for keys [32 kh, +32); add the partner's half
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + kColS + b * kT + 32 * kh, v);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarSFree + b));
 #pragma unroll
-        for (int i = 0; i < C::kQuarter; ++i) {
-          x[i] = __uint_as_float(sr[i]) * rs;
-          if (tail && key0 + i > vis_end) x[i] = -INFINITY;
+          for (int i = 0; i < 16; ++i) {
+            const float mine = __uint_as_float(sub ? v[16 + i] : v[i]);
+            const float give = __uint_as_float(sub ? v[i] : v[16 + i]);
+            x[i] = (mine + __shfl_xor_sync(0xffffffffu, give, 16)) * rs;
+          }
+        } else {
+          uint32_t v[16];
+          tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kColS + b * kT + 32 * kh, v);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarSFree + b));
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(v[i]) * rs;
+        }
+        const int key0 = lt * kT + 16 * qtr;
+        if (lt * kT + kT - 1 > pc.S - pc.L) {  // tail tile: causal mask
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (key0 + i > vis_end) x[i] = -INFINITY;
         }
         float tmax = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < C::kQuarter; i += 2) tmax = fmaxf(tmax, fmaxf(x[i], x[i + 1]));
-        tmax = row_max(tmax);
+        for (int i = 0; i < 16; i += 2) tmax = fmaxf(tmax, fmaxf(x[i], x[i + 1]));
+        tmax = exchange(tmax, true);
         if (!ok) break;
 
-        // P buffer pb was last read by PV(cur - 2)
-        if (cur >= 2 && !wait_or_fail(kBarPFree + pb, ((cur - 2) >> 1) & 1, 512)) break;
+        // P buffer pb was last read by PV(cur - kPBufs)
+        if (cur >= kPBufs && !wait_or_fail(kBarPFree + pb, ((cur - kPBufs) / kPBufs) & 1, 512)) break;
 
         const bool need = tmax > m_ref + kOvershoot;
         const float m_new = need ? tmax + kHeadroom : m_ref;
         const bool rescale = need && (m_ref != -INFINITY) && (cur > first);
         const float alpha = rescale ? ex2(m_ref - m_new) : 1.f;
         if (__any_sync(0xffffffffu, rescale)) {
-          // O holds earlier tiles of this piece: wait for PV(cur - 1), scale my
-          // 64 columns of my row in TMEM
-          if (!wait_or_fail(kBarPFree + ((cur - 1) & 1), ((cur - 1) >> 1) & 1, 1024)) break;
+          // O holds earlier tiles of this piece: wait for PV(cur - 1), then
+          // scale this thread's part of the row in TMEM
+          const int xp = cur - 1;
+          if (!wait_or_fail(kBarPFree + (xp & (kPBufs - 1)), (xp / kPBufs) & 1, 1024)) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int k = 0; k < 2; ++k) {
+          for (int k = 0; k < (FP8 ? 4 : 2); ++k) {
             uint32_t o[32];
             const uint32_t ta = tmem + lane_base + kColO + 128 * kh + 32 * k;
-            tmem_ld_16x32bx2_x32<64>(ta, o);
-            tmem_wait_ld();
+            if constexpr (FP8) {
+              tmem_ld_32x32b_x32(ta, o);
+              tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st_16x32bx2_x32<64>(ta, o);
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st_32x32b_x32(ta, o);
+            } else {
+              tmem_ld_16x32bx2_x32<64>(ta, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st_16x32bx2_x32<64>(ta, o);
+            }
           }
           tmem_wait_st();
         }
         l *= alpha;
         m_ref = m_new;
 
-        // P = 2^(x - m_ref + kPShift) into the K-major no-swizzle A operand:
-        // row r, keys [kQuarter qtr, +kQuarter) = 16 bytes = core-matrix column qtr
+        // P = 2^(x - m_ref + kPShift) into the K-major no-swizzle A operand
         const float mref_s = m_ref - kPShift;
         const bool live = m_ref != -INFINITY;
-        const int off0 = (r >> 3) * 512 + qtr * 128 + (r & 7) * 16;
         float ls0 = 0.f, ls1 = 0.f;
+        unsigned char* pbuf = sm + kOffP + pb * C::kPBuf;
         if constexpr (FP8) {
           uint32_t ph[4], pl[4];
 #pragma unroll
@@ -616,19 +648,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               pl[i >> 1] = l2;
             }
           }
-          *reinterpret_cast<uint4*>(sm + kOffP + (pb * 2 + 0) * C::kPPart + off0) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-          *reinterpret_cast<uint4*>(sm + kOffP + (pb * 2 + 1) * C::kPPart + off0) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+          // keys [16 qtr, +16) = 16-byte core-matrix column qtr of A rows
+          // 32q + rl (hi) and 32q + 16 + rl (lo)
+          const int ahi = 32 * q + rl, alo = ahi + 16;
+          *reinterpret_cast<uint4*>(pbuf + (ahi >> 3) * C::kPSbo + qtr * 128 + (ahi & 7) * 16) =
+              make_uint4(ph[0], ph[1], ph[2], ph[3]);
+          *reinterpret_cast<uint4*>(pbuf + (alo >> 3) * C::kPSbo + qtr * 128 + (alo & 7) * 16) =
+              make_uint4(pl[0], pl[1], pl[2], pl[3]);
         } else {
-          uint32_t pw[4];
+          uint32_t pw[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < 8; ++i) {
             const float a = live ? ex2(x[2 * i] - mref_s) : 0.f;
             const float bb = live ? ex2(x[2 * i + 1] - mref_s) : 0.f;
             ls0 += a;
             ls1 += bb;
             pw[i] = pack_bf16x2(a, bb);
           }
-          *reinterpret_cast<uint4*>(sm + kOffP + (pb * 2) * C::kPPart + off0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          // keys [16 qtr, +16) = 32 bytes = core-matrix columns 2 qtr, 2 qtr + 1 of row r
+          unsigned char* base = pbuf + (r >> 3) * C::kPSbo + (2 * qtr) * 128 + (r & 7) * 16;
+          *reinterpret_cast<uint4*>(base) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          *reinterpret_cast<uint4*>(base + 128) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
         }
         l += ls0 + ls1;
         // last tile of the item: V rows past S (partial page, pages never loaded)
@@ -652,39 +692,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
 
-      // -- epilogue: this thread holds O[r][128 kh + 64 sub, +64)
+      // -- epilogue: this thread writes O[r][128 kh + 64 sub, +64)
       if (!wait_or_fail(kBarOFull, piece_idx & 1, 4096)) break;
       tc_fence_after();
-      const float lrow = row_sum(l);
+      const float lrow = exchange(l, false);
       if (!ok) break;
       const float inv = lrow > 0.f ? vd / lrow : 0.f;
       const int64_t piece = (int64_t)pc.j + c;
-#pragma unroll 1
-      for (int k = 0; k < 2; ++k) {
-        uint32_t o[32];
-        tmem_ld_16x32bx2_x32<64>(tmem + lane_base + kColO + 128 * kh + 32 * k, o);
-        tmem_wait_ld();
-        const int col = 128 * kh + 64 * sub + 32 * k;
-        if (row_ok) {
-          if (pc.direct) {
-            uint16_t* dst = p.out + (int64_t)(pc.q0 + tq) * p.o_s0 + (int64_t)(pc.kvh * G + gq) * p.o_s1 + col;
+      auto emit = [&](const uint32_t (&o)[32], int col) {
+        if (!row_ok) return;
+        if (pc.direct) {
+          uint16_t* dst = p.out + (int64_t)(pc.q0 + tq) * p.o_s0 + (int64_t)(pc.kvh * G + gq) * p.o_s1 + col;
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint32_t w[4];
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint32_t w[4];
 #pragma unroll
-              for (int e2 = 0; e2 < 4; ++e2)
-                w[e2] = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2 * e2]) * inv,
-                                    __uint_as_float(o[v4 * 8 + 2 * e2 + 1]) * inv);
-              reinterpret_cast<uint4*>(dst)[v4] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          } else {
-            float* dst = p.ws_acc + (piece * p.max_rows + r) * kHeadDim + col;
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              reinterpret_cast<float4*>(dst)[v4] =
-                  make_float4(__uint_as_float(o[4 * v4]), __uint_as_float(o[4 * v4 + 1]),
-                              __uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3]));
+            for (int e2 = 0; e2 < 4; ++e2)
+              w[e2] = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2 * e2]) * inv,
+                                  __uint_as_float(o[v4 * 8 + 2 * e2 + 1]) * inv);
+            reinterpret_cast<uint4*>(dst)[v4] = make_uint4(w[0], w[1], w[2], w[3]);
           }
+        } else {
+          float* dst = p.ws_acc + (piece * p.max_rows + r) * kHeadDim + col;
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            reinterpret_cast<float4*>(dst)[v4] =
+                make_float4(__uint_as_float(o[4 * v4]), __uint_as_float(o[4 * v4 + 1]),
+                            __uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3]));
+        }
+      };
+      if constexpr (FP8) {
+        // own lane holds the hi (sub 0) or lo (sub 1) part of all 128 columns
+        // of the half; add the partner's and keep chunks 2 sub, 2 sub + 1
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + kColO + 128 * kh + 32 * k, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            o[i] = __float_as_uint(__uint_as_float(o[i]) +
+                                   __shfl_xor_sync(0xffffffffu, __uint_as_float(o[i]), 16));
+          if ((k >> 1) == sub) emit(o, 128 * kh + 32 * k);
+        }
+      } else {
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+          uint32_t o[32];
+          tmem_ld_16x32bx2_x32<64>(tmem + lane_base + kColO + 128 * kh + 32 * k, o);
+          tmem_wait_ld();
+          emit(o, 128 * kh + 64 * sub + 32 * k);
         }
       }
       if (row_ok && !pc.direct && kh == 0 && sub == 0) {
@@ -703,12 +760,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
-
-static_assert(Cfg<true>::kStageBytes == 32768 && Cfg<false>::kStageBytes == 32768, "stage size");
-static_assert(2 * Cfg<true>::kQPart == 32768 && Cfg<false>::kQPart == 32768, "Q size");
-static_assert(4 * Cfg<true>::kPPart <= 16384 && 2 * Cfg<false>::kPPart <= 16384, "P size");
-static_assert(kColS + kSBufs * Cfg<true>::kT <= kTmemCols, "TMEM columns");
-static_assert(kSmemBytes <= 232448, "shared memory");
 
 }  // namespace
 
