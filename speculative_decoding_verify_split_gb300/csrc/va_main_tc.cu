@@ -21,12 +21,13 @@
 // logit scale and the output scale.
 //
 // Roles (384 threads):
-//  warps 0,2,3 TMA producers (FP8: three, BF16: two, never more than the
-//              stages), tiles round-robin: block-table walk (32 page ids per
-//              lane load), one 2 KB box per lane.
-//  warp 1      TMEM owner and MMA issuer (one thread). Q K^T runs ahead of
-//              P V (two tiles for FP8, one for BF16) through four S buffers
-//              in TMEM; P has four buffers in shared memory.
+//  warps 0,2,3 TMA producers: warp 0 streams K tiles into a K ring (freed
+//              once Q K^T has read them), warps 2 and 3 alternate on V tiles
+//              (V ring, freed after P V). Block-table walk with 32 page ids
+//              per lane load; one 2 KB box per lane.
+//  warp 1      TMEM owner and MMA issuer (one thread). Q K^T of tile i is
+//              issued before P V of tile i - 1, through four S buffers in
+//              TMEM; P has four buffers in shared memory.
 //  warps 4-11  softmax, two warps per TMEM lane quadrant q = w % 4 (both on
 //              the same SMSP). Warp half kh = (w - 4) / 4 takes keys
 //              [32 kh, 32 kh + 32) of each tile and O columns
@@ -58,20 +59,17 @@ struct Cfg {
   static constexpr int kEsize = FP8 ? 1 : 2;               // bytes per KV element
   static constexpr int kChunks = kHeadDim * kEsize / 128;  // 128-byte d chunks (2 or 4)
   static constexpr int kRegion = kT * 128;                 // one d chunk of a K or V tile: 8 KB
-  static constexpr int kTensorBytes = kChunks * kRegion;   // K (or V) tile
-  static constexpr int kStageBytes = 2 * kTensorBytes;     // 32 KB (fp8) / 64 KB (bf16)
-  static constexpr int kStages = FP8 ? 4 : 2;              // 128 KB ring either way
-  // P V of tile i is issued after Q K^T of tile i + kPvLag; a stage holds
-  // tiles i - kPvLag .. i, so kPvLag < kStages (else Q K^T waits forever for
-  // a stage that only P V can free).
-  static constexpr int kPvLag = FP8 ? 2 : 1;
-  // TMA producer warps, tiles round-robin. A producer's wait for tile i's
-  // stage relies on its own previous wait (tile i - kProducers) to keep the
-  // stage's empty barrier within one phase of the wanted completion, which
-  // holds only while kProducers <= kStages.
-  static constexpr int kProducers = FP8 ? 3 : 2;
-  static_assert(kProducers <= kStages, "producer count exceeds the stage ring");
-  static_assert(kPvLag < kStages, "stage ring too short for the P V lag");
+  static constexpr int kTensorBytes = kChunks * kRegion;   // a K or V tile: 16 KB / 32 KB
+  // Separate K and V rings: a K slot is free again once Q K^T has read it,
+  // a V slot only after P V, so V gets the deeper ring. 128 KB in all.
+  static constexpr int kKSlots = FP8 ? 3 : 2;
+  static constexpr int kVSlots = FP8 ? 5 : 2;
+  // Producer warps: one streams K, two alternate on V's tiles. A producer's
+  // wait for a slot relies on its own previous wait (kVProducers tiles back)
+  // to keep that slot's empty barrier within one phase of the wanted
+  // completion, which holds while the producers of a ring <= its slots.
+  static constexpr int kVProducers = 2;
+  static_assert(kVProducers <= kVSlots, "V producers exceed the V ring");
   static constexpr int kPageBytes = kChunks * 2048;        // one page of one tensor
   static constexpr int kM = FP8 ? 128 : 64;                // MMA rows
   static constexpr int kQRegion = kM * 128;                // one 128-byte d chunk of Q
@@ -84,7 +82,7 @@ struct Cfg {
   static constexpr uint32_t kFmt = FP8 ? 0u : 1u;          // e4m3 / bf16
   static constexpr uint32_t kIdQK = instr_desc(kFmt, kFmt, false, kT, kM);
   static constexpr uint32_t kIdPV = instr_desc(kFmt, kFmt, true, kHeadDim, kM);
-  static_assert(kStages * kStageBytes == 131072, "ring size");
+  static_assert((kKSlots + kVSlots) * kTensorBytes == 131072, "ring size");
   static_assert(kChunks * kQRegion == 32768, "Q size");
   static_assert(kPBuf == 8192, "P buffer size");
 };
@@ -110,13 +108,14 @@ constexpr float kOvershoot = 2.5f;  // move only if the tile max > m_ref + kOver
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
-constexpr int kMaxStages = 4;
+constexpr int kMaxSlots = 5;
 // Barrier slots (8 bytes each) after kOffBar.
 enum : int {
   kBarFullK = 0,
-  kBarFullV = kBarFullK + kMaxStages,
-  kBarEmpty = kBarFullV + kMaxStages,
-  kBarSFull = kBarEmpty + kMaxStages,
+  kBarEmptyK = kBarFullK + kMaxSlots,
+  kBarFullV = kBarEmptyK + kMaxSlots,
+  kBarEmptyV = kBarFullV + kMaxSlots,
+  kBarSFull = kBarEmptyV + kMaxSlots,
   kBarSFree = kBarSFull + kSBufs,
   kBarPFull = kBarSFree + kSBufs,
   kBarPFree = kBarPFull + kPBufs,
@@ -206,7 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     va_main_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v) {
   using C = Cfg<FP8>;
-  constexpr int kStages = C::kStages;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -241,10 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- setup --------------------------------------------------------------------
   constexpr uint32_t kSwWarps = kSoftmaxThreads / 32;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::kKSlots; ++s) {
       mbar_init(bar(kBarFullK + s), 1);
+      mbar_init(bar(kBarEmptyK + s), 1);
+    }
+    for (int s = 0; s < C::kVSlots; ++s) {
       mbar_init(bar(kBarFullV + s), 1);
-      mbar_init(bar(kBarEmpty + s), 1);
+      mbar_init(bar(kBarEmptyV + s), 1);
     }
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
@@ -276,14 +277,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 || (warp >= 2 && warp < 1 + C::kProducers)) {
+  if (warp == 0 || warp == 2 || warp == 3) {
     // ======================= TMA producers ======================================
-    // Several warps take the tiles round-robin: one warp alone cannot issue
-    // the 2 KB page boxes fast enough to keep HBM busy. Within a warp the
-    // lanes issue the tile's boxes in parallel.
-    const int prod = warp == 0 ? 0 : warp - 1;  // 0 .. kProducers - 1
-    constexpr int kBoxes = kPagesPerTile * C::kChunks;  // boxes per tensor per tile
-    static_assert(2 * kBoxes <= 32, "one box per lane");
+    // Warp 0 streams the K tiles, warps 2 and 3 the V tiles of even and odd
+    // tiles: one warp alone cannot issue the 2 KB page boxes fast enough to
+    // keep HBM busy. Within a warp the lanes issue a tile's boxes in parallel.
+    const bool is_k = warp == 0;
+    const int nprod = is_k ? 1 : C::kVProducers;
+    const int prod = is_k ? 0 : warp - 2;
+    const int nslots = is_k ? C::kKSlots : C::kVSlots;
+    const int bar_full = is_k ? kBarFullK : kBarFullV;
+    const int bar_empty = is_k ? kBarEmptyK : kBarEmptyV;
+    const uint32_t ring = sbase + (is_k ? 0u : (uint32_t)(C::kKSlots * C::kTensorBytes));
+    const void* tmap = is_k ? (const void*)&tm_k : (const void*)&tm_v;
+    constexpr int kBoxes = kPagesPerTile * C::kChunks;  // boxes per tile
+    static_assert(kBoxes <= 32, "one box per lane");
     int it = 0;
     int j = j_first;
     long long ts = ts_first;
@@ -295,10 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int win = -1;       // first page index cached in the lanes
       int my_page = -1;   // page id of page (win + lane)
       for (int lt = pc.lt0; lt < pc.lt1 && ok; ++lt, ++it) {
-        if (it % C::kProducers != prod) continue;
-        const int s = it % kStages;
+        if (it % nprod != prod) continue;
+        const int s = it % nslots;
         const bool got = __all_sync(
-            0xffffffffu, mbar_wait(bar(kBarEmpty + s), ((it / kStages) & 1) ^ 1, abort_flag, kWaitLimitNs));
+            0xffffffffu, mbar_wait(bar(bar_empty + s), ((it / nslots) & 1) ^ 1, abort_flag, kWaitLimitNs));
         if (!got) {  // warp-uniform
           if (lane == 0) fail(p, abort_flag, 1);
           ok = false;
@@ -319,34 +327,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           ids[i] = v ? ids[i] : -1;
           nvalid += v ? 1u : 0u;
         }
-        const uint32_t kst = sbase + s * C::kStageBytes;
-        const uint32_t vst = kst + C::kTensorBytes;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(kBarFullK + s), nvalid * (uint32_t)C::kPageBytes);
-          mbar_arrive_expect_tx(bar(kBarFullV + s), nvalid * (uint32_t)C::kPageBytes);
-        }
+        const uint32_t dst = ring + s * C::kTensorBytes;
+        if (lane == 0) mbar_arrive_expect_tx(bar(bar_full + s), nvalid * (uint32_t)C::kPageBytes);
         __syncwarp();
-        if (lane < 2 * kBoxes) {  // lane -> (tensor, page, 128-byte d chunk)
-          const int tsr = lane / kBoxes, bx = lane % kBoxes;
-          const int i = bx / C::kChunks, ch = bx % C::kChunks;
+        if (lane < kBoxes) {  // lane -> (page, 128-byte d chunk)
+          const int i = lane / C::kChunks, ch = lane % C::kChunks;
           int id = ids[0];
 #pragma unroll
           for (int u = 1; u < kPagesPerTile; ++u)
             if (i == u) id = ids[u];
           if (id >= 0)
-            tma_load_4d((tsr ? vst : kst) + ch * C::kRegion + i * 2048, tsr ? &tm_v : &tm_k,
-                        ch * (128 / C::kEsize), pc.kvh, 0, id, bar((tsr ? kBarFullV : kBarFullK) + s));
+            tma_load_4d(dst + ch * C::kRegion + i * 2048, tmap, ch * (128 / C::kEsize), pc.kvh, 0, id,
+                        bar(bar_full + s));
         }
         __syncwarp();
       }
     }
     if (!ok) {
       // let copies already in flight land before the CTA goes away
-      for (int k = (it > kStages ? it - kStages : 0); k < it; ++k) {
-        if (k % C::kProducers != prod) continue;
-        const int s = k % kStages;
-        mbar_wait(bar(kBarFullK + s), (k / kStages) & 1, abort_flag, 10000000ull);
-        mbar_wait(bar(kBarFullV + s), (k / kStages) & 1, abort_flag, 10000000ull);
+      for (int k = (it > nslots ? it - nslots : 0); k < it; ++k) {
+        if (k % nprod != prod) continue;
+        mbar_wait(bar(bar_full + k % nslots), (k / nslots) & 1, abort_flag, 10000000ull);
       }
     }
   } else if (warp == 1) {
@@ -373,12 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         auto issue_pv = [&](int x) {
           const int pb = x & (kPBufs - 1);
-          const int s = x % kStages;
+          const int s = x % C::kVSlots;
           if (!wait_or_fail(kBarPFull + pb, (x / kPBufs) & 1, 4)) return;
-          if (!wait_or_fail(kBarFullV + s, (x / kStages) & 1, 8)) return;
+          if (!wait_or_fail(kBarFullV + s, (x / C::kVSlots) & 1, 8)) return;
           if (x == first && piece_idx > 0 && !wait_or_fail(kBarOFree, (piece_idx - 1) & 1, 16)) return;
           tc_fence_after();
-          const uint32_t vst = sbase + s * C::kStageBytes + C::kTensorBytes;
+          const uint32_t vst = sbase + (C::kKSlots + s) * C::kTensorBytes;
           const uint32_t pbuf = sbase + kOffP + pb * C::kPBuf;
 #pragma unroll
           for (int kk = 0; kk < C::kPvSteps; ++kk) {
@@ -388,17 +389,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma<FP8>(tmem + kColO, a, bdesc, C::kIdPV, (x == first && kk == 0) ? 0u : 1u);
           }
           mma_commit(bar(kBarPFree + pb));
-          mma_commit(bar(kBarEmpty + s));
+          mma_commit(bar(kBarEmptyV + s));
           if (x == first + ntile - 1) mma_commit(bar(kBarOFull));
         };
         for (int i = 0; i < ntile && ok; ++i) {
           const int cur = first + i;
-          const int s = cur % kStages;
+          const int s = cur % C::kKSlots;
           const int b = cur & (kSBufs - 1);
-          if (!wait_or_fail(kBarFullK + s, (cur / kStages) & 1, 32)) break;
+          if (!wait_or_fail(kBarFullK + s, (cur / C::kKSlots) & 1, 32)) break;
           if (cur >= kSBufs && !wait_or_fail(kBarSFree + b, ((cur - kSBufs) / kSBufs) & 1, 64)) break;
           tc_fence_after();
-          const uint32_t kst = sbase + s * C::kStageBytes;
+          const uint32_t kst = sbase + s * C::kTensorBytes;
 #pragma unroll
           for (int k = 0; k < C::kQkSteps; ++k) {
             const uint32_t qoff = (uint32_t)((k >> 2) * C::kQRegion + (k & 3) * 32);
@@ -408,11 +409,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma<FP8>(tmem + kColS + b * kT, a, bdesc, C::kIdQK, k ? 1u : 0u);
           }
           mma_commit(bar(kBarSFull + b));
+          mma_commit(bar(kBarEmptyK + s));
           if (i == ntile - 1) mma_commit(bar(kBarQFree));
-          if (i >= C::kPvLag) issue_pv(cur - C::kPvLag);
+          if (i >= 1) issue_pv(cur - 1);
         }
-        for (int x = first + (ntile > C::kPvLag ? ntile - C::kPvLag : 0); ok && x < first + ntile; ++x)
-          issue_pv(x);
+        if (ok) issue_pv(first + ntile - 1);
         it = first + ntile;
         ++piece_idx;
       }
@@ -548,7 +549,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cur = it;
         const int b = cur & (kSBufs - 1);
         const int pb = cur & (kPBufs - 1);
-        const int s = cur % kStages;
         if (!wait_or_fail(kBarSFull + b, (cur / kSBufs) & 1, 256)) break;
         tc_fence_after();
         float x[16];  // logits of keys [16 qtr, +16) of this tile, this row
@@ -674,10 +674,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // last tile of the item: V rows past S (partial page, pages never loaded)
         // are zeroed so that 0 * garbage cannot reach O
         if (lt == pc.nt - 1 && (pc.S % kT) != 0) {
-          if (!wait_or_fail(kBarFullV + s, (cur / kStages) & 1, 2048)) break;
+          const int vs = cur % C::kVSlots;
+          if (!wait_or_fail(kBarFullV + vs, (cur / C::kVSlots) & 1, 2048)) break;
           const int z0 = pc.S - lt * kT;
           const int nz = kT - z0;
-          unsigned char* vst = sm + s * C::kStageBytes + C::kTensorBytes;
+          unsigned char* vst = sm + (C::kKSlots + vs) * C::kTensorBytes;
           for (int idx = tid - 128; idx < nz * 8 * C::kChunks; idx += kSoftmaxThreads) {
             const int row = z0 + idx / (8 * C::kChunks);
             const int rem = idx % (8 * C::kChunks);
