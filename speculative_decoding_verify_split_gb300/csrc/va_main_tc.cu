@@ -20,14 +20,13 @@
 // V is the MN-major B operand of O += P V. The k/v descales fold into the
 // logit scale and the output scale.
 //
-// Roles (384 threads):
+// Roles (416 threads):
 //  warps 0,2,3 TMA producers: warp 0 streams K tiles into a K ring (freed
 //              once Q K^T has read them), warps 2 and 3 alternate on V tiles
 //              (V ring, freed after P V). Block-table walk with 32 page ids
 //              per lane load; one 2 KB box per lane.
-//  warp 1      TMEM owner and MMA issuer (one thread). Q K^T of tile i is
-//              issued before P V of tile i - 1, through four S buffers in
-//              TMEM; P has four buffers in shared memory.
+//  warp 1      TMEM owner; one thread issues Q K^T into four S buffers.
+//  warp 12     one thread issues P V into O (P has four smem buffers).
 //  warps 4-11  softmax, two warps per TMEM lane quadrant q = w % 4 (both on
 //              the same SMSP). Warp half kh = (w - 4) / 4 takes keys
 //              [32 kh, 32 kh + 32) of each tile and O columns
@@ -90,7 +89,7 @@ struct Cfg {
 constexpr int kPagesPerTile = kT / kPageSize;
 constexpr int kSBufs = 4;
 constexpr int kPBufs = 4;
-constexpr int kThreads = 384;
+constexpr int kThreads = 416;  // 13 warps
 constexpr int kSoftmaxThreads = 256;
 constexpr int kOffQ = 131072;
 constexpr int kOffP = kOffQ + 32768;
@@ -259,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarQFree), 1);
     mbar_init(bar(kBarOFull), 1);
     mbar_init(bar(kBarOFree), kSwWarps);
-    mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrain), 2);
     for (int i = 0; i < 4; ++i) mbar_init(bar(kBarX + i), 2);
     *abort_flag = 0;
     fence_mbar_init();
@@ -350,9 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar(bar_full + k % nslots), (k / nslots) & 1, abort_flag, 10000000ull);
       }
     }
-  } else if (warp == 1) {
-    // ======================= MMA issuer ===========================================
+  } else if (warp == 1 || warp == 12) {
+    // ======================= MMA issuers ==========================================
+    // Warp 1 issues Q K^T into the S buffers, warp 12 issues P V into O: the
+    // two write different TMEM columns, and splitting them halves the
+    // per-tile issue work of one thread (waits, descriptors, commits).
     if (lane == 0) {
+      const bool is_qk = warp == 1;
       const uint32_t qbase = sbase + kOffQ;
       int it = 0, piece_idx = 0;
       int j = j_first;
@@ -370,54 +373,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && next_piece(p, t0, t1, j, ts, pc)) {
         const int first = it;
         const int ntile = pc.lt1 - pc.lt0;
-        if (!wait_or_fail(kBarQFull, piece_idx & 1, 2)) break;
-        tc_fence_after();
-        auto issue_pv = [&](int x) {
-          const int pb = x & (kPBufs - 1);
-          const int s = x % C::kVSlots;
-          if (!wait_or_fail(kBarPFull + pb, (x / kPBufs) & 1, 4)) return;
-          if (!wait_or_fail(kBarFullV + s, (x / C::kVSlots) & 1, 8)) return;
-          if (x == first && piece_idx > 0 && !wait_or_fail(kBarOFree, (piece_idx - 1) & 1, 16)) return;
+        if (is_qk) {
+          if (!wait_or_fail(kBarQFull, piece_idx & 1, 2)) break;
           tc_fence_after();
-          const uint32_t vst = sbase + (C::kKSlots + s) * C::kTensorBytes;
-          const uint32_t pbuf = sbase + kOffP + pb * C::kPBuf;
+          for (int i = 0; i < ntile && ok; ++i) {
+            const int cur = first + i;
+            const int s = cur % C::kKSlots;
+            const int b = cur & (kSBufs - 1);
+            if (!wait_or_fail(kBarFullK + s, (cur / C::kKSlots) & 1, 32)) break;
+            if (cur >= kSBufs && !wait_or_fail(kBarSFree + b, ((cur - kSBufs) / kSBufs) & 1, 64)) break;
+            tc_fence_after();
+            const uint32_t kst = sbase + s * C::kTensorBytes;
 #pragma unroll
-          for (int kk = 0; kk < C::kPvSteps; ++kk) {
-            const uint64_t a = smem_desc(pbuf + kk * 256, 128, C::kPSbo, kLayoutNone);
-            const uint64_t bdesc = smem_desc(vst + kk * (C::kKeysPerPvStep / 8) * 1024, C::kRegion,
-                                             1024, kLayoutSw128);
-            mma<FP8>(tmem + kColO, a, bdesc, C::kIdPV, (x == first && kk == 0) ? 0u : 1u);
+            for (int k = 0; k < C::kQkSteps; ++k) {
+              const uint32_t qoff = (uint32_t)((k >> 2) * C::kQRegion + (k & 3) * 32);
+              const uint32_t koff = (uint32_t)((k >> 2) * C::kRegion + (k & 3) * 32);
+              const uint64_t a = smem_desc(qbase + qoff, 16, 1024, kLayoutSw128);
+              const uint64_t bdesc = smem_desc(kst + koff, 16, 1024, kLayoutSw128);
+              mma<FP8>(tmem + kColS + b * kT, a, bdesc, C::kIdQK, k ? 1u : 0u);
+            }
+            mma_commit(bar(kBarSFull + b));
+            mma_commit(bar(kBarEmptyK + s));
+            if (i == ntile - 1) mma_commit(bar(kBarQFree));
           }
-          mma_commit(bar(kBarPFree + pb));
-          mma_commit(bar(kBarEmptyV + s));
-          if (x == first + ntile - 1) mma_commit(bar(kBarOFull));
-        };
-        for (int i = 0; i < ntile && ok; ++i) {
-          const int cur = first + i;
-          const int s = cur % C::kKSlots;
-          const int b = cur & (kSBufs - 1);
-          if (!wait_or_fail(kBarFullK + s, (cur / C::kKSlots) & 1, 32)) break;
-          if (cur >= kSBufs && !wait_or_fail(kBarSFree + b, ((cur - kSBufs) / kSBufs) & 1, 64)) break;
-          tc_fence_after();
-          const uint32_t kst = sbase + s * C::kTensorBytes;
+        } else {
+          for (int i = 0; i < ntile && ok; ++i) {
+            const int x = first + i;
+            const int pb = x & (kPBufs - 1);
+            const int s = x % C::kVSlots;
+            if (!wait_or_fail(kBarPFull + pb, (x / kPBufs) & 1, 4)) break;
+            if (!wait_or_fail(kBarFullV + s, (x / C::kVSlots) & 1, 8)) break;
+            if (i == 0 && piece_idx > 0 && !wait_or_fail(kBarOFree, (piece_idx - 1) & 1, 16)) break;
+            tc_fence_after();
+            const uint32_t vst = sbase + (C::kKSlots + s) * C::kTensorBytes;
+            const uint32_t pbuf = sbase + kOffP + pb * C::kPBuf;
 #pragma unroll
-          for (int k = 0; k < C::kQkSteps; ++k) {
-            const uint32_t qoff = (uint32_t)((k >> 2) * C::kQRegion + (k & 3) * 32);
-            const uint32_t koff = (uint32_t)((k >> 2) * C::kRegion + (k & 3) * 32);
-            const uint64_t a = smem_desc(qbase + qoff, 16, 1024, kLayoutSw128);
-            const uint64_t bdesc = smem_desc(kst + koff, 16, 1024, kLayoutSw128);
-            mma<FP8>(tmem + kColS + b * kT, a, bdesc, C::kIdQK, k ? 1u : 0u);
+            for (int kk = 0; kk < C::kPvSteps; ++kk) {
+              const uint64_t a = smem_desc(pbuf + kk * 256, 128, C::kPSbo, kLayoutNone);
+              const uint64_t bdesc = smem_desc(vst + kk * (C::kKeysPerPvStep / 8) * 1024, C::kRegion,
+                                               1024, kLayoutSw128);
+              mma<FP8>(tmem + kColO, a, bdesc, C::kIdPV, (i == 0 && kk == 0) ? 0u : 1u);
+            }
+            mma_commit(bar(kBarPFree + pb));
+            mma_commit(bar(kBarEmptyV + s));
+            if (i == ntile - 1) mma_commit(bar(kBarOFull));
           }
-          mma_commit(bar(kBarSFull + b));
-          mma_commit(bar(kBarEmptyK + s));
-          if (i == ntile - 1) mma_commit(bar(kBarQFree));
-          if (i >= 1) issue_pv(cur - 1);
         }
-        if (ok) issue_pv(first + ntile - 1);
         it = first + ntile;
         ++piece_idx;
       }
-      // make sure every tensor-core operation has finished before TMEM is freed
+      // every tensor-core operation of both issuers has finished before TMEM is freed
       mma_commit(bar(kBarDrain));
       mbar_wait(bar(kBarDrain), 0, abort_flag, 100000000ull);
     }
