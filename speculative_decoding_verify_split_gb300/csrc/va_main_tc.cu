@@ -61,8 +61,8 @@ struct Cfg {
   static constexpr int kTensorBytes = kChunks * kRegion;   // a K or V tile: 16 KB / 32 KB
   // Separate K and V rings: a K slot is free again once Q K^T has read it,
   // a V slot only after P V, so V gets the deeper ring. 128 KB in all.
-  static constexpr int kKSlots = FP8 ? 3 : 2;
-  static constexpr int kVSlots = FP8 ? 5 : 2;
+  static constexpr int kKSlots = FP8 ? 4 : 2;
+  static constexpr int kVSlots = FP8 ? 4 : 2;
   // Producer warps: one streams K, two alternate on V's tiles. A producer's
   // wait for a slot relies on its own previous wait (kVProducers tiles back)
   // to keep that slot's empty barrier within one phase of the wanted
@@ -94,7 +94,8 @@ constexpr int kSoftmaxThreads = 256;
 constexpr int kOffQ = 131072;
 constexpr int kOffP = kOffQ + 32768;
 constexpr int kOffX = kOffP + kPBufs * 8192;  // row exchange: [2 parity][2 kh][64 rows] floats
-constexpr int kOffBar = kOffX + 1024;
+constexpr int kOffXSeq = kOffX + 1024;         // row exchange: [4 quadrants][2 kh] round counters
+constexpr int kOffBar = kOffXSeq + 128;
 constexpr int kSmemBytes = kOffBar + 1024 + 1024;
 
 constexpr uint32_t kColO = 0;    // 256 fp32 columns
@@ -123,8 +124,7 @@ enum : int {
   kBarOFull,
   kBarOFree,
   kBarDrain,
-  kBarX,  // four row-exchange barriers, one per TMEM lane quadrant
-  kNumBars = kBarX + 4
+  kNumBars
 };
 static_assert(8 * kNumBars + 16 + 34 * 8 <= 1024, "barrier area");
 static_assert(kSmemBytes <= 232448, "shared memory");
@@ -259,10 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarOFull), 1);
     mbar_init(bar(kBarOFree), kSwWarps);
     mbar_init(bar(kBarDrain), 2);
-    for (int i = 0; i < 4; ++i) mbar_init(bar(kBarX + i), 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (tid < 8) reinterpret_cast<volatile int*>(sm + kOffXSeq)[tid * 4] = 0;
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float cscale = p.scale_log2 * kd;
     const int G = p.group;
     unsigned char* qs = sm + kOffQ;
-    int it = 0, piece_idx = 0, xpar = 0;
+    int it = 0, piece_idx = 0;
     int j = j_first;
     long long ts = ts_first;
     Piece pc;
@@ -459,17 +459,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // Row-wide combine of a per-thread value: lanes t and t^16 share a row in
     // this warp, the partner warp of the quadrant holds the other half. The
-    // exchange goes through shared memory (double-buffered by round parity)
-    // and a per-quadrant mbarrier, so waits stay bounded and both warps give
-    // up together.
+    // values go through shared memory (double-buffered by round parity) and
+    // each warp publishes a round counter after writing; the partner spins on
+    // it with a time limit, so both warps give up together on a timeout.
+    volatile int* seq = reinterpret_cast<volatile int*>(sm + kOffXSeq);
+    int xround = 0;
     auto exchange = [&](float v, bool is_max) {
       v = is_max ? fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16)) : v + __shfl_xor_sync(0xffffffffu, v, 16);
-      if (sub == 0) xch[(xpar * 2 + kh) * 64 + r] = v;
+      const int par = xround & 1;
+      if (sub == 0) reinterpret_cast<volatile float*>(xch)[(par * 2 + kh) * 64 + r] = v;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarX + q));
-      if (!wait_or_fail(kBarX + q, (uint32_t)xpar, 8192)) return v;
-      const float other = xch[(xpar * 2 + (kh ^ 1)) * 64 + r];
-      xpar ^= 1;
+      ++xround;
+      bool got = true;
+      if (lane == 0) {
+        __threadfence_block();
+        seq[(q * 2 + kh) * 4] = xround;
+        volatile int* other_seq = &seq[(q * 2 + (kh ^ 1)) * 4];
+        if (*other_seq < xround) {
+          const uint64_t t0 = globaltimer_ns();
+          while (*other_seq < xround) {
+            if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+              got = false;
+              break;
+            }
+          }
+        }
+        __threadfence_block();
+      }
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) {
+        if (lane == 0) fail(p, abort_flag, 8192);
+        ok = false;
+        return v;
+      }
+      const float other = reinterpret_cast<volatile float*>(xch)[(par * 2 + (kh ^ 1)) * 64 + r];
       return is_max ? fmaxf(v, other) : v + other;
     };
     while (ok && next_piece(p, t0, t1, j, ts, pc)) {
