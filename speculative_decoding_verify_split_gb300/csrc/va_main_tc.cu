@@ -32,7 +32,8 @@
 //              [32 kh, 32 kh + 32) of each tile and O columns
 //              [128 kh, 128 kh + 128); lane bit 4 splits those again, so a
 //              thread owns 16 keys of one packed row. The two warps of a
-//              quadrant combine row maxima and sums through shared memory.
+//              quadrant combine row maxima and sums through shared memory
+//              around a per-quadrant named barrier.
 // Online softmax in log2 units keeps a per-row reference m_ref and computes
 // P = 2^(s - m_ref + 6) <= 2^8.5; m_ref moves (and O, l are rescaled in
 // TMEM) only when a tile's max exceeds it by more than 2.5, so rescales are
@@ -94,8 +95,7 @@ constexpr int kSoftmaxThreads = 256;
 constexpr int kOffQ = 131072;
 constexpr int kOffP = kOffQ + 32768;
 constexpr int kOffX = kOffP + kPBufs * 8192;  // row exchange: [2 parity][2 kh][64 rows] floats
-constexpr int kOffXSeq = kOffX + 1024;         // row exchange: [4 quadrants][2 kh] round counters
-constexpr int kOffBar = kOffXSeq + 128;
+constexpr int kOffBar = kOffX + 1024;
 constexpr int kSmemBytes = kOffBar + 1024 + 1024;
 
 constexpr uint32_t kColO = 0;    // 256 fp32 columns
@@ -262,7 +262,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (tid < 8) reinterpret_cast<volatile int*>(sm + kOffXSeq)[tid * 4] = 0;
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -427,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar(kBarDrain), 0, abort_flag, 100000000ull);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 12) {
     // ======================= softmax / epilogue ===================================
     const int q = warp & 3;              // TMEM lane quadrant
     const int kh = (warp - 4) >> 2;      // which half of the keys / O columns
@@ -448,6 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     // Every lane waits; the outcome is made warp-uniform so that a timeout can
     // never split the warp in front of a .sync.aligned tcgen05 instruction.
+    // After a failure the warp keeps walking the same pieces and tiles with
+    // all waits and work skipped ("dry"), so both warps of a quadrant still
+    // meet at every exchange barrier.
     auto wait_or_fail = [&](int b, uint32_t par, int code) {
       if (!ok) return false;
       const bool got = __all_sync(0xffffffffu, mbar_wait(bar(b), par, abort_flag, kWaitLimitNs));
@@ -458,46 +460,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       return ok;
     };
     // Row-wide combine of a per-thread value: lanes t and t^16 share a row in
-    // this warp, the partner warp of the quadrant holds the other half. The
-    // values go through shared memory (double-buffered by round parity) and
-    // each warp publishes a round counter after writing; the partner spins on
-    // it with a time limit, so both warps give up together on a timeout.
-    volatile int* seq = reinterpret_cast<volatile int*>(sm + kOffXSeq);
+    // this warp, the partner warp of the quadrant holds the other half. Values
+    // go through shared memory (double-buffered by round parity) around the
+    // quadrant's named barrier (ids 1..4, 64 threads). Both warps call this the
+    // same number of times, failed or not, so the barrier never strands one.
     int xround = 0;
     auto exchange = [&](float v, bool is_max) {
       v = is_max ? fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16)) : v + __shfl_xor_sync(0xffffffffu, v, 16);
       const int par = xround & 1;
-      if (sub == 0) reinterpret_cast<volatile float*>(xch)[(par * 2 + kh) * 64 + r] = v;
-      __syncwarp();
       ++xround;
-      bool got = true;
-      if (lane == 0) {
-        __threadfence_block();
-        seq[(q * 2 + kh) * 4] = xround;
-        volatile int* other_seq = &seq[(q * 2 + (kh ^ 1)) * 4];
-        if (*other_seq < xround) {
-          const uint64_t t0 = globaltimer_ns();
-          while (*other_seq < xround) {
-            if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
-              got = false;
-              break;
-            }
-          }
-        }
-        __threadfence_block();
-      }
-      got = __shfl_sync(0xffffffffu, got, 0);
-      if (!got) {
-        if (lane == 0) fail(p, abort_flag, 8192);
-        ok = false;
-        return v;
-      }
-      const float other = reinterpret_cast<volatile float*>(xch)[(par * 2 + (kh ^ 1)) * 64 + r];
+      if (sub == 0) xch[(par * 2 + kh) * 64 + r] = v;
+      named_bar(1 + q, 64);
+      const float other = xch[(par * 2 + (kh ^ 1)) * 64 + r];
       return is_max ? fmaxf(v, other) : v + other;
     };
-    while (ok && next_piece(p, t0, t1, j, ts, pc)) {
+    while (next_piece(p, t0, t1, j, ts, pc)) {
       // -- Q tile into the swizzled K-major A operand; this thread: d [64 qtr, +64)
-      if (piece_idx > 0 && !wait_or_fail(kBarQFree, (piece_idx - 1) & 1, 128)) break;
+      if (piece_idx > 0) wait_or_fail(kBarQFree, (piece_idx - 1) & 1, 128);
       const bool row_ok = r < pc.R;
       const int tq = row_ok ? r / G : 0;
       const int gq = row_ok ? r - tq * G : 0;
@@ -507,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint16_t* src = p.q + (int64_t)(pc.q0 + tq) * p.q_s0 + (int64_t)(pc.kvh * G + gq) * p.q_s1 + 64 * qtr;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          raw[i] = row_ok ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0, 0, 0, 0);
+          raw[i] = (ok && row_ok) ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0, 0, 0, 0);
         if constexpr (FP8) {
           float amax = 0.f;
 #pragma unroll
@@ -520,7 +499,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           amax = exchange(amax, true);
-          if (!ok) break;
           int e = 0;
           if (amax > 0.f && amax < INFINITY) {
             const int E = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
@@ -532,41 +510,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           rs = row_ok ? cscale * down : 0.f;
           // d [64 qtr, +64) = region kh, 16-byte pieces 4 sub .. 4 sub + 3;
           // hi to A row 32q + rl, lo to A row 32q + 16 + rl
+          if (ok) {
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t hw[4], lw[4];
+            for (int cc = 0; cc < 4; ++cc) {
+              uint32_t hw[4], lw[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint4 a = raw[2 * cc + (k >> 1)];
-              const uint32_t wa = (k & 1) ? a.z : a.x;
-              const uint32_t wb = (k & 1) ? a.w : a.y;
-              const float x0 = __uint_as_float(wa << 16) * up, x1 = __uint_as_float(wa & 0xFFFF0000u) * up;
-              const float x2 = __uint_as_float(wb << 16) * up, x3 = __uint_as_float(wb & 0xFFFF0000u) * up;
-              const uint32_t h01 = pack_fp8x2(x0, x1), h23 = pack_fp8x2(x2, x3);
-              const float2 f01 = unpack_fp8x2(h01), f23 = unpack_fp8x2(h23);
-              const uint32_t l01 = pack_fp8x2(x0 - f01.x, x1 - f01.y), l23 = pack_fp8x2(x2 - f23.x, x3 - f23.y);
-              hw[k] = h01 | (h23 << 16);
-              lw[k] = l01 | (l23 << 16);
+              for (int k = 0; k < 4; ++k) {
+                const uint4 a = raw[2 * cc + (k >> 1)];
+                const uint32_t wa = (k & 1) ? a.z : a.x;
+                const uint32_t wb = (k & 1) ? a.w : a.y;
+                const float x0 = __uint_as_float(wa << 16) * up, x1 = __uint_as_float(wa & 0xFFFF0000u) * up;
+                const float x2 = __uint_as_float(wb << 16) * up, x3 = __uint_as_float(wb & 0xFFFF0000u) * up;
+                const uint32_t h01 = pack_fp8x2(x0, x1), h23 = pack_fp8x2(x2, x3);
+                const float2 f01 = unpack_fp8x2(h01), f23 = unpack_fp8x2(h23);
+                const uint32_t l01 = pack_fp8x2(x0 - f01.x, x1 - f01.y), l23 = pack_fp8x2(x2 - f23.x, x3 - f23.y);
+                hw[k] = h01 | (h23 << 16);
+                lw[k] = l01 | (l23 << 16);
+              }
+              const int piece16 = 4 * sub + cc;
+              const int swz = (piece16 ^ (rl & 7)) << 4;
+              const int ahi = 32 * q + rl, alo = ahi + 16;
+              *reinterpret_cast<uint4*>(qs + kh * C::kQRegion + ahi * 128 + swz) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              *reinterpret_cast<uint4*>(qs + kh * C::kQRegion + alo * 128 + swz) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
-            const int piece16 = 4 * sub + cc;
-            const int swz = (piece16 ^ (rl & 7)) << 4;
-            const int ahi = 32 * q + rl, alo = ahi + 16;
-            *reinterpret_cast<uint4*>(qs + kh * C::kQRegion + ahi * 128 + swz) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(qs + kh * C::kQRegion + alo * 128 + swz) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
         } else {
           rs = row_ok ? cscale : 0.f;
           // d [64 qtr, +64) = one whole 128-byte region (qtr), eight 16-byte pieces
+          if (ok) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int off = qtr * C::kQRegion + r * 128 + ((i ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(qs + off) = raw[i];
+            for (int i = 0; i < 8; ++i) {
+              const int off = qtr * C::kQRegion + r * 128 + ((i ^ (r & 7)) << 4);
+              *reinterpret_cast<uint4*>(qs + off) = raw[i];
+            }
           }
         }
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarQFull));
+      if (ok) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarQFull));
+      }
 
       // -- key tiles
       float m_ref = -INFINITY;
@@ -577,48 +561,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cur = it;
         const int b = cur & (kSBufs - 1);
         const int pb = cur & (kPBufs - 1);
-        if (!wait_or_fail(kBarSFull + b, (cur / kSBufs) & 1, 256)) break;
-        tc_fence_after();
         float x[16];  // logits of keys [16 qtr, +16) of this tile, this row
-        if constexpr (FP8) {
-          // lane t reads its TMEM lane: hi (t < 16) or lo (t >= 16) partial of
-          // row 16q + rl for keys [32 kh, +32); add the partner's half
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + kColS + b * kT + 32 * kh, v);
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarSFree + b));
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float mine = __uint_as_float(sub ? v[16 + i] : v[i]);
-            const float give = __uint_as_float(sub ? v[i] : v[16 + i]);
-            x[i] = (mine + __shfl_xor_sync(0xffffffffu, give, 16)) * rs;
+        for (int i = 0; i < 16; ++i) x[i] = -INFINITY;
+        if (wait_or_fail(kBarSFull + b, (cur / kSBufs) & 1, 256)) {
+          tc_fence_after();
+          if constexpr (FP8) {
+            // lane t reads its TMEM lane: hi (t < 16) or lo (t >= 16) partial of
+            // row 16q + rl for keys [32 kh, +32); add the partner's half
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + lane_base + kColS + b * kT + 32 * kh, v);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarSFree + b));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float mine = __uint_as_float(sub ? v[16 + i] : v[i]);
+              const float give = __uint_as_float(sub ? v[i] : v[16 + i]);
+              x[i] = (mine + __shfl_xor_sync(0xffffffffu, give, 16)) * rs;
+            }
+          } else {
+            uint32_t v[16];
+            tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kColS + b * kT + 32 * kh, v);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarSFree + b));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(v[i]) * rs;
           }
-        } else {
-          uint32_t v[16];
-          tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kColS + b * kT + 32 * kh, v);
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarSFree + b));
+          const int key0 = lt * kT + 16 * qtr;
+          if (lt * kT + kT - 1 > pc.S - pc.L) {  // tail tile: causal mask
 #pragma unroll
-          for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(v[i]) * rs;
-        }
-        const int key0 = lt * kT + 16 * qtr;
-        if (lt * kT + kT - 1 > pc.S - pc.L) {  // tail tile: causal mask
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (key0 + i > vis_end) x[i] = -INFINITY;
+            for (int i = 0; i < 16; ++i)
+              if (key0 + i > vis_end) x[i] = -INFINITY;
+          }
         }
         float tmax = -INFINITY;
 #pragma unroll
         for (int i = 0; i < 16; i += 2) tmax = fmaxf(tmax, fmaxf(x[i], x[i + 1]));
         tmax = exchange(tmax, true);
-        if (!ok) break;
+        if (!ok) continue;
 
         // P buffer pb was last read by PV(cur - kPBufs)
-        if (cur >= kPBufs && !wait_or_fail(kBarPFree + pb, ((cur - kPBufs) / kPBufs) & 1, 512)) break;
+        if (cur >= kPBufs && !wait_or_fail(kBarPFree + pb, ((cur - kPBufs) / kPBufs) & 1, 512)) continue;
 
         const bool need = tmax > m_ref + kOvershoot;
         const float m_new = need ? tmax + kHeadroom : m_ref;
@@ -628,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // O holds earlier tiles of this piece: wait for PV(cur - 1), then
           // scale this thread's part of the row in TMEM
           const int xp = cur - 1;
-          if (!wait_or_fail(kBarPFree + (xp & (kPBufs - 1)), (xp / kPBufs) & 1, 1024)) break;
+          if (!wait_or_fail(kBarPFree + (xp & (kPBufs - 1)), (xp / kPBufs) & 1, 1024)) continue;
           tc_fence_after();
 #pragma unroll 1
           for (int k = 0; k < (FP8 ? 4 : 2); ++k) {
@@ -703,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // are zeroed so that 0 * garbage cannot reach O
         if (lt == pc.nt - 1 && (pc.S % kT) != 0) {
           const int vs = cur % C::kVSlots;
-          if (!wait_or_fail(kBarFullV + vs, (cur / C::kVSlots) & 1, 2048)) break;
+          if (!wait_or_fail(kBarFullV + vs, (cur / C::kVSlots) & 1, 2048)) continue;
           const int z0 = pc.S - lt * kT;
           const int nz = kT - z0;
           unsigned char* vst = sm + (C::kKSlots + vs) * C::kTensorBytes;
@@ -719,13 +706,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarPFull + pb));
       }
-      if (!ok) break;
 
       // -- epilogue: this thread writes O[r][128 kh + 64 sub, +64)
-      if (!wait_or_fail(kBarOFull, piece_idx & 1, 4096)) break;
+      wait_or_fail(kBarOFull, piece_idx & 1, 4096);
       tc_fence_after();
       const float lrow = exchange(l, false);
-      if (!ok) break;
+      ++piece_idx;
+      if (!ok) continue;
       const float inv = lrow > 0.f ? vd / lrow : 0.f;
       const int64_t piece = (int64_t)pc.j + c;
       auto emit = [&](const uint32_t (&o)[32], int col) {
@@ -780,7 +767,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarOFree));
-      ++piece_idx;
     }
   }
 
