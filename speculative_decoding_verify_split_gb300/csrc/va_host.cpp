@@ -132,7 +132,7 @@ va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t m
   if (kv_dtype != VA_FP8_E4M3 && kv_dtype != VA_BF16) return VA_ERR_UNSUPPORTED;
   const int64_t G = hq / hkv;
   if (G * max_q > kMaxRows) return VA_ERR_UNSUPPORTED;
-  const int tile = kTcTileKeys;
+  const int tile = kv_dtype == VA_FP8_E4M3 ? kTcTileKeysFp8 : kTcTileKeysBf16;
   const int64_t J = B * hkv;
   const int64_t tiles_bound = J * ((max_k + tile - 1) / tile);
   if (tiles_bound > INT32_MAX / 2) return VA_ERR_UNSUPPORTED;

@@ -66,7 +66,8 @@ inline WorkspaceLayout workspace_layout(int64_t num_work, int64_t num_splits, in
 
 // Main kernel (tensor cores) and its key-tile sizes.
 enum Kernel : int32_t { kKernelTc = 1 };
-constexpr int kTcTileKeys = 64;  // keys per tile, FP8 and BF16 KV
+constexpr int kTcTileKeysFp8 = 128;  // keys per tile, FP8 KV
+constexpr int kTcTileKeysBf16 = 64;  // keys per tile, BF16 KV
 
 cudaError_t launch_merge(const Params& p, cudaStream_t stream);
 cudaError_t prepare_main_tc();  // once per device: opt in to its shared memory

@@ -52,18 +52,21 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kT = kTcTileKeys;  // 64 keys per tile, both KV types
-
 template <bool FP8>
 struct Cfg {
+  static constexpr int kT = FP8 ? kTcTileKeysFp8 : kTcTileKeysBf16;  // keys per tile: 128 / 64
+  static constexpr int kPagesPerTile = kT / kPageSize;
+  static constexpr int kKpt = kT / 4;                      // keys per softmax thread per tile
+  static constexpr int kSBufs = FP8 ? 2 : 4;               // S tiles in TMEM (256 columns)
+  static constexpr int kPBufs = FP8 ? 2 : 4;               // P buffers in smem (32 KB)
   static constexpr int kEsize = FP8 ? 1 : 2;               // bytes per KV element
   static constexpr int kChunks = kHeadDim * kEsize / 128;  // 128-byte d chunks (2 or 4)
-  static constexpr int kRegion = kT * 128;                 // one d chunk of a K or V tile: 8 KB
+  static constexpr int kRegion = kT * 128;                 // one d chunk of a K or V tile
   static constexpr int kTensorBytes = kChunks * kRegion;   // a K or V tile: 16 KB / 32 KB
-  // Separate K and V rings: a K slot is free again once Q K^T has read it,
-  // a V slot only after P V, so V gets the deeper ring. 128 KB in all.
-  static constexpr int kKSlots = FP8 ? 4 : 2;
-  static constexpr int kVSlots = FP8 ? 4 : 2;
+  // Separate K and V rings (a K slot is free again once Q K^T has read it, a
+  // V slot only after P V), two 32 KB tiles each: 128 KB in all.
+  static constexpr int kKSlots = 2;
+  static constexpr int kVSlots = 2;
   // Producer warps: one streams K, two alternate on V's tiles. A producer's
   // wait for a slot relies on its own previous wait (kVProducers tiles back)
   // to keep that slot's empty barrier within one phase of the wanted
@@ -73,9 +76,9 @@ struct Cfg {
   static constexpr int kPageBytes = kChunks * 2048;        // one page of one tensor
   static constexpr int kM = FP8 ? 128 : 64;                // MMA rows
   static constexpr int kQRegion = kM * 128;                // one 128-byte d chunk of Q
-  static constexpr int kPRowBytes = kT * kEsize;           // 64 (fp8) / 128 (bf16)
+  static constexpr int kPRowBytes = kT * kEsize;           // 128 bytes
   static constexpr int kPSbo = 8 * kPRowBytes;             // 8-row group stride, no swizzle
-  static constexpr int kPBuf = kM * kPRowBytes;            // 8 KB
+  static constexpr int kPBuf = kM * kPRowBytes;            // 16 KB (fp8) / 8 KB (bf16)
   static constexpr int kQkSteps = 4 * kChunks;             // K-steps of 32 bytes over d
   static constexpr int kPvSteps = kT * kEsize / 32;        // K-steps of 32 bytes over keys
   static constexpr int kKeysPerPvStep = 32 / kEsize;
@@ -84,17 +87,18 @@ struct Cfg {
   static constexpr uint32_t kIdPV = instr_desc(kFmt, kFmt, true, kHeadDim, kM);
   static_assert((kKSlots + kVSlots) * kTensorBytes == 131072, "ring size");
   static_assert(kChunks * kQRegion == 32768, "Q size");
-  static_assert(kPBuf == 8192, "P buffer size");
+  static_assert(kPBufs * kPBuf == 32768, "P buffers");
+  static_assert(kSBufs * kT == 256, "S buffers");
+  static_assert(kPagesPerTile * kChunks <= 32, "one TMA box per lane");
 };
 
-constexpr int kPagesPerTile = kT / kPageSize;
-constexpr int kSBufs = 4;
-constexpr int kPBufs = 4;
+constexpr int kMaxSBufs = 4;
+constexpr int kMaxPBufs = 4;
 constexpr int kThreads = 416;  // 13 warps
 constexpr int kSoftmaxThreads = 256;
 constexpr int kOffQ = 131072;
 constexpr int kOffP = kOffQ + 32768;
-constexpr int kOffX = kOffP + kPBufs * 8192;  // row exchange: [2 parity][2 kh][64 rows] floats
+constexpr int kOffX = kOffP + 32768;  // row exchange: [2 parity][2 kh][64 rows] floats
 constexpr int kOffBar = kOffX + 1024;
 constexpr int kSmemBytes = kOffBar + 1024 + 1024;
 
@@ -116,10 +120,10 @@ enum : int {
   kBarFullV = kBarEmptyK + kMaxSlots,
   kBarEmptyV = kBarFullV + kMaxSlots,
   kBarSFull = kBarEmptyV + kMaxSlots,
-  kBarSFree = kBarSFull + kSBufs,
-  kBarPFull = kBarSFree + kSBufs,
-  kBarPFree = kBarPFull + kPBufs,
-  kBarQFull = kBarPFree + kPBufs,
+  kBarSFree = kBarSFull + kMaxSBufs,
+  kBarPFull = kBarSFree + kMaxSBufs,
+  kBarPFree = kBarPFull + kMaxPBufs,
+  kBarQFull = kBarPFree + kMaxPBufs,
   kBarQFree,
   kBarOFull,
   kBarOFree,
@@ -128,7 +132,6 @@ enum : int {
 };
 static_assert(8 * kNumBars + 16 + 34 * 8 <= 1024, "barrier area");
 static_assert(kSmemBytes <= 232448, "shared memory");
-static_assert(kColS + kSBufs * kT <= kTmemCols, "TMEM columns");
 
 struct Piece {
   int j, b, kvh, S, L, q0, R, nt, lt0, lt1;
@@ -204,6 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     va_main_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v) {
   using C = Cfg<FP8>;
+  constexpr int kT = C::kT;
+  constexpr int kSBufs = C::kSBufs;
+  constexpr int kPBufs = C::kPBufs;
+  constexpr int kPagesPerTile = C::kPagesPerTile;
+  constexpr int kKpt = C::kKpt;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -561,24 +569,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cur = it;
         const int b = cur & (kSBufs - 1);
         const int pb = cur & (kPBufs - 1);
-        float x[16];  // logits of keys [16 qtr, +16) of this tile, this row
+        float x[kKpt];  // logits of keys [kKpt qtr, +kKpt) of this tile, this row
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = -INFINITY;
+        for (int i = 0; i < kKpt; ++i) x[i] = -INFINITY;
         if (wait_or_fail(kBarSFull + b, (cur / kSBufs) & 1, 256)) {
           tc_fence_after();
           if constexpr (FP8) {
             // lane t reads its TMEM lane: hi (t < 16) or lo (t >= 16) partial of
-            // row 16q + rl for keys [32 kh, +32); add the partner's half
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + lane_base + kColS + b * kT + 32 * kh, v);
+            // row 16q + rl for keys [64 kh, +64); sub 0 keeps the first 32
+            // keys, sub 1 the second, each adding the partner lane's part
+            uint32_t va[32], vb[32];
+            tmem_ld_32x32b_x32(tmem + lane_base + kColS + b * kT + 64 * kh, va);
+            tmem_ld_32x32b_x32(tmem + lane_base + kColS + b * kT + 64 * kh + 32, vb);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarSFree + b));
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float mine = __uint_as_float(sub ? v[16 + i] : v[i]);
-              const float give = __uint_as_float(sub ? v[i] : v[16 + i]);
+            for (int i = 0; i < 32; ++i) {
+              const float mine = __uint_as_float(sub ? vb[i] : va[i]);
+              const float give = __uint_as_float(sub ? va[i] : vb[i]);
               x[i] = (mine + __shfl_xor_sync(0xffffffffu, give, 16)) * rs;
             }
           } else {
@@ -591,16 +601,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(v[i]) * rs;
           }
-          const int key0 = lt * kT + 16 * qtr;
+          const int key0 = lt * kT + kKpt * qtr;
           if (lt * kT + kT - 1 > pc.S - pc.L) {  // tail tile: causal mask
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
+            for (int i = 0; i < kKpt; ++i)
               if (key0 + i > vis_end) x[i] = -INFINITY;
           }
         }
         float tmax = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) tmax = fmaxf(tmax, fmaxf(x[i], x[i + 1]));
+        for (int i = 0; i < kKpt; i += 2) tmax = fmaxf(tmax, fmaxf(x[i], x[i + 1]));
         tmax = exchange(tmax, true);
         if (!ok) continue;
 
@@ -646,9 +656,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float ls0 = 0.f, ls1 = 0.f;
         unsigned char* pbuf = sm + kOffP + pb * C::kPBuf;
         if constexpr (FP8) {
-          uint32_t ph[4], pl[4];
+          uint32_t ph[8], pl[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
+          for (int i = 0; i < 16; ++i) {
             const float a = live ? ex2(x[2 * i] - mref_s) : 0.f;
             const float bb = live ? ex2(x[2 * i + 1] - mref_s) : 0.f;
             ls0 += a;
@@ -663,13 +673,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               pl[i >> 1] = l2;
             }
           }
-          // keys [16 qtr, +16) = 16-byte core-matrix column qtr of A rows
-          // 32q + rl (hi) and 32q + 16 + rl (lo)
+          // keys [32 qtr, +32) = 16-byte core-matrix columns 2 qtr, 2 qtr + 1 of
+          // A rows 32q + rl (hi) and 32q + 16 + rl (lo)
           const int ahi = 32 * q + rl, alo = ahi + 16;
-          *reinterpret_cast<uint4*>(pbuf + (ahi >> 3) * C::kPSbo + qtr * 128 + (ahi & 7) * 16) =
-              make_uint4(ph[0], ph[1], ph[2], ph[3]);
-          *reinterpret_cast<uint4*>(pbuf + (alo >> 3) * C::kPSbo + qtr * 128 + (alo & 7) * 16) =
-              make_uint4(pl[0], pl[1], pl[2], pl[3]);
+          unsigned char* bh = pbuf + (ahi >> 3) * C::kPSbo + (2 * qtr) * 128 + (ahi & 7) * 16;
+          unsigned char* bl = pbuf + (alo >> 3) * C::kPSbo + (2 * qtr) * 128 + (alo & 7) * 16;
+          *reinterpret_cast<uint4*>(bh) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+          *reinterpret_cast<uint4*>(bh + 128) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
+          *reinterpret_cast<uint4*>(bl) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+          *reinterpret_cast<uint4*>(bl + 128) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
         } else {
           uint32_t pw[8];
 #pragma unroll
