@@ -11,23 +11,27 @@
 // held by one CTA were written by the main kernel; items with no key tiles
 // get zero rows here.
 //
-// One warp per packed row: the lanes read the segments' (m, l) in parallel,
-// reduce, then each lane accumulates 8 of the 256 output columns. Launched as
-// a programmatic dependent of the main kernel; it waits for the main kernel's
-// memory before touching the workspace.
+// 64 threads per packed row, one float4 of the 256 output columns each, so a
+// row's segments are read as coalesced 1 KB lines. Segments are taken eight
+// at a time with all their loads in flight together, and folded into a
+// running (max, denominator, accumulator) triple: the latency of a merge is
+// one L2 round trip per eight segments. Launched as a programmatic dependent
+// of the main kernel; it waits for the main kernel's memory before touching
+// the workspace.
 #include "va_split.cuh"
 
 namespace va {
 namespace {
 
-constexpr int kRowsPerCta = 8;
+constexpr int kRowsPerCta = 4;
+constexpr int kThreadsPerRow = kHeadDim / 4;  // 64
+constexpr int kSegChunk = 8;
 
-__global__ void __launch_bounds__(32 * kRowsPerCta) va_merge_kernel(const Params p) {
+__global__ void __launch_bounds__(kRowsPerCta * kThreadsPerRow, 4) va_merge_kernel(const Params p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int j = blockIdx.x;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int r = blockIdx.y * kRowsPerCta + warp;
+  const int r = blockIdx.y * kRowsPerCta + (int)(threadIdx.x / kThreadsPerRow);
+  const int col4 = (int)(threadIdx.x % kThreadsPerRow);
   const int b = j / p.hkv;
   const int kvh = j - b * p.hkv;
   const int L = seq_q_len(p, b);
@@ -35,11 +39,11 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) va_merge_kernel(const Params
   if (r >= G * L) return;
   const int t = r / G, g = r - t * G;
   const int q0 = p.cu_q[b];
-  uint16_t* dst = p.out + (int64_t)(q0 + t) * p.o_s0 + (int64_t)(kvh * G + g) * p.o_s1 + 8 * lane;
+  uint16_t* dst = p.out + (int64_t)(q0 + t) * p.o_s0 + (int64_t)(kvh * G + g) * p.o_s1 + 4 * col4;
 
   const int nt = work_tiles(p, j);
   if (nt == 0) {
-    *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
     return;
   }
   const long long N = p.ws_meta[p.num_work];
@@ -49,69 +53,56 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) va_merge_kernel(const Params
   if (c0 == c1) return;  // one CTA held the whole item and wrote it
   const int ns = c1 - c0 + 1;
 
-  // (m, l) of every segment, lanes in parallel
-  auto seg_m = [&](int k, float& m, float& l) {
-    const int c = c0 + k;
-    m = -INFINITY;
-    l = 0.f;
-    if (split_begin(N, c, p.num_splits) == split_begin(N, c + 1, p.num_splits)) return;  // empty CTA
-    const int64_t piece = (int64_t)j + c;
-    const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + (piece * p.max_rows + r) * 2);
-    m = ml.x;
-    l = ml.y;
-  };
-  float M = -INFINITY;
-  for (int k = lane; k < ns; k += 32) {
-    float m, l;
-    seg_m(k, m, l);
-    M = fmaxf(M, m);
-  }
+  float M = -INFINITY, den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = 0; base < ns; base += kSegChunk) {
+    float m[kSegChunk], l[kSegChunk];
+    float4 a[kSegChunk];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int k = 0; k < kSegChunk; ++k) {
+      m[k] = -INFINITY;
+      l[k] = 0.f;
+      a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int c = c0 + base + k;
+      if (base + k < ns && split_begin(N, c, p.num_splits) != split_begin(N, c + 1, p.num_splits)) {
+        const int64_t row = ((int64_t)j + c) * p.max_rows + r;
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + row * 2));
+        m[k] = ml.x;
+        l[k] = ml.y;
+        a[k] = __ldcg(reinterpret_cast<const float4*>(p.ws_acc + row * kHeadDim) + col4);
+      }
+    }
+    float mc = M;
+#pragma unroll
+    for (int k = 0; k < kSegChunk; ++k) mc = fmaxf(mc, m[k]);
+    if (mc == -INFINITY) continue;  // nothing visible yet
+    const float sc = (M == -INFINITY) ? 0.f : exp2f(M - mc);
+    den *= sc;
+    acc.x *= sc;
+    acc.y *= sc;
+    acc.z *= sc;
+    acc.w *= sc;
+#pragma unroll
+    for (int k = 0; k < kSegChunk; ++k) {
+      if (m[k] == -INFINITY) continue;  // weight 0; its partial is never read
+      const float w = exp2f(m[k] - mc);
+      den = fmaf(w, l[k], den);
+      acc.x = fmaf(w, a[k].x, acc.x);
+      acc.y = fmaf(w, a[k].y, acc.y);
+      acc.z = fmaf(w, a[k].z, acc.z);
+      acc.w = fmaf(w, a[k].w, acc.w);
+    }
+    M = mc;
+  }
   if (M == -INFINITY) {
-    *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
     return;
   }
-
-  float den = 0.f;
-  float acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int base = 0; base < ns; base += 32) {
-    float m, l, w = 0.f;
-    if (base + lane < ns) {
-      seg_m(base + lane, m, l);
-      w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-      den = fmaf(w, l, den);
-    }
-    const int cnt = ns - base < 32 ? ns - base : 32;
-#pragma unroll 4
-    for (int k = 0; k < cnt; ++k) {
-      const float wk = __shfl_sync(0xffffffffu, w, k);
-      if (wk == 0.f) continue;
-      const int64_t piece = (int64_t)j + c0 + base + k;
-      const float4* src = reinterpret_cast<const float4*>(p.ws_acc + (piece * p.max_rows + r) * kHeadDim) + 2 * lane;
-      const float4 a = src[0], bq = src[1];
-      acc[0] = fmaf(wk, a.x, acc[0]);
-      acc[1] = fmaf(wk, a.y, acc[1]);
-      acc[2] = fmaf(wk, a.z, acc[2]);
-      acc[3] = fmaf(wk, a.w, acc[3]);
-      acc[4] = fmaf(wk, bq.x, acc[4]);
-      acc[5] = fmaf(wk, bq.y, acc[5]);
-      acc[6] = fmaf(wk, bq.z, acc[6]);
-      acc[7] = fmaf(wk, bq.w, acc[7]);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
   const float vd = p.v_descale ? *p.v_descale : 1.0f;
   const float inv = vd / den;
-  uint32_t w4[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    w4[i] = (uint32_t)float_to_bf16_bits(acc[2 * i] * inv) |
-            ((uint32_t)float_to_bf16_bits(acc[2 * i + 1] * inv) << 16);
-  *reinterpret_cast<uint4*>(dst) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  const uint32_t w0 = (uint32_t)float_to_bf16_bits(acc.x * inv) | ((uint32_t)float_to_bf16_bits(acc.y * inv) << 16);
+  const uint32_t w1 = (uint32_t)float_to_bf16_bits(acc.z * inv) | ((uint32_t)float_to_bf16_bits(acc.w * inv) << 16);
+  *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
 }
 
 }  // namespace
@@ -120,7 +111,7 @@ cudaError_t launch_merge(const Params& p, cudaStream_t stream) {
   if (p.num_work == 0 || p.max_rows == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.num_work, (unsigned)((p.max_rows + kRowsPerCta - 1) / kRowsPerCta));
-  cfg.blockDim = dim3(32 * kRowsPerCta);
+  cfg.blockDim = dim3(kRowsPerCta * kThreadsPerRow);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
