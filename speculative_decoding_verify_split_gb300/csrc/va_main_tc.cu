@@ -52,6 +52,8 @@ namespace {
 
 using namespace ptx;
 
+constexpr int kRingBytes = 4 * 32768;  // K and V rings
+
 template <bool FP8>
 struct Cfg {
   static constexpr int kT = FP8 ? kTcTileKeysFp8 : kTcTileKeysBf16;  // keys per tile: 128 / 64
@@ -64,7 +66,8 @@ struct Cfg {
   static constexpr int kRegion = kT * 128;                 // one d chunk of a K or V tile
   static constexpr int kTensorBytes = kChunks * kRegion;   // a K or V tile: 16 KB / 32 KB
   // Separate K and V rings (a K slot is free again once Q K^T has read it, a
-  // V slot only after P V), two 32 KB tiles each: 128 KB in all.
+  // V slot only after P V), two 32 KB tiles each: 128 KB in all. A third K
+  // slot (160 KB) measured no faster.
   static constexpr int kKSlots = 2;
   static constexpr int kVSlots = 2;
   // Producer warps: one streams K, two alternate on V's tiles. A producer's
@@ -85,7 +88,7 @@ struct Cfg {
   static constexpr uint32_t kFmt = FP8 ? 0u : 1u;          // e4m3 / bf16
   static constexpr uint32_t kIdQK = instr_desc(kFmt, kFmt, false, kT, kM);
   static constexpr uint32_t kIdPV = instr_desc(kFmt, kFmt, true, kHeadDim, kM);
-  static_assert((kKSlots + kVSlots) * kTensorBytes == 131072, "ring size");
+  static_assert((kKSlots + kVSlots) * kTensorBytes == kRingBytes, "ring size");
   static_assert(kChunks * kQRegion == 32768, "Q size");
   static_assert(kPBufs * kPBuf == 32768, "P buffers");
   static_assert(kSBufs * kT == 256, "S buffers");
@@ -96,11 +99,11 @@ constexpr int kMaxSBufs = 4;
 constexpr int kMaxPBufs = 4;
 constexpr int kThreads = 416;  // 13 warps
 constexpr int kSoftmaxThreads = 256;
-constexpr int kOffQ = 131072;
+constexpr int kOffQ = kRingBytes;
 constexpr int kOffP = kOffQ + 32768;
 constexpr int kOffX = kOffP + 32768;  // row exchange: [2 parity][2 kh][64 rows] floats
 constexpr int kOffBar = kOffX + 1024;
-constexpr int kSmemBytes = kOffBar + 1024 + 1024;
+constexpr int kSmemBytes = kOffBar + 1024;
 
 constexpr uint32_t kColO = 0;    // 256 fp32 columns
 constexpr uint32_t kColS = 256;  // four 64-column S tiles
@@ -702,6 +705,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // are zeroed so that 0 * garbage cannot reach O
         if (lt == pc.nt - 1 && (pc.S % kT) != 0) {
           const int vs = cur % C::kVSlots;
+          // FullV(vs) alternates between the tiles that share slot vs, so its
+          // parity names tile cur only once the slot's previous tile
+          // (cur - kVSlots) has been consumed by P V. With more P buffers than
+          // V slots the softmax can run that far ahead of P V: wait for it.
+          if constexpr (kPBufs > C::kVSlots) {
+            const int xv = cur - C::kVSlots;
+            if (xv >= 0 && !wait_or_fail(kBarPFree + (xv & (kPBufs - 1)), (xv / kPBufs) & 1, 2049)) continue;
+          }
           if (!wait_or_fail(kBarFullV + vs, (cur / C::kVSlots) & 1, 2048)) continue;
           const int z0 = pc.S - lt * kT;
           const int nz = kT - z0;
