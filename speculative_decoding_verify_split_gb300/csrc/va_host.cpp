@@ -135,7 +135,7 @@ va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t m
   const int tile = kv_dtype == VA_FP8_E4M3 ? kTcTileKeysFp8 : kTcTileKeysBf16;
   const int64_t J = B * hkv;
   const int64_t tiles_bound = J * ((max_k + tile - 1) / tile);
-  if (tiles_bound > INT32_MAX / 2) return VA_ERR_UNSUPPORTED;
+  if (tiles_bound + J * kPieceCostTiles > INT32_MAX / 2) return VA_ERR_UNSUPPORTED;
   // Heuristic: every SM gets one CTA (the main kernel keeps one CTA per SM),
   // but no CTA gets fewer than kMinTiles tiles of the upper-bound workload,
   // so small batches do not pay a merge for nothing.
@@ -272,6 +272,7 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
   p.num_splits = plan.num_splits;
   p.max_rows = plan.max_rows;
   p.num_work = plan.num_work;
+  p.piece_cost = kPieceCostTiles;
   const WorkspaceLayout lay = workspace_layout(plan.num_work, plan.num_splits, plan.max_rows);
   char* base = static_cast<char*>(ws);
   p.ws_meta = reinterpret_cast<int32_t*>(base + lay.meta_off);

@@ -36,10 +36,13 @@ struct Params {
   float scale_log2;  // softmax_scale * log2(e)
 
   // Split-KV decomposition: one stream of key tiles over all work items
-  // j = b * hkv + kvh, cut into num_splits equal ranges (one per CTA).
-  int32_t tile_keys, num_splits, max_rows, num_work;
+  // j = b * hkv + kvh, cut into num_splits equal ranges (one per CTA). Each
+  // item also costs piece_cost units ahead of its first tile (its Q staging,
+  // epilogue and pipeline refill), so a CTA that starts an item gets fewer
+  // tiles.
+  int32_t tile_keys, num_splits, max_rows, num_work, piece_cost;
   int32_t* ws_status;  // sticky error bits (a bounded wait timed out); never cleared by kernels
-  int32_t* ws_meta;  // [num_work + 1]: first tile of each work item, then the total
+  int32_t* ws_meta;  // [num_work + 1]: first tile of each work item (split units), then the total
   float* ws_ml;      // [pieces][max_rows][2]: running max (log2 units), row sum
   float* ws_acc;     // [pieces][max_rows][256]: unnormalised output rows
 };
@@ -68,6 +71,10 @@ inline WorkspaceLayout workspace_layout(int64_t num_work, int64_t num_splits, in
 enum Kernel : int32_t { kKernelTc = 1 };
 constexpr int kTcTileKeysFp8 = 128;  // keys per tile, FP8 KV
 constexpr int kTcTileKeysBf16 = 64;  // keys per tile, BF16 KV
+// Split cost of starting a work item, in tiles: a CTA's boundary between two
+// items (epilogue of one, Q staging and pipeline refill of the next) measured
+// about 10 us on the long-context FP8 workload, ~6 tiles of 1.6 us.
+constexpr int kPieceCostTiles = 6;
 
 cudaError_t launch_merge(const Params& p, cudaStream_t stream);
 cudaError_t prepare_main_tc();  // once per device: opt in to its shared memory

@@ -52,8 +52,6 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kRingBytes = 4 * 32768;  // K and V rings
-
 template <bool FP8>
 struct Cfg {
   static constexpr int kT = FP8 ? kTcTileKeysFp8 : kTcTileKeysBf16;  // keys per tile: 128 / 64
@@ -65,11 +63,16 @@ struct Cfg {
   static constexpr int kChunks = kHeadDim * kEsize / 128;  // 128-byte d chunks (2 or 4)
   static constexpr int kRegion = kT * 128;                 // one d chunk of a K or V tile
   static constexpr int kTensorBytes = kChunks * kRegion;   // a K or V tile: 16 KB / 32 KB
-  // Separate K and V rings (a K slot is free again once Q K^T has read it, a
-  // V slot only after P V), two 32 KB tiles each: 128 KB in all. A third K
-  // slot (160 KB) measured no faster.
-  static constexpr int kKSlots = 2;
-  static constexpr int kVSlots = 2;
+  // Separate K and V rings of 32 KB tiles (a K slot is free again once Q K^T
+  // has read it, a V slot only after P V). A slot turns over in about DRAM
+  // latency + hold + producer reaction (~3500 + 1500 + 500 cycles at full HBM
+  // load), so the tile rate is slots / that: FP8 keeps P in TMEM and spends
+  // the freed shared memory on three slots per ring (192 KB); BF16 keeps its
+  // smem P buffers and has room for 3 K + 2 V (160 KB).
+  static constexpr bool kPInTmem = FP8;
+  static constexpr int kKSlots = 3;
+  static constexpr int kVSlots = FP8 ? 3 : 2;
+  static constexpr int kRingBytes = (kKSlots + kVSlots) * 32768;
   // Producer warps: one streams K, two alternate on V's tiles. A producer's
   // wait for a slot relies on its own previous wait (kVProducers tiles back)
   // to keep that slot's empty barrier within one phase of the wanted
@@ -88,7 +91,15 @@ struct Cfg {
   static constexpr uint32_t kFmt = FP8 ? 0u : 1u;          // e4m3 / bf16
   static constexpr uint32_t kIdQK = instr_desc(kFmt, kFmt, false, kT, kM);
   static constexpr uint32_t kIdPV = instr_desc(kFmt, kFmt, true, kHeadDim, kM);
-  static_assert((kKSlots + kVSlots) * kTensorBytes == kRingBytes, "ring size");
+  static_assert(kTensorBytes == 32768, "ring slot size");
+  // shared memory: rings | Q | P buffers (smem P only) | row exchange | barriers
+  static constexpr int kOffQ = kRingBytes;
+  static constexpr int kOffP = kOffQ + 32768;
+  static constexpr int kOffX = kOffP + (kPInTmem ? 0 : 32768);  // [2 parity][2 kh][64 rows] floats
+  static constexpr int kOffBar = kOffX + 1024;
+  static constexpr int kSmemBytes = kOffBar + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(!kPInTmem || kSBufs == kPBufs, "a TMEM P shares its S buffer's index and barriers");
   static_assert(kChunks * kQRegion == 32768, "Q size");
   static_assert(kPBufs * kPBuf == 32768, "P buffers");
   static_assert(kSBufs * kT == 256, "S buffers");
@@ -99,11 +110,6 @@ constexpr int kMaxSBufs = 4;
 constexpr int kMaxPBufs = 4;
 constexpr int kThreads = 416;  // 13 warps
 constexpr int kSoftmaxThreads = 256;
-constexpr int kOffQ = kRingBytes;
-constexpr int kOffP = kOffQ + 32768;
-constexpr int kOffX = kOffP + 32768;  // row exchange: [2 parity][2 kh][64 rows] floats
-constexpr int kOffBar = kOffX + 1024;
-constexpr int kSmemBytes = kOffBar + 1024;
 
 constexpr uint32_t kColO = 0;    // 256 fp32 columns
 constexpr uint32_t kColS = 256;  // four 64-column S tiles
@@ -134,14 +140,14 @@ enum : int {
   kNumBars
 };
 static_assert(8 * kNumBars + 16 + 34 * 8 <= 1024, "barrier area");
-static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct Piece {
   int j, b, kvh, S, L, q0, R, nt, lt0, lt1;
   bool direct;
 };
 
-// Next (sequence, KV head) item of this CTA's tile range [t0, t1).
+// Next (sequence, KV head) item with tiles in this CTA's split range [t0, t1);
+// ts is the split unit of item j's first tile.
 __device__ __forceinline__ bool next_piece(const Params& p, long long t0, long long t1, int& j,
                                            long long& ts, Piece& pc) {
   while (j < p.num_work && ts < t1) {
@@ -161,7 +167,7 @@ __device__ __forceinline__ bool next_piece(const Params& p, long long t0, long l
     pc.lt0 = (int)((t0 > ts ? t0 : ts) - ts);
     pc.lt1 = (int)((t1 < ts + nt ? t1 : ts + nt) - ts);
     pc.direct = (pc.lt0 == 0 && pc.lt1 == nt);
-    ts += nt;
+    ts += work_cost(p, nt);  // the next item's first tile follows its start-up units
     ++j;
     return true;
   }
@@ -218,13 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + 8 * kNumBars);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffBar + 8 * kNumBars + 4);
-  long long* scratch = reinterpret_cast<long long*>(sm + kOffBar + 8 * kNumBars + 16);  // 32 slots
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffBar + 8 * kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffBar + 8 * kNumBars + 4);
+  long long* scratch = reinterpret_cast<long long*>(sm + C::kOffBar + 8 * kNumBars + 16);  // 32 slots
   long long* s_ts = scratch + 32;
   int* s_j = reinterpret_cast<int*>(scratch + 33);
-  float* xch = reinterpret_cast<float*>(sm + kOffX);
+  float* xch = reinterpret_cast<float*>(sm + C::kOffX);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // per-tile issue work of one thread (waits, descriptors, commits).
     if (lane == 0) {
       const bool is_qk = warp == 1;
-      const uint32_t qbase = sbase + kOffQ;
+      const uint32_t qbase = sbase + C::kOffQ;
       int it = 0, piece_idx = 0;
       int j = j_first;
       long long ts = ts_first;
@@ -391,7 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = cur % C::kKSlots;
             const int b = cur & (kSBufs - 1);
             if (!wait_or_fail(kBarFullK + s, (cur / C::kKSlots) & 1, 32)) break;
-            if (cur >= kSBufs && !wait_or_fail(kBarSFree + b, ((cur - kSBufs) / kSBufs) & 1, 64)) break;
+            // S buffer b is free once the softmax has read S(cur - kSBufs) or,
+            // with P in TMEM over it, once P V(cur - kSBufs) has read that P
+            if (cur >= kSBufs &&
+                !wait_or_fail(C::kPInTmem ? kBarPFree + b : kBarSFree + b, ((cur - kSBufs) / kSBufs) & 1, 64))
+              break;
             tc_fence_after();
             const uint32_t kst = sbase + s * C::kTensorBytes;
 #pragma unroll
@@ -416,13 +426,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (i == 0 && piece_idx > 0 && !wait_or_fail(kBarOFree, (piece_idx - 1) & 1, 16)) break;
             tc_fence_after();
             const uint32_t vst = sbase + (C::kKSlots + s) * C::kTensorBytes;
-            const uint32_t pbuf = sbase + kOffP + pb * C::kPBuf;
+            const uint32_t pbuf = sbase + C::kOffP + pb * C::kPBuf;
 #pragma unroll
             for (int kk = 0; kk < C::kPvSteps; ++kk) {
-              const uint64_t a = smem_desc(pbuf + kk * 256, 128, C::kPSbo, kLayoutNone);
               const uint64_t bdesc = smem_desc(vst + kk * (C::kKeysPerPvStep / 8) * 1024, C::kRegion,
                                                1024, kLayoutSw128);
-              mma<FP8>(tmem + kColO, a, bdesc, C::kIdPV, (i == 0 && kk == 0) ? 0u : 1u);
+              const uint32_t acc = (i == 0 && kk == 0) ? 0u : 1u;
+              if constexpr (C::kPInTmem) {
+                // P(x) sits in the first kT/4 columns of S buffer pb, 8 per K-step
+                mma_f8f6f4_ta(tmem + kColO, tmem + kColS + pb * kT + 8 * kk, bdesc, C::kIdPV, acc);
+              } else {
+                const uint64_t a = smem_desc(pbuf + kk * 256, 128, C::kPSbo, kLayoutNone);
+                mma<FP8>(tmem + kColO, a, bdesc, C::kIdPV, acc);
+              }
             }
             mma_commit(bar(kBarPFree + pb));
             mma_commit(bar(kBarEmptyV + s));
@@ -450,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float vd = p.v_descale ? *p.v_descale : 1.0f;
     const float cscale = p.scale_log2 * kd;
     const int G = p.group;
-    unsigned char* qs = sm + kOffQ;
+    unsigned char* qs = sm + C::kOffQ;
     int it = 0, piece_idx = 0;
     int j = j_first;
     long long ts = ts_first;
@@ -581,13 +597,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // lane t reads its TMEM lane: hi (t < 16) or lo (t >= 16) partial of
             // row 16q + rl for keys [64 kh, +64); sub 0 keeps the first 32
             // keys, sub 1 the second, each adding the partner lane's part
+            // (S buffer b is then overwritten by P(cur); P V's commit frees it)
             uint32_t va[32], vb[32];
             tmem_ld_32x32b_x32(tmem + lane_base + kColS + b * kT + 64 * kh, va);
             tmem_ld_32x32b_x32(tmem + lane_base + kColS + b * kT + 64 * kh + 32, vb);
             tmem_wait_ld();
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarSFree + b));
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float mine = __uint_as_float(sub ? vb[i] : va[i]);
@@ -617,8 +632,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmax = exchange(tmax, true);
         if (!ok) continue;
 
-        // P buffer pb was last read by PV(cur - kPBufs)
-        if (cur >= kPBufs && !wait_or_fail(kBarPFree + pb, ((cur - kPBufs) / kPBufs) & 1, 512)) continue;
+        // P buffer pb was last read by PV(cur - kPBufs). (A TMEM P goes over
+        // S(cur), whose Q K^T already waited for that.)
+        if (!C::kPInTmem && cur >= kPBufs &&
+            !wait_or_fail(kBarPFree + pb, ((cur - kPBufs) / kPBufs) & 1, 512))
+          continue;
 
         const bool need = tmax > m_ref + kOvershoot;
         const float m_new = need ? tmax + kHeadroom : m_ref;
@@ -657,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mref_s = m_ref - kPShift;
         const bool live = m_ref != -INFINITY;
         float ls0 = 0.f, ls1 = 0.f;
-        unsigned char* pbuf = sm + kOffP + pb * C::kPBuf;
+        unsigned char* pbuf = sm + C::kOffP + pb * C::kPBuf;
         if constexpr (FP8) {
           uint32_t ph[8], pl[8];
 #pragma unroll
@@ -676,15 +694,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               pl[i >> 1] = l2;
             }
           }
-          // keys [32 qtr, +32) = 16-byte core-matrix columns 2 qtr, 2 qtr + 1 of
-          // A rows 32q + rl (hi) and 32q + 16 + rl (lo)
-          const int ahi = 32 * q + rl, alo = ahi + 16;
-          unsigned char* bh = pbuf + (ahi >> 3) * C::kPSbo + (2 * qtr) * 128 + (ahi & 7) * 16;
-          unsigned char* bl = pbuf + (alo >> 3) * C::kPSbo + (2 * qtr) * 128 + (alo & 7) * 16;
-          *reinterpret_cast<uint4*>(bh) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-          *reinterpret_cast<uint4*>(bh + 128) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
-          *reinterpret_cast<uint4*>(bl) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-          *reinterpret_cast<uint4*>(bl + 128) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
+          // A operand of P V in TMEM, over S(cur): lane 32q + rl (hi row) and
+          // lane 32q + 16 + rl (lo row) take the e4m3 bytes of keys
+          // [64 kh, +64) at columns [16 kh, +16). This thread holds keys
+          // [32 qtr, +32) of both; it trades the part its lane does not take
+          // with the partner lane (t ^ 16).
+          uint32_t pw[16];
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, sub ? ph[w] : pl[w], 16);
+            pw[w] = sub ? recv : ph[w];
+            pw[8 + w] = sub ? pl[w] : recv;
+          }
+          // the quadrant's other warp read its S columns before the exchange
+          tc_fence_after();
+          tmem_st_32x32b_x16(tmem + lane_base + kColS + b * kT + 16 * kh, pw);
+          tmem_wait_st();
         } else {
           uint32_t pw[8];
 #pragma unroll
@@ -707,8 +732,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int vs = cur % C::kVSlots;
           // FullV(vs) alternates between the tiles that share slot vs, so its
           // parity names tile cur only once the slot's previous tile
-          // (cur - kVSlots) has been consumed by P V. With more P buffers than
-          // V slots the softmax can run that far ahead of P V: wait for it.
+          // (cur - kVSlots) has been consumed by P V. The softmax at tile cur
+          // only knows P V(cur - kPBufs) done (its P buffer, or for a TMEM P
+          // the S buffer Q K^T waited for); if that is not enough, wait.
           if constexpr (kPBufs > C::kVSlots) {
             const int xv = cur - C::kVSlots;
             if (xv >= 0 && !wait_or_fail(kBarPFree + (xv & (kPBufs - 1)), (xv / kPBufs) & 1, 2049)) continue;
@@ -725,6 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(vst + ch * C::kRegion + row * 128 + piece16 * 16) = make_uint4(0, 0, 0, 0);
           }
         }
+        if constexpr (C::kPInTmem) tc_fence_before();  // the P store, before the arrive
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarPFull + pb));
@@ -802,19 +829,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t prepare_main_tc() {
-  cudaError_t e = cudaFuncSetAttribute(va_main_tc_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(va_main_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<true>::kSmemBytes);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(va_main_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemBytes);
+                              Cfg<false>::kSmemBytes);
 }
 
 cudaError_t launch_main_tc(const Params& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            cudaStream_t stream) {
   if (p.kv_fp8)
-    va_main_tc_kernel<true><<<p.num_splits, kThreads, kSmemBytes, stream>>>(p, tm_k, tm_v);
+    va_main_tc_kernel<true><<<p.num_splits, kThreads, Cfg<true>::kSmemBytes, stream>>>(p, tm_k, tm_v);
   else
-    va_main_tc_kernel<false><<<p.num_splits, kThreads, kSmemBytes, stream>>>(p, tm_k, tm_v);
+    va_main_tc_kernel<false><<<p.num_splits, kThreads, Cfg<false>::kSmemBytes, stream>>>(p, tm_k, tm_v);
   return cudaGetLastError();
 }
 

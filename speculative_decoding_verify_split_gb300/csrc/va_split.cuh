@@ -38,12 +38,18 @@ __device__ __forceinline__ int work_tiles(const Params& p, int j) {
   return (seq_kv_len(p, b) + p.tile_keys - 1) / p.tile_keys;
 }
 
-// First global tile of CTA c when N tiles are cut into G equal ranges.
+// Split cost of work item j with nt tiles: the tiles plus the item's start-up
+// cost, which comes first in split units.
+__device__ __forceinline__ long long work_cost(const Params& p, int nt) {
+  return nt > 0 ? (long long)nt + p.piece_cost : 0;
+}
+
+// First split unit of CTA c when N units are cut into G equal ranges.
 __device__ __forceinline__ long long split_begin(long long N, int c, int G) {
   return (N * (long long)c) / G;
 }
 
-// The CTA whose range contains tile x (0 <= x < N): the largest c with
+// The CTA whose range contains split unit x (0 <= x < N): the largest c with
 // split_begin(c) <= x, i.e. c*N < (x+1)*G.
 __device__ __forceinline__ int split_of(long long x, long long N, int G) {
   return (int)(((x + 1) * (long long)G - 1) / N);
@@ -81,39 +87,41 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
   return base + x - v;
 }
 
-// Scans the tile counts of all work items. When write_meta, stores the first
-// tile of every item in ws_meta and the total at ws_meta[num_work]. Returns
-// the total tile count N.
+// Scans the split costs of all work items. When write_meta, stores the split
+// unit of the first tile of every item in ws_meta and the total at
+// ws_meta[num_work]. Returns the total N.
 template <int NT>
 __device__ long long scan_work(const Params& p, long long* scratch, bool write_meta) {
   long long running = 0;
   for (int base = 0; base < p.num_work; base += NT) {
     const int j = base + (int)threadIdx.x;
-    const long long v = j < p.num_work ? work_tiles(p, j) : 0;
+    const int nt = j < p.num_work ? work_tiles(p, j) : 0;
+    const long long v = work_cost(p, nt);
     long long tot;
     const long long ex = block_exclusive_scan<NT>(v, scratch, &tot);
-    if (write_meta && j < p.num_work) p.ws_meta[j] = (int32_t)(running + ex);
+    if (write_meta && j < p.num_work) p.ws_meta[j] = (int32_t)(running + ex + (v - nt));
     running += tot;
   }
   if (write_meta && threadIdx.x == 0) p.ws_meta[p.num_work] = (int32_t)running;
   return running;
 }
 
-// Finds the work item containing global tile x (0 <= x < N) and its first
-// tile. Every thread gets the answer.
+// Finds the work item whose split range contains unit x (0 <= x < N) and the
+// unit of its first tile. Every thread gets the answer.
 template <int NT>
 __device__ void find_work(const Params& p, long long x, long long* scratch, int* s_j,
                           long long* s_ts, int* out_j, long long* out_ts) {
   long long running = 0;
   for (int base = 0; base < p.num_work; base += NT) {
     const int j = base + (int)threadIdx.x;
-    const long long v = j < p.num_work ? work_tiles(p, j) : 0;
+    const int nt = j < p.num_work ? work_tiles(p, j) : 0;
+    const long long v = work_cost(p, nt);
     long long tot;
     const long long ex = block_exclusive_scan<NT>(v, scratch, &tot);
     const long long s = running + ex;
     if (j < p.num_work && v > 0 && s <= x && x < s + v) {
       *s_j = j;
-      *s_ts = s;
+      *s_ts = s + (v - nt);
     }
     running += tot;
   }
