@@ -136,10 +136,12 @@ va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t m
   const int64_t J = B * hkv;
   const int64_t tiles_bound = J * ((max_k + tile - 1) / tile);
   if (tiles_bound + J * kPieceCostTiles > INT32_MAX / 2) return VA_ERR_UNSUPPORTED;
-  // Heuristic: every SM gets one CTA (the main kernel keeps one CTA per SM),
-  // but no CTA gets fewer than kMinTiles tiles of the upper-bound workload,
-  // so small batches do not pay a merge for nothing.
-  constexpr int64_t kMinTiles = 4;
+  // Heuristic: one CTA per SM (the main kernel keeps one CTA per SM), fewer
+  // only when the upper-bound workload has fewer tiles than SMs. A CTA's
+  // time is its start-up and drain plus its tiles, so spreading a small batch
+  // thinly is the lowest-latency choice; the merge that it needs costs a few
+  // microseconds.
+  constexpr int64_t kMinTiles = 1;
   int64_t splits;
   if (force > 0) {
     splits = force;

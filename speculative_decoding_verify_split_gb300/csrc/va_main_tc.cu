@@ -244,13 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---- work range (all threads) -------------------------------------------------
-  const long long N = scan_work<kThreads>(p, scratch, c == 0);
-  const long long t0 = split_begin(N, c, p.num_splits);
-  const long long t1 = split_begin(N, c + 1, p.num_splits);
+  long long t0, t1, ts_first = 0;
+  int j_first = 0;
+  locate_work<kThreads>(p, c, scratch, s_j, s_ts, &t0, &t1, &j_first, &ts_first);
   if (t0 >= t1) return;
-  int j_first;
-  long long ts_first;
-  find_work<kThreads>(p, t0, scratch, s_j, s_ts, &j_first, &ts_first);
 
   // ---- setup --------------------------------------------------------------------
   constexpr uint32_t kSwWarps = kSoftmaxThreads / 32;

@@ -52,6 +52,9 @@ __global__ void __launch_bounds__(kRowsPerCta * kThreadsPerRow, 4) va_merge_kern
   const int c1 = split_of(ts + nt - 1, N, p.num_splits);
   if (c0 == c1) return;  // one CTA held the whole item and wrote it
   const int ns = c1 - c0 + 1;
+  // A CTA range can only be empty when there are fewer split units than CTAs;
+  // otherwise skip the two 64-bit divisions per segment.
+  const bool may_be_empty = N < (long long)p.num_splits;
 
   float M = -INFINITY, den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -64,7 +67,8 @@ __global__ void __launch_bounds__(kRowsPerCta * kThreadsPerRow, 4) va_merge_kern
       l[k] = 0.f;
       a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       const int c = c0 + base + k;
-      if (base + k < ns && split_begin(N, c, p.num_splits) != split_begin(N, c + 1, p.num_splits)) {
+      if (base + k < ns &&
+          (!may_be_empty || split_begin(N, c, p.num_splits) != split_begin(N, c + 1, p.num_splits))) {
         const int64_t row = ((int64_t)j + c) * p.max_rows + r;
         const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + row * 2));
         m[k] = ml.x;

@@ -106,6 +106,14 @@ __device__ long long scan_work(const Params& p, long long* scratch, bool write_m
   return running;
 }
 
+// The block-table entry of item j's tile lt, prefetched into L2: the TMA
+// producers' first load, whose latency then overlaps the CTA's setup.
+__device__ __forceinline__ void prefetch_first_pages(const Params& p, int j, long long lt) {
+  const int* bt = p.block_table + (int64_t)(j / p.hkv) * p.bt_s0 +
+                  (int64_t)(lt * p.tile_keys / kPageSize) * p.bt_s1;
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(bt));
+}
+
 // Finds the work item whose split range contains unit x (0 <= x < N) and the
 // unit of its first tile. Every thread gets the answer.
 template <int NT>
@@ -122,12 +130,48 @@ __device__ void find_work(const Params& p, long long x, long long* scratch, int*
     if (j < p.num_work && v > 0 && s <= x && x < s + v) {
       *s_j = j;
       *s_ts = s + (v - nt);
+      prefetch_first_pages(p, j, x > s + (v - nt) ? x - (s + (v - nt)) : 0);
     }
     running += tot;
   }
   __syncthreads();
   *out_j = *s_j;
   *out_ts = *s_ts;
+}
+
+// This CTA's split range [t0, t1) and, if it is not empty, its first work
+// item and the unit of that item's first tile. With at most one item per
+// thread the block scan's total is known in the same pass, so one scan does
+// both jobs; larger batches scan twice. Returns N.
+template <int NT>
+__device__ long long locate_work(const Params& p, int c, long long* scratch, int* s_j,
+                                 long long* s_ts, long long* t0, long long* t1, int* out_j,
+                                 long long* out_ts) {
+  if (p.num_work > NT) {
+    const long long N = scan_work<NT>(p, scratch, c == 0);
+    *t0 = split_begin(N, c, p.num_splits);
+    *t1 = split_begin(N, c + 1, p.num_splits);
+    if (*t0 < *t1) find_work<NT>(p, *t0, scratch, s_j, s_ts, out_j, out_ts);
+    return N;
+  }
+  const int j = (int)threadIdx.x;
+  const int nt = j < p.num_work ? work_tiles(p, j) : 0;
+  const long long v = work_cost(p, nt);
+  long long N;
+  const long long s = block_exclusive_scan<NT>(v, scratch, &N);
+  *t0 = split_begin(N, c, p.num_splits);
+  *t1 = split_begin(N, c + 1, p.num_splits);
+  if (c == 0 && j < p.num_work) p.ws_meta[j] = (int32_t)(s + (v - nt));
+  if (c == 0 && j == 0) p.ws_meta[p.num_work] = (int32_t)N;
+  if (*t0 < *t1 && j < p.num_work && v > 0 && s <= *t0 && *t0 < s + v) {
+    *s_j = j;
+    *s_ts = s + (v - nt);
+    prefetch_first_pages(p, j, *t0 > s + (v - nt) ? *t0 - (s + (v - nt)) : 0);
+  }
+  __syncthreads();
+  *out_j = *s_j;
+  *out_ts = *s_ts;
+  return N;
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {

@@ -97,12 +97,15 @@ def test_plan_fills_the_sms():
     assert p["workspace_bytes"] >= (16 + 152) * 64 * 256 * 4
 
 
-def test_plan_small_batches_use_few_splits():
+def test_plan_spreads_small_batches_one_tile_per_cta():
+    # one CTA per key tile of the upper-bound workload, up to one per SM
     p = va.plan(1, 1, 16, 2, 16, "fp8_e4m3", 152)
     assert p["num_splits"] == 1
-    p = va.plan(2, 1, 16, 4, 1024, "fp8_e4m3", 152)
-    assert 1 <= p["num_splits"] <= 152
-    assert p["num_splits"] * 4 * p["tile_keys"] >= 2 * 1024 - 4 * p["tile_keys"]
+    for dt in ("fp8_e4m3", "bf16"):
+        p = va.plan(2, 1, 16, 4, 1024, dt, 152)
+        assert p["num_splits"] == 2 * (1024 // p["tile_keys"])
+        p = va.plan(8, 2, 32, 4, 4096, dt, 152)
+        assert p["num_splits"] == 152
 
 
 def test_plan_force_and_clamp():
