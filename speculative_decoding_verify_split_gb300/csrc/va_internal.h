@@ -72,9 +72,10 @@ enum Kernel : int32_t { kKernelTc = 1 };
 constexpr int kTcTileKeysFp8 = 128;  // keys per tile, FP8 KV
 constexpr int kTcTileKeysBf16 = 64;  // keys per tile, BF16 KV
 // Split cost of starting a work item, in tiles: a CTA's boundary between two
-// items (epilogue of one, Q staging and pipeline refill of the next) measured
-// about 10 us on the long-context FP8 workload, ~6 tiles of 1.6 us.
-constexpr int kPieceCostTiles = 6;
+// items (epilogue of one, Q staging and pipeline refill of the next). Swept
+// over 3/4/6/8 on the mid- and long-context FP8 workloads: 4 is best on the
+// first and within noise on the second.
+constexpr int kPieceCostTiles = 4;
 
 cudaError_t launch_merge(const Params& p, cudaStream_t stream);
 cudaError_t prepare_main_tc();  // once per device: opt in to its shared memory

@@ -498,16 +498,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float other = xch[(par * 2 + (kh ^ 1)) * 64 + r];
       return is_max ? fmaxf(v, other) : v + other;
     };
-    while (next_piece(p, t0, t1, j, ts, pc)) {
-      // -- Q tile into the swizzled K-major A operand; this thread: d [64 qtr, +64)
-      if (piece_idx > 0) wait_or_fail(kBarQFree, (piece_idx - 1) & 1, 128);
-      const bool row_ok = r < pc.R;
+    // Q tile of piece pq (the qidx-th piece of this CTA) into the swizzled
+    // K-major A operand, after Q K^T of the previous piece has read the old
+    // one; this thread: d [64 qtr, +64). Returns the row's logit scale.
+    auto stage_q = [&](const Piece& pq, int qidx) -> float {
+      if (qidx > 0) wait_or_fail(kBarQFree, (qidx - 1) & 1, 128);
+      const bool row_ok = r < pq.R;
       const int tq = row_ok ? r / G : 0;
       const int gq = row_ok ? r - tq * G : 0;
       float rs = 0.f;
       {
         uint4 raw[8];  // 64 bf16
-        const uint16_t* src = p.q + (int64_t)(pc.q0 + tq) * p.q_s0 + (int64_t)(pc.kvh * G + gq) * p.q_s1 + 64 * qtr;
+        const uint16_t* src = p.q + (int64_t)(pq.q0 + tq) * p.q_s0 + (int64_t)(pq.kvh * G + gq) * p.q_s1 + 64 * qtr;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           raw[i] = (ok && row_ok) ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0, 0, 0, 0);
@@ -575,6 +577,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarQFull));
       }
+      return rs;
+    };
+    // The first lines of the next piece's Q rows, pulled into L2 early.
+    auto prefetch_q = [&](const Piece& pq) {
+      if (r < pq.R) {
+        const int tq = r / G, gq = r - tq * G;
+        const uint16_t* src = p.q + (int64_t)(pq.q0 + tq) * p.q_s0 + (int64_t)(pq.kvh * G + gq) * p.q_s1 + 64 * qtr;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+      }
+    };
+    float rs_next = 0.f;
+    bool staged_next = false;
+    while (next_piece(p, t0, t1, j, ts, pc)) {
+      // The next piece's Q is staged at the start of this piece's last tile,
+      // so its first Q K^T overlaps that tile and this piece's epilogue.
+      Piece pn;
+      int jn = j;
+      long long tsn = ts;
+      const bool has_next = next_piece(p, t0, t1, jn, tsn, pn);
+      const float rs = staged_next ? rs_next : stage_q(pc, piece_idx);
+      staged_next = false;
+      if (has_next) prefetch_q(pn);
+      const bool row_ok = r < pc.R;
+      const int tq = row_ok ? r / G : 0;
+      const int gq = row_ok ? r - tq * G : 0;
 
       // -- key tiles
       float m_ref = -INFINITY;
@@ -585,6 +612,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cur = it;
         const int b = cur & (kSBufs - 1);
         const int pb = cur & (kPBufs - 1);
+        if (lt == pc.lt1 - 1 && has_next) {
+          rs_next = stage_q(pn, piece_idx + 1);
+          staged_next = true;
+        }
         float x[kKpt];  // logits of keys [kKpt qtr, +kKpt) of this tile, this row
 #pragma unroll
         for (int i = 0; i < kKpt; ++i) x[i] = -INFINITY;
