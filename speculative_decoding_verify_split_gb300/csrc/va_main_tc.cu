@@ -317,18 +317,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int lt = pc.lt0; lt < pc.lt1 && ok; ++lt, ++it) {
         if (it % nprod != prod) continue;
         const int s = it % nslots;
-        const bool got = __all_sync(
-            0xffffffffu, mbar_wait(bar(bar_empty + s), ((it / nslots) & 1) ^ 1, abort_flag, kWaitLimitNs));
-        if (!got) {  // warp-uniform
-          if (lane == 0) fail(p, abort_flag, 1);
-          ok = false;
-          break;
-        }
+        // page ids first (a block-table load every 32 pages), so that their
+        // latency overlaps the wait for the ring slot
         const int pg0 = lt * kPagesPerTile;
         if (win < 0 || pg0 + kPagesPerTile > win + 32) {
           win = pg0;
           const int pg = win + lane;
           my_page = pg < npages ? bt_row[(int64_t)pg * p.bt_s1] : -1;
+          if (lane == 0 && win + 32 < npages)  // the next window's entries
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(bt_row + (int64_t)(win + 32) * p.bt_s1));
         }
         uint32_t nvalid = 0;
         int ids[kPagesPerTile];
@@ -338,6 +335,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool v = (pg0 + i) < npages && (unsigned)ids[i] < (unsigned)p.num_blocks;
           ids[i] = v ? ids[i] : -1;
           nvalid += v ? 1u : 0u;
+        }
+        const bool got = __all_sync(
+            0xffffffffu, mbar_wait(bar(bar_empty + s), ((it / nslots) & 1) ^ 1, abort_flag, kWaitLimitNs));
+        if (!got) {  // warp-uniform
+          if (lane == 0) fail(p, abort_flag, 1);
+          ok = false;
+          break;
         }
         const uint32_t dst = ring + s * C::kTensorBytes;
         if (lane == 0) mbar_arrive_expect_tx(bar(bar_full + s), nvalid * (uint32_t)C::kPageBytes);
