@@ -224,6 +224,48 @@ va_status verify_attn_noalloc(const va_tensor* q, const va_tensor* k_cache,
                               const va_tensor* k_descale, const va_tensor* v_descale,
                               va_tensor* out, void* stream);
 
+/*
+ * verify_attn_block_table_from_indptr - the block table and KV lengths of a
+ * batch given in flat token-slot form. This is the draft-extend pass of the
+ * sglang PR 30105 digest ("Fix 2: draft_extend_v2 re-routed to
+ * unified_attention"): it builds a 2D page table from its flat metadata, takes
+ * each sequence's KV length as the difference of consecutive kv_indptr
+ * entries, and then runs the same split-KV attention as target verify. After
+ * this call, verify_attn on (block_table, seqused_k) with
+ * max_seqlen_k = width * 16 is that attention.
+ *
+ * Arguments (all device memory, all int32):
+ *  kv_indptr    [B+1], contiguous. Sequence b's tokens are kv_indices
+ *               [kv_indptr[b], kv_indptr[b+1]).
+ *  kv_indices   [nnz], contiguous. The KV-cache token slot of every token,
+ *               slot = page * 16 + position in the page.
+ *  block_table  [B, width], any non-negative strides; written. Entry p of
+ *               row b is the page holding sequence b's tokens [16p, 16p + 16),
+ *               i.e. the page of the first of those slots. Entries past the
+ *               sequence's last page are set to pad_page.
+ *  seqused_k    [B], any stride; written with kv_indptr[b+1] - kv_indptr[b].
+ *  status       optional (NULL: not reported), one int32. The kernel ORs in:
+ *                 1  a page's slots are not one page in order: the first slot
+ *                    is not a multiple of 16, or the next ones are not
+ *                    consecutive. The entry still names the first slot's page.
+ *                 2  a sequence has more than width pages; its row keeps the
+ *                    first width pages.
+ *                 4  kv_indptr[b] is negative, decreases, or passes nnz; that
+ *                    row is all pad_page and its length 0.
+ *               The kernel never clears it.
+ *
+ * Behaviour:
+ *  - One launch, asynchronous on stream.
+ *  - Returns before launching: VA_ERR_NULL, VA_ERR_DTYPE, VA_ERR_SHAPE; VA_ERR_LAYOUT
+ *    for a strided kv_indptr / kv_indices; VA_ERR_UNSUPPORTED for more than 65535
+ *    sequences.
+ *  - Returns VA_ERR_CUDA if the launch fails.
+ */
+va_status verify_attn_block_table_from_indptr(const va_tensor* kv_indptr,
+                                              const va_tensor* kv_indices, va_tensor* block_table,
+                                              va_tensor* seqused_k, int32_t pad_page,
+                                              int32_t* status, void* stream);
+
 /* Static, NUL-terminated name of a status code. */
 const char* verify_attn_status_string(int32_t status);
 

@@ -28,7 +28,11 @@ _DTYPES = {torch.bfloat16: VA_BF16, torch.float8_e4m3fn: VA_FP8_E4M3,
 
 # Every symbol include/verify_attn.h declares.
 EXPORTS = ("verify_attn", "verify_attn_ex", "verify_attn_check", "verify_attn_plan",
-           "verify_attn_workspace_size", "verify_attn_status_string", "verify_attn_noalloc")
+           "verify_attn_workspace_size", "verify_attn_status_string", "verify_attn_noalloc",
+           "verify_attn_block_table_from_indptr")
+
+# Status bits of verify_attn_block_table_from_indptr.
+BT_BAD_PAGE, BT_TRUNCATED, BT_BAD_INDPTR = 1, 2, 4
 
 # Size of the library's built-in partials array used by verify_attn_noalloc.
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -79,6 +83,9 @@ def _lib():
         lib.verify_attn_workspace_size.restype = ctypes.c_size_t
         lib.verify_attn_noalloc.argtypes = tens + [ctypes.c_float, P, P, P, ctypes.c_void_p]
         lib.verify_attn_noalloc.restype = ctypes.c_int32
+        lib.verify_attn_block_table_from_indptr.argtypes = [P, P, P, P, ctypes.c_int32,
+                                                            ctypes.c_void_p, ctypes.c_void_p]
+        lib.verify_attn_block_table_from_indptr.restype = ctypes.c_int32
         lib.verify_attn_status_string.argtypes = [ctypes.c_int32]
         lib.verify_attn_status_string.restype = ctypes.c_char_p
         _LIB = lib
@@ -251,3 +258,38 @@ def run_workload_ex(w, out=None, workspace=None, num_splits=0, stream=None,
                           w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale, w.k_descale,
                           w.v_descale, out=out, workspace=workspace, num_splits=num_splits,
                           stream=stream, event_after_main=event_after_main)
+
+
+def block_table_from_indptr(kv_indptr, kv_indices, width: int, pad_page: int = 0,
+                            block_table=None, seqused_k=None, status=None, stream=None):
+    """Block table [B, width] and KV lengths [B] of a batch in flat token-slot
+    form (see include/verify_attn.h). ``status``, if given, is a one-element
+    int32 device tensor the kernel ORs BT_* bits into. Returns
+    (block_table, seqused_k)."""
+    B = kv_indptr.shape[0] - 1
+    dev = kv_indptr.device
+    if block_table is None:
+        block_table = torch.empty((B, int(width)), dtype=torch.int32, device=dev)
+    if seqused_k is None:
+        seqused_k = torch.empty((B,), dtype=torch.int32, device=dev)
+    st = 0 if status is None else status.data_ptr()
+    di, dx, db, ds = desc(kv_indptr), desc(kv_indices), desc(block_table), desc(seqused_k)
+    with torch.cuda.device(dev):
+        s = _lib().verify_attn_block_table_from_indptr(
+            _ref(di), _ref(dx), _ref(db), _ref(ds), int(pad_page), ctypes.c_void_p(st),
+            ctypes.c_void_p(_stream_handle(stream, dev)))
+    if s != VA_OK:
+        raise VerifyAttnError(s, "verify_attn_block_table_from_indptr")
+    return block_table, seqused_k
+
+
+def draft_extend_attn(q, k_cache, v_cache, kv_indptr, kv_indices, cu_seqlens_q,
+                      max_seqlen_q: int, width: int, softmax_scale: float, k_descale=None,
+                      v_descale=None, out=None, pad_page: int = 0, status=None, stream=None):
+    """The draft-extend pass: block table and lengths from the flat token-slot
+    form, then the same attention as target verify with
+    max_seqlen_k = width * 16. Two C-ABI calls on ``stream``."""
+    bt, sk = block_table_from_indptr(kv_indptr, kv_indices, width, pad_page, status=status,
+                                     stream=stream)
+    return verify_attn(q, k_cache, v_cache, bt, cu_seqlens_q, sk, max_seqlen_q, int(width) * 16,
+                       softmax_scale, k_descale, v_descale, out=out, stream=stream)

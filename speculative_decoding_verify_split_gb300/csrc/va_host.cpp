@@ -404,6 +404,43 @@ VA_EXPORT va_status verify_attn(const va_tensor* q, const va_tensor* k_cache,
                 st->ws_bytes, nullptr, static_cast<cudaStream_t>(stream));
 }
 
+// Descriptor checks of verify_attn_block_table_from_indptr (host only).
+static va_status validate_block_table_args(const va_tensor* indptr, const va_tensor* indices,
+                                           const va_tensor* bt, const va_tensor* seqused) {
+  if (!indptr || !indices || !bt || !seqused) return VA_ERR_NULL;
+  if (indptr->dtype != VA_INT32 || indices->dtype != VA_INT32 || bt->dtype != VA_INT32 ||
+      seqused->dtype != VA_INT32)
+    return VA_ERR_DTYPE;
+  if (!dims_ok(indptr, 1) || !dims_ok(indices, 1) || !dims_ok(bt, 2) || !dims_ok(seqused, 1))
+    return VA_ERR_SHAPE;
+  const int64_t B = indptr->shape[0] - 1;
+  if (B < 0 || bt->shape[0] != B || seqused->shape[0] != B) return VA_ERR_SHAPE;
+  if (B > 65535 || bt->shape[1] > INT32_MAX || indices->shape[0] > INT32_MAX)
+    return VA_ERR_UNSUPPORTED;
+  if ((B + 1 > 1 && indptr->stride[0] != 1) || (indices->shape[0] > 1 && indices->stride[0] != 1))
+    return VA_ERR_LAYOUT;
+  if (!indptr->data) return VA_ERR_NULL;
+  if (B > 0 && (!seqused->data || (bt->shape[1] > 0 && !bt->data))) return VA_ERR_NULL;
+  if (indices->shape[0] > 0 && !indices->data) return VA_ERR_NULL;
+  return VA_OK;
+}
+
+VA_EXPORT va_status verify_attn_block_table_from_indptr(const va_tensor* kv_indptr,
+                                                        const va_tensor* kv_indices,
+                                                        va_tensor* block_table, va_tensor* seqused_k,
+                                                        int32_t pad_page, int32_t* status,
+                                                        void* stream) {
+  const va_status v = validate_block_table_args(kv_indptr, kv_indices, block_table, seqused_k);
+  if (v != VA_OK) return v;
+  const cudaError_t e = va::launch_block_table(
+      static_cast<const int32_t*>(kv_indptr->data), static_cast<const int32_t*>(kv_indices->data),
+      kv_indices->shape[0], (int32_t)(kv_indptr->shape[0] - 1), (int32_t)block_table->shape[1],
+      static_cast<int32_t*>(block_table->data), block_table->stride[0], block_table->stride[1],
+      static_cast<int32_t*>(seqused_k->data), seqused_k->stride[0], pad_page, status,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+}
+
 VA_EXPORT const char* verify_attn_status_string(int32_t status) {
   switch (status) {
     case VA_OK: return "VA_OK";

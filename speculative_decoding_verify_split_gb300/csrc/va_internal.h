@@ -78,6 +78,15 @@ constexpr int kTcTileKeysBf16 = 64;  // keys per tile, BF16 KV
 constexpr int kPieceCostTiles = 4;
 
 cudaError_t launch_merge(const Params& p, cudaStream_t stream);
+
+// Block table from the flat token-slot form (va_pagetable.cu). Status bits:
+constexpr int32_t kBtBadPage = 1;     // a page's slots are not one aligned page in order
+constexpr int32_t kBtTruncated = 2;   // a sequence has more pages than the table is wide
+constexpr int32_t kBtBadIndptr = 4;   // kv_indptr decreases, is negative or passes nnz
+cudaError_t launch_block_table(const int32_t* indptr, const int32_t* indices, int64_t nnz,
+                               int32_t num_seqs, int32_t width, int32_t* bt, int64_t bt_s0,
+                               int64_t bt_s1, int32_t* seqused, int64_t sk_s0, int32_t pad,
+                               int32_t* status, cudaStream_t stream);
 cudaError_t prepare_main_tc();  // once per device: opt in to its shared memory
 cudaError_t launch_main_tc(const Params& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            cudaStream_t stream);

@@ -277,6 +277,26 @@ def named_workload(name: str, seed: int = 0, value_device: str = "cpu") -> Workl
                      value_device, HEAD_DIM, arange_table=arange)
 
 
+def flat_kv_slots(w: Workload):
+    """The workload's KV layout in the flat token-slot form of the
+    draft-extend pass (sglang PR 30105 digest, "Fix 2"): kv_indptr [B+1]
+    (token offsets) and kv_indices (the cache slot of every token,
+    page * 16 + position), both int32 on the workload's device. Input
+    construction only: each sequence's first ceil(S/16) table entries are
+    written out token by token."""
+    bt = w.block_table.cpu().to(torch.int64)
+    indptr, chunks = [0], []
+    pos = torch.arange(PAGE_SIZE, dtype=torch.int64)
+    for b, S in enumerate(w.kv_lens):
+        pages = bt[b, :(S + PAGE_SIZE - 1) // PAGE_SIZE]
+        chunks.append((pages[:, None] * PAGE_SIZE + pos[None, :]).reshape(-1)[:S])
+        indptr.append(indptr[-1] + S)
+    dev = w.block_table.device
+    slots = torch.cat(chunks) if chunks else torch.zeros(0, dtype=torch.int64)
+    return (torch.tensor(indptr, dtype=torch.int32, device=dev),
+            slots.to(torch.int32).to(dev))
+
+
 def workload_sizes(name: str, seed: int = 0) -> dict:
     """Structure-only summary (no value draws): lengths and byte counts."""
     st = workload_structure(name, seed)

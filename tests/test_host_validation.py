@@ -121,3 +121,26 @@ def test_plan_rejects():
                 (1, 1, 16, 1, 100, "fp8_e4m3", 0), (1, 1, 16, 0, 100, "bf16", 152)]:
         with pytest.raises(va.VerifyAttnError):
             va.plan(*bad)
+
+
+def _bt_call(indptr, indices, table, seqused):
+    import ctypes
+    d = [va.desc(t) for t in (indptr, indices, table, seqused)]
+    return va.library().verify_attn_block_table_from_indptr(
+        *[None if x is None else ctypes.byref(x) for x in d], 0, None, None)
+
+
+def test_block_table_builder_rejects_bad_descriptors_before_launch():
+    # host validation only: every case returns before anything is launched
+    i32 = torch.int32
+    ip, ix = torch.zeros(4, dtype=i32), torch.zeros(10, dtype=i32)
+    bt, sk = torch.zeros(3, 5, dtype=i32), torch.zeros(3, dtype=i32)
+    assert _bt_call(ip, ix, bt, None) == 1                                   # NULL
+    assert _bt_call(ip.float(), ix, bt, sk) == 3                             # dtype
+    assert _bt_call(ip, ix, torch.zeros(2, 5, dtype=i32), sk) == 2           # B mismatch
+    assert _bt_call(ip, ix, bt, torch.zeros(4, dtype=i32)) == 2
+    assert _bt_call(ip, ix, bt.view(-1), sk) == 2                            # table not 2D
+    assert _bt_call(torch.zeros(8, dtype=i32)[::2], ix, bt, sk) == 7         # strided indptr
+    assert _bt_call(ip, torch.zeros(20, dtype=i32)[::2], bt, sk) == 7        # strided indices
+    big = torch.zeros(65537, dtype=i32)
+    assert _bt_call(big, ix, torch.zeros(65536, 1, dtype=i32), torch.zeros(65536, dtype=i32)) == 4
