@@ -112,40 +112,76 @@ def visible_keys(S: int, L: int, t: int) -> int:
     return max(0, min(S, S - L + t + 1))
 
 
+def first_visible_key(S: int, L: int, t: int, window_left: int) -> int:
+    """First key draft token t sees. Without a window (window_left < 0) that
+    is key 0. With window_size = (window_left, 0) the token at position
+    i = S - L + t sees keys [i - window_left, i] (sglang PR 30105 digest,
+    "Key code excerpts": window_size = (sliding_window_size - 1, 0))."""
+    if window_left < 0:
+        return 0
+    return max(0, S - L + t - window_left)
+
+
 def gather_kv(cache_raw: np.ndarray, decode, block_table_row: np.ndarray, S: int,
-              descale: float) -> np.ndarray:
-    """[S, Hkv, D] float64: the first S token slots reached through the block table."""
-    n_pages = (S + PAGE_SIZE - 1) // PAGE_SIZE
-    if n_pages == 0:
+              descale: float, start: int = 0) -> np.ndarray:
+    """[S - start, Hkv, D] float64: token slots [start, S) reached through the
+    block table. Pages holding only keys before ``start`` are never read (a
+    sliding-window page table need not map them)."""
+    if S <= start:
         return np.zeros((0,) + cache_raw.shape[2:], dtype=np.float64)
-    pages = np.asarray(block_table_row[:n_pages], dtype=np.int64)
-    raw = cache_raw[pages]                                  # [n_pages, 16, Hkv, D]
-    raw = raw.reshape((n_pages * PAGE_SIZE,) + cache_raw.shape[2:])[:S]
+    p0 = start // PAGE_SIZE
+    n_pages = (S + PAGE_SIZE - 1) // PAGE_SIZE
+    pages = np.asarray(block_table_row[p0:n_pages], dtype=np.int64)
+    raw = cache_raw[pages]                                  # [pages, 16, Hkv, D]
+    raw = raw.reshape((len(pages) * PAGE_SIZE,) + cache_raw.shape[2:])
+    raw = raw[start - p0 * PAGE_SIZE:S - p0 * PAGE_SIZE]
     return decode(raw) * float(descale)
 
 
+def softcapped(logits: np.ndarray, softcap: float) -> np.ndarray:
+    """Logit soft-capping, softcap * tanh(s / softcap); 0 means off (sglang PR
+    30105 digest, "Key code excerpts": softcap=layer.logit_cap)."""
+    if not softcap:
+        return logits
+    return softcap * np.tanh(logits / softcap)
+
+
+def sink_weight(sink: float, m: np.ndarray) -> np.ndarray:
+    """Weight of a sink logit in the normaliser, relative to the row max m."""
+    return np.exp(sink - m)
+
+
 def softmax_attend(q_rows: np.ndarray, K: np.ndarray, V: np.ndarray,
-                   n_visible: np.ndarray, scale: float) -> np.ndarray:
-    """Row i attends to K[:n_visible[i]]; rows with no visible key give 0.
+                   n_visible: np.ndarray, scale: float, first=None, softcap: float = 0.0,
+                   sink: Optional[float] = None) -> np.ndarray:
+    """Row i attends to K[first[i]:n_visible[i]] (first defaults to 0); rows
+    with no visible key give 0.
 
     q_rows [R, D], K [S, D], V [S, D] -> [R, D]; softmax in the usual
-    max-subtracted form (exact up to fp64 rounding)."""
+    max-subtracted form (exact up to fp64 rounding). ``sink`` is an extra
+    logit with a zero value vector: it joins the normaliser only."""
     R = q_rows.shape[0]
     out = np.zeros((R, V.shape[1]), dtype=np.float64)
     if K.shape[0] == 0:
         return out
-    logits = scale * (q_rows @ K.T)                          # [R, S]
+    lo = np.zeros(R, dtype=np.int64) if first is None else np.asarray(first, dtype=np.int64)
+    logits = softcapped(scale * (q_rows @ K.T), softcap)     # [R, S]
     cols = np.arange(K.shape[0])[None, :]
-    vis = cols < n_visible[:, None]
+    vis = (cols < n_visible[:, None]) & (cols >= lo[:, None])
     logits = np.where(vis, logits, -np.inf)
-    has = n_visible > 0
+    has = vis.any(axis=1)
     if not np.any(has):
         return out
     lg = logits[has]
     m = lg.max(axis=1, keepdims=True)
+    if sink is not None:
+        m = np.maximum(m, sink)
     p = np.exp(lg - m)
     p = np.where(vis[has], p, 0.0)
-    out[has] = (p @ V) / p.sum(axis=1, keepdims=True)
+    den = p.sum(axis=1, keepdims=True)
+    if sink is not None:
+        den = den + sink_weight(sink, m)
+    out[has] = (p @ V) / den
     return out
 
 
@@ -166,11 +202,19 @@ def verify_attn_oracle(
     k_descale: Optional[float] = None,
     v_descale: Optional[float] = None,
     seqs: Optional[Sequence[int]] = None,
+    window_left: int = -1,        # sliding window: keys [i - window_left, i]; -1 = none
+    softcap: float = 0.0,         # logit soft cap; 0 = none
+    sinks: Optional[np.ndarray] = None,  # [Hq] per-head sink logits (natural log); None = none
 ) -> np.ndarray:
     """Exact (fp64) verify attention. Returns out [total_q, Hq, D] float64.
 
     ``seqs`` restricts the work to a subset of sequences (the other rows of the
-    result stay NaN), so full-size workloads can be checked on a sample."""
+    result stay NaN), so full-size workloads can be checked on a sample.
+    ``window_left``, ``softcap`` and ``sinks`` are the generic attention's
+    variants the pages pass through (sglang PR 30105 digest, "Key code
+    excerpts": window_size, softcap, sinks): the logits are
+    softcap * tanh(scale * q.k / softcap), a row sees the keys of its window
+    only, and a sink logit joins each head's softmax normaliser."""
     decode = DECODERS[kv_dtype]
     q = decode_bf16(q_raw)
     total_q, Hq, D = q.shape
@@ -189,21 +233,28 @@ def verify_attn_oracle(
         S = int(su[b])
         if L <= 0:
             continue
-        K = gather_kv(k_raw, decode, block_table[b], S, kd)     # [S, Hkv, D]
-        V = gather_kv(v_raw, decode, block_table[b], S, vd)
-        n_vis = np.array([visible_keys(S, L, t) for t in range(L)], dtype=np.int64)
+        first = np.array([first_visible_key(S, L, t, window_left) for t in range(L)],
+                         dtype=np.int64)
+        k0 = int(first.min()) if L else 0                         # keys before k0: never read
+        K = gather_kv(k_raw, decode, block_table[b], S, kd, k0)  # [S - k0, Hkv, D]
+        V = gather_kv(v_raw, decode, block_table[b], S, vd, k0)
+        n_vis = np.array([visible_keys(S, L, t) for t in range(L)], dtype=np.int64) - k0
         for h in range(Hq):
             kvh = kv_head_of(h, G, Hkv)
             rows = q[cu[b]:cu[b] + L, h, :]                       # [L, D]
+            sink = None if sinks is None else float(sinks[h])
             out[cu[b]:cu[b] + L, h, :] = softmax_attend(rows, K[:, kvh, :], V[:, kvh, :],
-                                                        n_vis, softmax_scale)
+                                                        n_vis, softmax_scale, first - k0,
+                                                        softcap, sink)
     return out
 
 
-def oracle_from_torch(w, seqs=None) -> np.ndarray:
+def oracle_from_torch(w, seqs=None, window_left=None, softcap=None, sinks=None) -> np.ndarray:
     """Convenience: run the oracle on a workload of CPU torch tensors.
 
-    Only reads the tensors' bytes (``.view`` to integer types, ``.numpy()``)."""
+    Only reads the tensors' bytes (``.view`` to integer types, ``.numpy()``).
+    The variants default to the workload's own (attributes window_left,
+    softcap, sinks when it has them)."""
     import torch
     kv_dtype = "fp8_e4m3" if w.k_cache.dtype == torch.float8_e4m3fn else "bf16"
     def raw(t):
@@ -213,6 +264,13 @@ def oracle_from_torch(w, seqs=None) -> np.ndarray:
         return t.view(torch.int16).numpy().view(np.uint16)
     kd = None if w.k_descale is None else float(w.k_descale.cpu()[0])
     vd = None if w.v_descale is None else float(w.v_descale.cpu()[0])
+    if window_left is None:
+        window_left = int(getattr(w, "window_left", -1))
+    if softcap is None:
+        softcap = float(getattr(w, "softcap", 0.0))
+    if sinks is None and getattr(w, "sinks", None) is not None:
+        sinks = w.sinks.detach().cpu().numpy().astype(np.float64)
     return verify_attn_oracle(raw(w.q), raw(w.k_cache), raw(w.v_cache), kv_dtype,
                               w.block_table.cpu().numpy(), w.cu_seqlens_q.cpu().numpy(),
-                              w.seqused_k.cpu().numpy(), w.softmax_scale, kd, vd, seqs)
+                              w.seqused_k.cpu().numpy(), w.softmax_scale, kd, vd, seqs,
+                              window_left, softcap, sinks)

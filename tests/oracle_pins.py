@@ -35,13 +35,13 @@ def _raw(t: torch.Tensor) -> np.ndarray:
     return t.view(torch.int16).numpy().view(np.uint16)
 
 
-def run(orc, w, seqs=None):
+def run(orc, w, seqs=None, **variants):
     kv_dtype = "fp8_e4m3" if w.k_cache.dtype == torch.float8_e4m3fn else "bf16"
     kd = None if w.k_descale is None else float(w.k_descale[0])
     vd = None if w.v_descale is None else float(w.v_descale[0])
     return orc.verify_attn_oracle(_raw(w.q), _raw(w.k_cache), _raw(w.v_cache), kv_dtype,
                                   w.block_table.numpy(), w.cu_seqlens_q.numpy(),
-                                  w.seqused_k.numpy(), w.softmax_scale, kd, vd, seqs)
+                                  w.seqused_k.numpy(), w.softmax_scale, kd, vd, seqs, **variants)
 
 
 def dense_kv(w, b):
@@ -57,9 +57,10 @@ def dense_kv(w, b):
     return k * kd, v * vd
 
 
-def sdpa_reference(w, b, causal=True):
+def sdpa_reference(w, b, causal=True, window_left=-1):
     """torch SDPA in float64 over the expanded (MHA) K/V of sequence b.
-    Returns [L, Hq, D]; rows with no visible key are NaN from SDPA itself."""
+    Returns [L, Hq, D]; rows with no visible key are NaN from SDPA itself.
+    With window_left >= 0 the mask also drops keys before i - window_left."""
     L = int(w.cu_seqlens_q[b + 1] - w.cu_seqlens_q[b])
     S = int(w.seqused_k[b])
     q0 = int(w.cu_seqlens_q[b])
@@ -73,6 +74,8 @@ def sdpa_reference(w, b, causal=True):
         t = torch.arange(L)[:, None]
         j = torch.arange(S)[None, :]
         mask = j <= (S - L + t)                                   # bottom-right causal
+        if window_left >= 0:
+            mask = mask & (j >= (S - L + t - window_left))
         o = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=w.softmax_scale)
     else:
         o = F.scaled_dot_product_attention(q, k, v, scale=w.softmax_scale)
@@ -240,6 +243,89 @@ def pin_empty_rows(orc):
     assert np.all(got[4:6] == 0.0)
 
 
+def pin_window_sdpa(orc):
+    """Sliding window (window_size = (w, 0)): torch SDPA with the band mask, for
+    windows from 0 (only the token's own key) to beyond the sequence."""
+    ql, kl = [4, 2, 3], [70, 19, 5]
+    w = make_workload(ql, kl, 8, 2, "bf16", seed=43)
+    for win in (0, 1, 5, 16, 33, 200):
+        got = run(orc, w, window_left=win)
+        for b in range(3):
+            q0, L = int(w.cu_seqlens_q[b]), ql[b]
+            _close(got[q0:q0 + L], sdpa_reference(w, b, window_left=win))
+
+
+def pin_window_never_reads_pages_before_it(orc):
+    """Pages wholly before every row's window may be unmapped (a sliding-window
+    page table): pointing them past the cache must not change the result."""
+    ql, kl = [3, 2], [150, 90]
+    w = make_workload(ql, kl, 4, 1, "fp8_e4m3", seed=47)
+    win = 20
+    ref = run(orc, w, window_left=win)
+    bt = w.block_table.clone()
+    for b in range(2):
+        first = max(0, kl[b] - ql[b] - win)
+        bt[b, :first // 16] = 10 ** 6                              # would raise if read
+    w.block_table = bt
+    try:
+        got = run(orc, w, window_left=win)
+    except IndexError as e:
+        raise AssertionError(f"read a page before the window: {e}")
+    _close(got, ref, 0.0)
+
+
+def pin_softcap_closed_forms(orc):
+    """A huge cap changes nothing; constant keys still give the mean of the
+    visible V; a spike key of logit 128 among zero logits with cap c weighs
+    e^(c tanh(128 / c)) against 1 for each other key."""
+    w = make_workload([2, 3], [40, 25], 4, 1, "bf16", seed=53)
+    _close(run(orc, w, softcap=1e9), run(orc, w), 1e-9)
+    L, S = 4, 37
+    w = make_workload([L], [S], 2, 1, "bf16", seed=19)
+    w.q = torch.ones_like(w.q)
+    k = torch.zeros_like(w.k_cache)
+    p = S - 2
+    k[int(w.block_table[0, p // 16]), p % 16] = 8.0                # logit 256 * 8 / 16 = 128
+    w.k_cache = k
+    cap = 2.0
+    got = run(orc, w, softcap=cap)
+    _, v = dense_kv(w, 0)
+    e = math.exp(cap * math.tanh(128.0 / cap))
+    for t in range(L):
+        n = S - L + t + 1
+        if n > p:
+            ref = ((v[:n, 0].sum(dim=0) - v[p, 0]) + e * v[p, 0]) / (n - 1 + e)
+        else:
+            ref = v[:n, 0].mean(dim=0)
+        for h in range(2):
+            _close(got[t, h], ref.numpy(), 1e-12)
+
+
+def pin_sink_closed_forms(orc):
+    """A sink of -inf changes nothing; with constant keys every visible logit
+    is c = scale q.k, so out = mean(V) n e^c / (n e^c + e^sink)."""
+    w = make_workload([2, 3], [40, 25], 4, 1, "fp8_e4m3", seed=59)
+    _close(run(orc, w, sinks=np.full(4, -np.inf)), run(orc, w), 0.0)
+    ql, kl = [4, 3], [29, 18]
+    w = make_workload(ql, kl, 4, 1, "bf16", seed=61)
+    row = w.k_cache[0, 0, 0].clone()
+    w.k_cache = w.k_cache.clone()
+    w.k_cache[:] = row
+    sinks = np.array([-1.0, 0.5, 2.0, 7.0])
+    got = run(orc, w, sinks=sinks)
+    kvec = row.to(torch.float64)
+    for b in range(2):
+        _, v = dense_kv(w, b)
+        S, L, q0 = kl[b], ql[b], int(w.cu_seqlens_q[b])
+        for t in range(L):
+            n = S - L + t + 1
+            for h in range(4):
+                c = w.softmax_scale * float(w.q[q0 + t, h].to(torch.float64) @ kvec)
+                scale = n * math.exp(c) / (n * math.exp(c) + math.exp(sinks[h]))
+                _close(got[q0 + t, h], (v[:n, 0].mean(dim=0) * scale).numpy(), 1e-12)
+
+
 ALL_PINS = [pin_e4m3_exhaustive, pin_e4m3_spec_points, pin_bf16_exhaustive, pin_sdpa_bruteforce,
             pin_gqa_equals_mha, pin_page_permutation, pin_qlen1_decode, pin_constant_keys,
-            pin_spike_boundary, pin_descale, pin_empty_rows]
+            pin_spike_boundary, pin_descale, pin_empty_rows, pin_window_sdpa,
+            pin_window_never_reads_pages_before_it, pin_softcap_closed_forms, pin_sink_closed_forms]

@@ -32,24 +32,40 @@ def _head_modulo(h, group, num_kv_heads):
     return h % num_kv_heads
 
 
-def _gather_logical_pages(cache_raw, decode, row, S, descale):
-    return _real_gather(cache_raw, decode, np.arange(len(row)), S, descale)
+def _gather_logical_pages(cache_raw, decode, row, S, descale, start=0):
+    return _real_gather(cache_raw, decode, np.arange(len(row)), S, descale, start)
 
 
-def _gather_no_descale(cache_raw, decode, row, S, descale):
-    return _real_gather(cache_raw, decode, row, S, 1.0)
+def _gather_no_descale(cache_raw, decode, row, S, descale, start=0):
+    return _real_gather(cache_raw, decode, row, S, 1.0, start)
 
 
-def _attend_no_scale(q, K, V, n, scale):
-    return _real_attend(q, K, V, n, 1.0)
+def _attend_no_scale(q, K, V, n, scale, *rest):
+    return _real_attend(q, K, V, n, 1.0, *rest)
 
 
-def _attend_keys_as_values(q, K, V, n, scale):
-    return _real_attend(q, K, K, n, scale)
+def _attend_keys_as_values(q, K, V, n, scale, *rest):
+    return _real_attend(q, K, K, n, scale, *rest)
 
 
-def _attend_reversed_rows(q, K, V, n, scale):
-    return _real_attend(q[::-1], K, V, n, scale)[::-1]
+def _attend_reversed_rows(q, K, V, n, scale, *rest):
+    return _real_attend(q[::-1], K, V, n, scale, *rest)[::-1]
+
+
+def _window_off_by_one(S, L, t, window_left):
+    return 0 if window_left < 0 else max(0, S - L + t - window_left + 1)
+
+
+def _window_ignored(S, L, t, window_left):
+    return 0
+
+
+def _no_softcap(logits, softcap):
+    return logits
+
+
+def _sink_ignored(sink, m):
+    return 0.0 * m
 
 
 def _e4m3_bias8(raw):
@@ -73,6 +89,10 @@ MUTATIONS = {
     "drops_softmax_scale": ("softmax_attend", _attend_no_scale),
     "keys_used_as_values": ("softmax_attend", _attend_keys_as_values),
     "rows_reversed": ("softmax_attend", _attend_reversed_rows),
+    "window_off_by_one": ("first_visible_key", _window_off_by_one),
+    "window_ignored": ("first_visible_key", _window_ignored),
+    "softcap_dropped": ("softcapped", _no_softcap),
+    "sink_ignored": ("sink_weight", _sink_ignored),
 }
 
 DECODER_MUTATIONS = {
