@@ -190,6 +190,48 @@ size_t verify_attn_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_
                                   int32_t num_splits);
 
 /*
+ * va_options - variants of the generic attention that the pages pass through
+ * (sglang PR 30105 digest, "Key code excerpts": unified_attention(...,
+ * window_size, softcap, sinks)). All off is window_left = -1, softcap = 0,
+ * sinks = NULL.
+ *  window_left  sliding window: the draft token at position i = S - L + t
+ *               sees keys [i - window_left, i] (the pages' window_size =
+ *               (sliding_window_size - 1, 0)); -1 = no window. Block-table
+ *               pages holding only keys before every token's window are never
+ *               read, so a sliding-window page table need not map them.
+ *  softcap      > 0: each logit s = softmax_scale * k_descale * q.k becomes
+ *               softcap * tanh(s / softcap) before masking; 0 = off.
+ *  sinks        [Hq] fp32, contiguous, or NULL: a per-query-head logit
+ *               (natural-log units) that joins that head's softmax normaliser
+ *               with a zero value vector. A row that sees no key is still 0.
+ */
+typedef struct va_options {
+  int32_t window_left;
+  float softcap;
+  const va_tensor* sinks;
+} va_options;
+
+/*
+ * verify_attn_opt - verify_attn with the variants above.
+ *  opts       NULL means all variants off (then this is verify_attn_ex).
+ *  workspace  a caller workspace as for verify_attn_ex, or NULL to use the
+ *             library's own per-device workspace as verify_attn does (which
+ *             may then allocate, so not during stream capture).
+ * Other arguments, layouts and results are those of verify_attn_ex; num_splits
+ * 0 lets the heuristic pick (with a window it counts only the window's tiles).
+ * Returns VA_ERR_SHAPE / VA_ERR_DTYPE / VA_ERR_NULL / VA_ERR_UNSUPPORTED for
+ * bad options before launching (window_left < -1, softcap negative or not
+ * finite, sinks not fp32 [Hq] contiguous).
+ */
+va_status verify_attn_opt(const va_tensor* q, const va_tensor* k_cache, const va_tensor* v_cache,
+                          const va_tensor* block_table, const va_tensor* cu_seqlens_q,
+                          const va_tensor* seqused_k, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                          float softmax_scale, const va_tensor* k_descale,
+                          const va_tensor* v_descale, va_tensor* out, const va_options* opts,
+                          void* workspace, size_t workspace_bytes, int32_t num_splits,
+                          void* stream);
+
+/*
  * verify_attn_noalloc - verify_attn for callers that cannot allocate device
  * memory. The pages have no counterpart; this is a library addition.
  *

@@ -29,7 +29,7 @@ _DTYPES = {torch.bfloat16: VA_BF16, torch.float8_e4m3fn: VA_FP8_E4M3,
 # Every symbol include/verify_attn.h declares.
 EXPORTS = ("verify_attn", "verify_attn_ex", "verify_attn_check", "verify_attn_plan",
            "verify_attn_workspace_size", "verify_attn_status_string", "verify_attn_noalloc",
-           "verify_attn_block_table_from_indptr")
+           "verify_attn_block_table_from_indptr", "verify_attn_opt")
 
 # Status bits of verify_attn_block_table_from_indptr.
 BT_BAD_PAGE, BT_TRUNCATED, BT_BAD_INDPTR = 1, 2, 4
@@ -48,6 +48,11 @@ class VaPlan(ctypes.Structure):
                 ("max_rows", ctypes.c_int32), ("num_work", ctypes.c_int32),
                 ("kernel", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64)]
+
+
+class VaOptions(ctypes.Structure):
+    _fields_ = [("window_left", ctypes.c_int32), ("softcap", ctypes.c_float),
+                ("sinks", ctypes.POINTER(VaTensor))]
 
 
 class VerifyAttnError(RuntimeError):
@@ -86,6 +91,10 @@ def _lib():
         lib.verify_attn_block_table_from_indptr.argtypes = [P, P, P, P, ctypes.c_int32,
                                                             ctypes.c_void_p, ctypes.c_void_p]
         lib.verify_attn_block_table_from_indptr.restype = ctypes.c_int32
+        lib.verify_attn_opt.argtypes = tens + [ctypes.c_float, P, P, P, ctypes.POINTER(VaOptions),
+                                               ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32,
+                                               ctypes.c_void_p]
+        lib.verify_attn_opt.restype = ctypes.c_int32
         lib.verify_attn_status_string.argtypes = [ctypes.c_int32]
         lib.verify_attn_status_string.restype = ctypes.c_char_p
         _LIB = lib
@@ -283,13 +292,51 @@ def block_table_from_indptr(kv_indptr, kv_indices, width: int, pad_page: int = 0
     return block_table, seqused_k
 
 
+def verify_attn_opt(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
+                    max_seqlen_q: int, max_seqlen_k: int, softmax_scale: float, k_descale=None,
+                    v_descale=None, out=None, window_left: int = -1, softcap: float = 0.0,
+                    sinks=None, workspace: Optional[torch.Tensor] = None, num_splits: int = 0,
+                    stream=None):
+    """verify_attn with the generic attention's variants (see include/verify_attn.h):
+    sliding window (keys [i - window_left, i]), logit soft cap, per-head sinks
+    ([Hq] fp32). ``workspace`` None uses the library's own."""
+    if out is None:
+        out = torch.empty_like(q)
+    ds, r = _args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, k_descale,
+                  v_descale, out)
+    dsk = desc(sinks)
+    opts = VaOptions(int(window_left), float(softcap),
+                     ctypes.pointer(dsk) if dsk is not None else None)
+    if workspace is None:
+        addr, nbytes = 0, 0
+    else:
+        a = workspace.data_ptr()
+        off = (-a) % 256
+        addr, nbytes = a + off, workspace.numel() - off
+    with torch.cuda.device(q.device):
+        s = _lib().verify_attn_opt(r[0], r[1], r[2], r[3], r[4], r[5], int(max_seqlen_q),
+                                   int(max_seqlen_k), float(softmax_scale), r[6], r[7], r[8],
+                                   ctypes.byref(opts), ctypes.c_void_p(addr), nbytes,
+                                   int(num_splits), ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if s != VA_OK:
+        raise VerifyAttnError(s, "verify_attn_opt")
+    return out
+
+
 def draft_extend_attn(q, k_cache, v_cache, kv_indptr, kv_indices, cu_seqlens_q,
                       max_seqlen_q: int, width: int, softmax_scale: float, k_descale=None,
-                      v_descale=None, out=None, pad_page: int = 0, status=None, stream=None):
+                      v_descale=None, out=None, pad_page: int = 0, status=None, stream=None,
+                      window_left: int = -1, softcap: float = 0.0, sinks=None):
     """The draft-extend pass: block table and lengths from the flat token-slot
     form, then the same attention as target verify with
-    max_seqlen_k = width * 16. Two C-ABI calls on ``stream``."""
+    max_seqlen_k = width * 16 (and the pages' window / softcap / sinks
+    pass-through). Two C-ABI calls on ``stream``."""
     bt, sk = block_table_from_indptr(kv_indptr, kv_indices, width, pad_page, status=status,
                                      stream=stream)
-    return verify_attn(q, k_cache, v_cache, bt, cu_seqlens_q, sk, max_seqlen_q, int(width) * 16,
-                       softmax_scale, k_descale, v_descale, out=out, stream=stream)
+    if window_left < 0 and not softcap and sinks is None:
+        return verify_attn(q, k_cache, v_cache, bt, cu_seqlens_q, sk, max_seqlen_q,
+                           int(width) * 16, softmax_scale, k_descale, v_descale, out=out,
+                           stream=stream)
+    return verify_attn_opt(q, k_cache, v_cache, bt, cu_seqlens_q, sk, max_seqlen_q,
+                           int(width) * 16, softmax_scale, k_descale, v_descale, out=out,
+                           window_left=window_left, softcap=softcap, sinks=sinks, stream=stream)

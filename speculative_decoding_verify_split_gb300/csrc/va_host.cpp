@@ -125,7 +125,7 @@ va_status validate(const va_tensor* q, const va_tensor* k, const va_tensor* v,
 }
 
 va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t max_k, int32_t kv_dtype,
-                    int32_t num_sms, int32_t force, va_plan* plan) {
+                    int32_t num_sms, int32_t force, va_plan* plan, int32_t window_left) {
   if (!plan) return VA_ERR_NULL;
   if (B < 0 || hkv < 1 || hq < 1 || hq % hkv != 0 || max_q < 1 || max_k < 0 || num_sms < 1)
     return VA_ERR_UNSUPPORTED;
@@ -134,7 +134,12 @@ va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t m
   if (G * max_q > kMaxRows) return VA_ERR_UNSUPPORTED;
   const int tile = kv_dtype == VA_FP8_E4M3 ? kTcTileKeysFp8 : kTcTileKeysBf16;
   const int64_t J = B * hkv;
-  const int64_t tiles_bound = J * ((max_k + tile - 1) / tile);
+  int64_t item_tiles = (max_k + tile - 1) / tile;
+  if (window_left >= 0) {  // a window of max_q + window_left keys spans at most this many tiles
+    const int64_t w_tiles = ((int64_t)max_q + window_left + tile - 1) / tile + 1;
+    if (w_tiles < item_tiles) item_tiles = w_tiles;
+  }
+  const int64_t tiles_bound = J * item_tiles;
   if (tiles_bound + J * kPieceCostTiles > INT32_MAX / 2) return VA_ERR_UNSUPPORTED;
   // Heuristic: one CTA per SM (the main kernel keeps one CTA per SM), fewer
   // only when the upper-bound workload has fewer tiles than SMs. A CTA's
@@ -228,11 +233,25 @@ static va_status device_state(DeviceState** out) {
   return VA_OK;
 }
 
+va_status validate_options(const va_options* opts, const Shapes& sh) {
+  if (!opts) return VA_OK;
+  if (opts->window_left < -1) return VA_ERR_UNSUPPORTED;
+  if (!(opts->softcap >= 0.f) || !std::isfinite(opts->softcap)) return VA_ERR_UNSUPPORTED;
+  const va_tensor* t = opts->sinks;
+  if (t) {
+    if (t->dtype != VA_FP32) return VA_ERR_DTYPE;
+    if (!dims_ok(t, 1) || t->shape[0] != sh.hq) return VA_ERR_SHAPE;
+    if (sh.hq > 1 && t->stride[0] != 1) return VA_ERR_LAYOUT;
+    if (!t->data) return VA_ERR_NULL;
+  }
+  return VA_OK;
+}
+
 va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, const va_tensor* bt,
                  const va_tensor* cu, const va_tensor* su, int32_t max_q, int32_t max_k,
                  float scale, const va_tensor* kd, const va_tensor* vd, va_tensor* out,
                  const Shapes& sh, const va_plan& plan, void* ws, size_t ws_bytes,
-                 cudaEvent_t ev_mid, cudaStream_t stream) {
+                 cudaEvent_t ev_mid, cudaStream_t stream, const va_options* opts) {
   if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;  // no output rows
   if ((size_t)plan.workspace_bytes > ws_bytes || !ws) return VA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return VA_ERR_WORKSPACE;
@@ -270,6 +289,9 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
   p.max_seqlen_k = max_k;
   p.kv_fp8 = sh.kv_dtype == VA_FP8_E4M3 ? 1 : 0;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.window_left = opts ? opts->window_left : -1;
+  p.softcap_log2 = opts ? (float)((double)opts->softcap * 1.4426950408889634) : 0.f;
+  p.sinks = (opts && opts->sinks) ? static_cast<const float*>(opts->sinks->data) : nullptr;
   p.tile_keys = plan.tile_keys;
   p.num_splits = plan.num_splits;
   p.max_rows = plan.max_rows;
@@ -338,6 +360,54 @@ VA_EXPORT size_t verify_attn_workspace_size(int32_t num_seqs, int32_t num_kv_hea
   return (size_t)plan.workspace_bytes;
 }
 
+// Shared body of verify_attn, verify_attn_ex and verify_attn_opt. A NULL
+// workspace with own_ws uses (and grows) the library's per-device workspace.
+static va_status run_call(const va_tensor* q, const va_tensor* k_cache, const va_tensor* v_cache,
+                          const va_tensor* block_table, const va_tensor* cu_seqlens_q,
+                          const va_tensor* seqused_k, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                          float softmax_scale, const va_tensor* k_descale,
+                          const va_tensor* v_descale, va_tensor* out, const va_options* opts,
+                          void* workspace, size_t workspace_bytes, bool own_ws, int32_t num_splits,
+                          cudaEvent_t ev_mid, cudaStream_t stream) {
+  Shapes sh;
+  va_status s = validate(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
+                         max_seqlen_k, k_descale, v_descale, out, &sh);
+  if (s != VA_OK) return s;
+  s = validate_options(opts, sh);
+  if (s != VA_OK) return s;
+  if (num_splits < 0) return VA_ERR_UNSUPPORTED;
+  std::unique_lock<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  s = device_state(&st);
+  if (s != VA_OK) return s;
+  va_plan plan;
+  s = make_plan(sh.num_seqs, sh.hkv, sh.hq, max_seqlen_q, max_seqlen_k, sh.kv_dtype, st->sms,
+                num_splits, &plan, opts ? opts->window_left : -1);
+  if (s != VA_OK) return s;
+  if (own_ws) {
+    if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;
+    if ((size_t)plan.workspace_bytes > st->ws_bytes) {
+      // Grow only. cudaFree waits for work already queued on the old buffer.
+      if (st->ws) cudaFree(st->ws);
+      st->ws = nullptr;
+      st->ws_bytes = 0;
+      if (cudaMalloc(&st->ws, (size_t)plan.workspace_bytes) != cudaSuccess) {
+        st->ws = nullptr;
+        return VA_ERR_CUDA;
+      }
+      if (cudaMemset(st->ws, 0, (size_t)plan.workspace_bytes) != cudaSuccess) return VA_ERR_CUDA;
+      st->ws_bytes = (size_t)plan.workspace_bytes;
+    }
+    workspace = st->ws;
+    workspace_bytes = st->ws_bytes;
+  } else {
+    lk.unlock();
+  }
+  return launch(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
+                max_seqlen_k, softmax_scale, k_descale, v_descale, out, sh, plan, workspace,
+                workspace_bytes, ev_mid, stream, opts);
+}
+
 VA_EXPORT va_status verify_attn_ex(const va_tensor* q, const va_tensor* k_cache,
                                    const va_tensor* v_cache, const va_tensor* block_table,
                                    const va_tensor* cu_seqlens_q, const va_tensor* seqused_k,
@@ -345,27 +415,10 @@ VA_EXPORT va_status verify_attn_ex(const va_tensor* q, const va_tensor* k_cache,
                                    const va_tensor* k_descale, const va_tensor* v_descale,
                                    va_tensor* out, void* workspace, size_t workspace_bytes,
                                    int32_t num_splits, void* event_after_main, void* stream) {
-  Shapes sh;
-  va_status s = validate(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
-                         max_seqlen_k, k_descale, v_descale, out, &sh);
-  if (s != VA_OK) return s;
-  if (num_splits < 0) return VA_ERR_UNSUPPORTED;
-  int sms = 0;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    DeviceState* st = nullptr;
-    s = device_state(&st);
-    if (s != VA_OK) return s;
-    sms = st->sms;
-  }
-  va_plan plan;
-  s = make_plan(sh.num_seqs, sh.hkv, sh.hq, max_seqlen_q, max_seqlen_k, sh.kv_dtype, sms,
-                num_splits, &plan);
-  if (s != VA_OK) return s;
-  return launch(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
-                max_seqlen_k, softmax_scale, k_descale, v_descale, out, sh, plan, workspace,
-                workspace_bytes, static_cast<cudaEvent_t>(event_after_main),
-                static_cast<cudaStream_t>(stream));
+  return run_call(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
+                  max_seqlen_k, softmax_scale, k_descale, v_descale, out, nullptr, workspace,
+                  workspace_bytes, false, num_splits, static_cast<cudaEvent_t>(event_after_main),
+                  static_cast<cudaStream_t>(stream));
 }
 
 VA_EXPORT va_status verify_attn(const va_tensor* q, const va_tensor* k_cache,
@@ -374,34 +427,22 @@ VA_EXPORT va_status verify_attn(const va_tensor* q, const va_tensor* k_cache,
                                 int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
                                 const va_tensor* k_descale, const va_tensor* v_descale,
                                 va_tensor* out, void* stream) {
-  Shapes sh;
-  va_status s = validate(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
-                         max_seqlen_k, k_descale, v_descale, out, &sh);
-  if (s != VA_OK) return s;
-  std::lock_guard<std::mutex> lk(g_mu);
-  DeviceState* st = nullptr;
-  s = device_state(&st);
-  if (s != VA_OK) return s;
-  va_plan plan;
-  s = make_plan(sh.num_seqs, sh.hkv, sh.hq, max_seqlen_q, max_seqlen_k, sh.kv_dtype, st->sms, 0,
-                &plan);
-  if (s != VA_OK) return s;
-  if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;
-  if ((size_t)plan.workspace_bytes > st->ws_bytes) {
-    // Grow only. cudaFree waits for work already queued on the old buffer.
-    if (st->ws) cudaFree(st->ws);
-    st->ws = nullptr;
-    st->ws_bytes = 0;
-    if (cudaMalloc(&st->ws, (size_t)plan.workspace_bytes) != cudaSuccess) {
-      st->ws = nullptr;
-      return VA_ERR_CUDA;
-    }
-    if (cudaMemset(st->ws, 0, (size_t)plan.workspace_bytes) != cudaSuccess) return VA_ERR_CUDA;
-    st->ws_bytes = (size_t)plan.workspace_bytes;
-  }
-  return launch(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
-                max_seqlen_k, softmax_scale, k_descale, v_descale, out, sh, plan, st->ws,
-                st->ws_bytes, nullptr, static_cast<cudaStream_t>(stream));
+  return run_call(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
+                  max_seqlen_k, softmax_scale, k_descale, v_descale, out, nullptr, nullptr, 0, true,
+                  0, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+VA_EXPORT va_status verify_attn_opt(const va_tensor* q, const va_tensor* k_cache,
+                                    const va_tensor* v_cache, const va_tensor* block_table,
+                                    const va_tensor* cu_seqlens_q, const va_tensor* seqused_k,
+                                    int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
+                                    const va_tensor* k_descale, const va_tensor* v_descale,
+                                    va_tensor* out, const va_options* opts, void* workspace,
+                                    size_t workspace_bytes, int32_t num_splits, void* stream) {
+  return run_call(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
+                  max_seqlen_k, softmax_scale, k_descale, v_descale, out, opts, workspace,
+                  workspace_bytes, workspace == nullptr, num_splits, nullptr,
+                  static_cast<cudaStream_t>(stream));
 }
 
 // Descriptor checks of verify_attn_block_table_from_indptr (host only).

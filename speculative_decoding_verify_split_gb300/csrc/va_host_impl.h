@@ -21,16 +21,22 @@ va_status validate(const va_tensor* q, const va_tensor* k, const va_tensor* v,
                    int32_t max_seqlen_q, int32_t max_seqlen_k, const va_tensor* kd,
                    const va_tensor* vd, const va_tensor* out, Shapes* sh);
 
-// The split heuristic (pure host code).
+// The split heuristic (pure host code). With a sliding window (window_left
+// >= 0) an item's tiles are bounded by the window.
 va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t max_k,
-                    int32_t kv_dtype, int32_t num_sms, int32_t force, va_plan* plan);
+                    int32_t kv_dtype, int32_t num_sms, int32_t force, va_plan* plan,
+                    int32_t window_left = -1);
 
-// Launches the main and merge kernels with the given workspace.
+// Checks the variant options against the shapes (NULL = all off).
+va_status validate_options(const va_options* opts, const Shapes& sh);
+
+// Launches the main and merge kernels with the given workspace and options
+// (NULL = all off).
 va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, const va_tensor* bt,
                  const va_tensor* cu, const va_tensor* su, int32_t max_q, int32_t max_k,
                  float scale, const va_tensor* kd, const va_tensor* vd, va_tensor* out,
                  const Shapes& sh, const va_plan& plan, void* ws, size_t ws_bytes,
-                 cudaEvent_t ev_mid, cudaStream_t stream);
+                 cudaEvent_t ev_mid, cudaStream_t stream, const va_options* opts = nullptr);
 
 // SM count of the current device (initialises the per-device state once).
 va_status current_device_sms(int* sms);

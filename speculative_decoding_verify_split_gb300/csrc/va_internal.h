@@ -34,6 +34,10 @@ struct Params {
   int32_t num_seqs, hq, hkv, group, num_blocks, total_q, max_seqlen_q, max_seqlen_k;
   int32_t kv_fp8;
   float scale_log2;  // softmax_scale * log2(e)
+  // Variants of the generic attention (sliding window, logit soft-cap, sinks).
+  int32_t window_left;     // -1: none; else position i sees keys [i - window_left, i]
+  float softcap_log2;      // 0: none; else softcap * log2(e): x -> c tanh(x / c) in log2 units
+  const float* sinks;      // nullable, [hq]: per-head sink logits (natural log)
 
   // Split-KV decomposition: one stream of key tiles over all work items
   // j = b * hkv + kvh, cut into num_splits equal ranges (one per CTA). Each

@@ -115,6 +115,7 @@ constexpr uint32_t kColO = 0;    // 256 fp32 columns
 constexpr uint32_t kColS = 256;  // four 64-column S tiles
 constexpr uint32_t kTmemCols = 512;
 
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kPShift = 6.f;      // P = 2^(s - m_ref + kPShift)
 constexpr float kHeadroom = 1.f;    // m_ref = tile max + kHeadroom when it moves
 constexpr float kOvershoot = 2.5f;  // move only if the tile max > m_ref + kOvershoot
@@ -141,8 +142,10 @@ enum : int {
 };
 static_assert(8 * kNumBars + 16 + 34 * 8 <= 1024, "barrier area");
 
+// One (sequence, KV head) item's share of this CTA. Tile indices are absolute
+// within the sequence: the item's tiles are [tb, nt), this CTA's [lt0, lt1).
 struct Piece {
-  int j, b, kvh, S, L, q0, R, nt, lt0, lt1;
+  int j, b, kvh, S, L, q0, R, nt, tb, lt0, lt1;
   bool direct;
 };
 
@@ -163,10 +166,11 @@ __device__ __forceinline__ bool next_piece(const Params& p, long long t0, long l
     pc.L = seq_q_len(p, pc.b);
     pc.q0 = p.cu_q[pc.b];
     pc.R = p.group * pc.L;
-    pc.nt = nt;
-    pc.lt0 = (int)((t0 > ts ? t0 : ts) - ts);
-    pc.lt1 = (int)((t1 < ts + nt ? t1 : ts + nt) - ts);
-    pc.direct = (pc.lt0 == 0 && pc.lt1 == nt);
+    pc.tb = first_tile(p, pc.S, pc.L);
+    pc.nt = pc.tb + nt;
+    pc.lt0 = pc.tb + (int)((t0 > ts ? t0 : ts) - ts);
+    pc.lt1 = pc.tb + (int)((t1 < ts + nt ? t1 : ts + nt) - ts);
+    pc.direct = (pc.lt0 == pc.tb && pc.lt1 == pc.nt);
     ts += work_cost(p, nt);  // the next item's first tile follows its start-up units
     ++j;
     return true;
@@ -211,7 +215,9 @@ __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t
     mma_f16(d, a, b, idesc, acc);
 }
 
-template <bool FP8>
+// VAR: compiled with the sliding-window / soft-cap / sink code (the plain path
+// is compiled without it).
+template <bool FP8, bool VAR>
 __global__ void __launch_bounds__(kThreads, 1)
     va_main_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v) {
@@ -311,6 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (ok && next_piece(p, t0, t1, j, ts, pc)) {
       const int npages = (pc.S + kPageSize - 1) / kPageSize;
+      // pages wholly before the window are never loaded (a sliding-window
+      // page table need not map them); the softmax zeroes their V rows
+      const int pg_first = VAR ? first_key(p, pc.S, pc.L) / kPageSize : 0;
       const int* bt_row = p.block_table + (int64_t)pc.b * p.bt_s0;
       int win = -1;       // first page index cached in the lanes
       int my_page = -1;   // page id of page (win + lane)
@@ -332,7 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kPagesPerTile; ++i) {
           ids[i] = __shfl_sync(0xffffffffu, my_page, pg0 + i - win);
-          const bool v = (pg0 + i) < npages && (unsigned)ids[i] < (unsigned)p.num_blocks;
+          const bool v = (pg0 + i) < npages && (pg0 + i) >= pg_first &&
+                         (unsigned)ids[i] < (unsigned)p.num_blocks;
           ids[i] = v ? ids[i] : -1;
           nvalid += v ? 1u : 0u;
         }
@@ -611,6 +621,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_ref = -INFINITY;
       float l = 0.f;
       const int vis_end = pc.S - pc.L + tq;  // last visible key of this row
+      // first visible key of this row (sliding window), and the largest over rows
+      const int vis_lo = VAR && p.window_left >= 0 ? pc.S - pc.L + tq - p.window_left : 0;
+      const int vis_lo_max = VAR && p.window_left >= 0 ? pc.S - 1 - p.window_left : 0;
       const int first = it;
       for (int lt = pc.lt0; lt < pc.lt1; ++lt, ++it) {
         const int cur = it;
@@ -651,11 +664,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(v[i]) * rs;
           }
+          if constexpr (VAR) {
+            if (p.softcap_log2 > 0.f) {
+              // soft cap in log2 units, c tanh(x / c), before masking, with
+              // tanh(y) = 1 - 2 / (1 + e^(2y)) (ends at -1 and 1 without overflow)
+              const float c = p.softcap_log2;
+              const float k2 = 2.f * kLog2e / c;
+#pragma unroll
+              for (int i = 0; i < kKpt; ++i) x[i] = c - __fdividef(2.f * c, 1.f + ex2(x[i] * k2));
+            }
+          }
           const int key0 = lt * kT + kKpt * qtr;
           if (lt * kT + kT - 1 > pc.S - pc.L) {  // tail tile: causal mask
 #pragma unroll
             for (int i = 0; i < kKpt; ++i)
               if (key0 + i > vis_end) x[i] = -INFINITY;
+          }
+          if constexpr (VAR) {
+            if (lt * kT < vis_lo_max) {  // a window's first tiles: keys before the row's window
+#pragma unroll
+              for (int i = 0; i < kKpt; ++i)
+                if (key0 + i < vis_lo) x[i] = -INFINITY;
+            }
           }
         }
         float tmax = -INFINITY;
@@ -758,9 +788,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(base + 128) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
         }
         l += ls0 + ls1;
-        // last tile of the item: V rows past S (partial page, pages never loaded)
-        // are zeroed so that 0 * garbage cannot reach O
-        if (lt == pc.nt - 1 && (pc.S % kT) != 0) {
+        // V rows no row may see and whose pages may hold anything are zeroed,
+        // so that 0 * garbage cannot reach O: past S in the item's last tile
+        // (partial page, pages never loaded), and in its first tile the pages
+        // wholly before a sliding window (never loaded)
+        const int zt0 = (lt == pc.nt - 1 && (pc.S % kT) != 0) ? pc.S - lt * kT : kT;
+        int zh1 = 0;
+        if constexpr (VAR) {
+          const int k_first = first_key(p, pc.S, pc.L);
+          if (lt == pc.tb && k_first >= kPageSize) zh1 = (k_first / kPageSize) * kPageSize - lt * kT;
+        }
+        if (zt0 < kT || zh1 > 0) {
           const int vs = cur % C::kVSlots;
           // FullV(vs) alternates between the tiles that share slot vs, so its
           // parity names tile cur only once the slot's previous tile
@@ -772,11 +810,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (xv >= 0 && !wait_or_fail(kBarPFree + (xv & (kPBufs - 1)), (xv / kPBufs) & 1, 2049)) continue;
           }
           if (!wait_or_fail(kBarFullV + vs, (cur / C::kVSlots) & 1, 2048)) continue;
-          const int z0 = pc.S - lt * kT;
-          const int nz = kT - z0;
+          const int nz = zh1 + (kT - zt0);  // rows [0, zh1) and [zt0, kT)
           unsigned char* vst = sm + (C::kKSlots + vs) * C::kTensorBytes;
           for (int idx = tid - 128; idx < nz * 8 * C::kChunks; idx += kSoftmaxThreads) {
-            const int row = z0 + idx / (8 * C::kChunks);
+            const int k = idx / (8 * C::kChunks);
+            const int row = k < zh1 ? k : zt0 + (k - zh1);
             const int rem = idx % (8 * C::kChunks);
             const int ch = rem >> 3;
             const int piece16 = rem & 7;
@@ -792,9 +830,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // -- epilogue: this thread writes O[r][128 kh + 64 sub, +64)
       wait_or_fail(kBarOFull, piece_idx & 1, 4096);
       tc_fence_after();
-      const float lrow = exchange(l, false);
+      float lrow = exchange(l, false);
       ++piece_idx;
       if (!ok) continue;
+      // an attention sink joins the normaliser once per row: here for rows
+      // written directly, in the merge for split ones
+      if constexpr (VAR) {
+        if (p.sinks && pc.direct && row_ok && m_ref != -INFINITY)
+          lrow += exp2f(p.sinks[pc.kvh * G + gq] * kLog2e - (m_ref - kPShift));
+      }
       const float inv = lrow > 0.f ? vd / lrow : 0.f;
       const int64_t piece = (int64_t)pc.j + c;
       auto emit = [&](const uint32_t (&o)[32], int col) {
@@ -860,20 +904,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+template <bool FP8, bool VAR>
+cudaError_t set_smem() {
+  return cudaFuncSetAttribute(va_main_tc_kernel<FP8, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<FP8>::kSmemBytes);
+}
+
 cudaError_t prepare_main_tc() {
-  cudaError_t e = cudaFuncSetAttribute(va_main_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg<true>::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(va_main_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<false>::kSmemBytes);
+  cudaError_t e = set_smem<true, false>();
+  if (e == cudaSuccess) e = set_smem<false, false>();
+  if (e == cudaSuccess) e = set_smem<true, true>();
+  if (e == cudaSuccess) e = set_smem<false, true>();
+  return e;
 }
 
 cudaError_t launch_main_tc(const Params& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            cudaStream_t stream) {
-  if (p.kv_fp8)
-    va_main_tc_kernel<true><<<p.num_splits, kThreads, Cfg<true>::kSmemBytes, stream>>>(p, tm_k, tm_v);
-  else
-    va_main_tc_kernel<false><<<p.num_splits, kThreads, Cfg<false>::kSmemBytes, stream>>>(p, tm_k, tm_v);
+  const bool var = p.window_left >= 0 || p.softcap_log2 > 0.f || p.sinks != nullptr;
+  const dim3 grid(p.num_splits);
+  if (p.kv_fp8) {
+    if (var)
+      va_main_tc_kernel<true, true><<<grid, kThreads, Cfg<true>::kSmemBytes, stream>>>(p, tm_k, tm_v);
+    else
+      va_main_tc_kernel<true, false><<<grid, kThreads, Cfg<true>::kSmemBytes, stream>>>(p, tm_k, tm_v);
+  } else {
+    if (var)
+      va_main_tc_kernel<false, true><<<grid, kThreads, Cfg<false>::kSmemBytes, stream>>>(p, tm_k, tm_v);
+    else
+      va_main_tc_kernel<false, false><<<grid, kThreads, Cfg<false>::kSmemBytes, stream>>>(p, tm_k, tm_v);
+  }
   return cudaGetLastError();
 }
 

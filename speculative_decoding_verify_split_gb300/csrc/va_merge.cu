@@ -27,6 +27,8 @@ constexpr int kRowsPerCta = 4;
 constexpr int kThreadsPerRow = kHeadDim / 4;  // 64
 constexpr int kSegChunk = 8;
 
+// SINKS: compiled with the attention-sink term.
+template <bool SINKS>
 __global__ void __launch_bounds__(kRowsPerCta * kThreadsPerRow, 4) va_merge_kernel(const Params p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int j = blockIdx.x;
@@ -102,6 +104,8 @@ __global__ void __launch_bounds__(kRowsPerCta * kThreadsPerRow, 4) va_merge_kern
     *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
     return;
   }
+  if constexpr (SINKS)  // the attention sink's share of the normaliser, once per row
+    den += exp2f(p.sinks[kvh * G + g] * 1.4426950408889634f - M);
   const float vd = p.v_descale ? *p.v_descale : 1.0f;
   const float inv = vd / den;
   const uint32_t w0 = (uint32_t)float_to_bf16_bits(acc.x * inv) | ((uint32_t)float_to_bf16_bits(acc.y * inv) << 16);
@@ -123,7 +127,8 @@ cudaError_t launch_merge(const Params& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, va_merge_kernel, p);
+  return p.sinks ? cudaLaunchKernelEx(&cfg, va_merge_kernel<true>, p)
+                 : cudaLaunchKernelEx(&cfg, va_merge_kernel<false>, p);
 }
 
 }  // namespace va

@@ -30,12 +30,29 @@ __device__ __forceinline__ int seq_kv_len(const Params& p, int b) {
   return S > cap ? cap : S;
 }
 
-// Key tiles of work item j (b = j / hkv). A sequence without draft tokens
-// needs no work.
+// First key any draft token of a sequence (S cached tokens, L draft tokens)
+// can see: 0, or with a sliding window the start of the first token's window.
+__device__ __forceinline__ int first_key(const Params& p, int S, int L) {
+  if (p.window_left < 0) return 0;
+  const int k0 = S - L - p.window_left;
+  return k0 > 0 ? k0 : 0;
+}
+
+// First key tile of a sequence's work (tiles wholly before the window are
+// never read).
+__device__ __forceinline__ int first_tile(const Params& p, int S, int L) {
+  return first_key(p, S, L) / p.tile_keys;
+}
+
+// Key tiles of work item j (b = j / hkv): those from the first visible key to
+// the end. A sequence without draft tokens needs no work.
 __device__ __forceinline__ int work_tiles(const Params& p, int j) {
   const int b = j / p.hkv;
-  if (seq_q_len(p, b) == 0) return 0;
-  return (seq_kv_len(p, b) + p.tile_keys - 1) / p.tile_keys;
+  const int L = seq_q_len(p, b);
+  if (L == 0) return 0;
+  const int S = seq_kv_len(p, b);
+  const int nt = (S + p.tile_keys - 1) / p.tile_keys;
+  return nt > 0 ? nt - first_tile(p, S, L) : 0;
 }
 
 // Split cost of work item j with nt tiles: the tiles plus the item's start-up
@@ -109,7 +126,9 @@ __device__ long long scan_work(const Params& p, long long* scratch, bool write_m
 // The block-table entry of item j's tile lt, prefetched into L2: the TMA
 // producers' first load, whose latency then overlaps the CTA's setup.
 __device__ __forceinline__ void prefetch_first_pages(const Params& p, int j, long long lt) {
-  const int* bt = p.block_table + (int64_t)(j / p.hkv) * p.bt_s0 +
+  const int b = j / p.hkv;
+  lt += first_tile(p, seq_kv_len(p, b), seq_q_len(p, b));  // lt counts from the item's first tile
+  const int* bt = p.block_table + (int64_t)b * p.bt_s0 +
                   (int64_t)(lt * p.tile_keys / kPageSize) * p.bt_s1;
   asm volatile("prefetch.global.L2 [%0];" ::"l"(bt));
 }
