@@ -162,6 +162,23 @@ def needs_flush(w):
     return w.algorithmic_bytes() < 2 * L2_BYTES
 
 
+def max_over_ranks(x: float, world: int, dist, device) -> float:
+    """The largest of every rank's x (the slowest rank's time); x itself on
+    one rank. A collective of the timing only: the ranks' work is
+    independent (replicas)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(alg_bytes: int, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank's algorithmic bytes over the slowest step time."""
+    return alg_bytes * world / (ms_per_step / 1e3) / 1e9
+
+
 def workload_config(w, name, world):
     return {"workload": name, "num_seqs": w.num_seqs, "q_lens": sorted(set(w.q_lens)),
             "kv_len_range": [min(w.kv_lens), max(w.kv_lens)], "kv_tokens": sum(w.kv_lens),
@@ -344,12 +361,9 @@ def run_ours(args):
         torch.cuda.synchronize()
     clocks = sampler.stop()
 
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dist if world > 1 else None, dev)
     ms_per_step = total_ms / K
-    value = alg * world / (ms_per_step / 1e3) / 1e9
+    value = throughput(alg, world, ms_per_step)
 
     # End to end through the public API with host buffers: every step copies
     # all inputs from pinned host memory and reads the output back.
@@ -380,10 +394,7 @@ def run_ours(args):
     eb.record(stream)
     torch.cuda.synchronize()
     e2e_ms = ea.elapsed_time(eb) / E
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dist if world > 1 else None, dev)
 
     draft = draft_extend_timing(va, w, stream, torch, min(K, 200))
 
@@ -403,7 +414,7 @@ def run_ours(args):
                      "peak_source": f"{peak_src} (HBM copy bandwidth)",
                      "traffic": recorded_traffic(args.workload),
                      "bytes_per_launch": alg},
-        "e2e": {"value": round(alg * world / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+        "e2e": {"value": round(throughput(alg, world, e2e_ms), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": 2 * K,
