@@ -195,6 +195,30 @@ def test_out_of_range_page_ids_do_not_fault():
     run_gpu(wg)
 
 
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3", "bf16"])
+def test_more_items_than_threads(kv_dtype):
+    """1000 (sequence, KV head) items: more than one per thread of a CTA, so
+    the work scan takes its two-pass path."""
+    g = torch.Generator().manual_seed(77)
+    B = 500
+    q_lens = torch.randint(1, 5, (B,), generator=g).tolist()
+    kv_lens = torch.randint(1, 400, (B,), generator=g).tolist()
+    w = make_workload(q_lens, kv_lens, 8, 2, kv_dtype, seed=78)
+    assert w.num_seqs * w.num_kv_heads > 416
+    seqs = sorted(set(range(0, B, 37)) | {int(np.argmax(kv_lens)), int(np.argmin(kv_lens))})
+    check_against_oracle(w, seqs)
+
+
+def test_one_sequence_of_a_million_keys():
+    """A single work item split over every SM: the merge combines one segment
+    per CTA; the block table is 62,500 pages wide."""
+    w = make_workload([4], [1_000_000], 16, 1, "fp8_e4m3", seed=79, value_device="cuda")
+    wg = w.to("cuda")
+    got = run_gpu(wg)
+    ref = oracle_from_torch(wg.to("cpu"))
+    compare(got, ref)
+
+
 def test_no_bounded_wait_timed_out():
     """The tensor-core kernel bounds every wait; a timeout sets a status bit in
     the workspace. None may be set on a normal run."""
