@@ -1,45 +1,52 @@
 // Split-KV main kernel on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
-// One CTA per SM takes an equal share of the batch's 64-key tiles, and for
-// every (sequence, KV head) in its share packs all G query heads x L draft
-// tokens (<= 64 rows) into one MMA tile, so each KV page is read from HBM once
-// per KV head (sglang PR 30105 digest, "Implementation breakdown" item 2;
-// sglang PR 34517 digest, "Motivation": one KV load shared by the heads of a
-// group).
+// One CTA per SM takes an equal share of the batch's key tiles (128 keys for
+// an FP8 cache, 64 for BF16; each (sequence, KV head) item is also charged a
+// start-up cost in the split), and for every item in its share packs all G
+// query heads x L draft tokens (<= 64 rows) into one MMA tile, so each KV page
+// is read from HBM once per KV head (sglang PR 30105 digest, "Implementation
+// breakdown" item 2; sglang PR 34517 digest, "Motivation": one KV load shared
+// by the heads of a group).
 //
 // KV pages are TMA-loaded as 128-byte-swizzled boxes (16 tokens x 128 bytes
-// of one KV head) into a 128 KB ring and fed to the tensor cores as they are.
+// of one KV head) into separate K and V rings of 32 KB tiles and fed to the
+// tensor cores as they are.
 //  * FP8 E4M3 cache, kind::f8f6f4. Q (bf16) is scaled per row by an exact
 //    power of two 2^e and split into two e4m3 terms, Qh = e4m3(Q 2^e) and
 //    Ql = e4m3(Q 2^e - Qh); P is split the same way. The two terms are
 //    stacked in one M=128 MMA: packed row 16q + i uses A rows 32q + i (hi)
 //    and 32q + 16 + i (lo), so the hi and lo results land in lanes i and
 //    16 + i of the same TMEM lane quadrant and one lane shuffle adds them.
+//    P is written back into TMEM over its S tile, and P V reads its A operand
+//    there; the smem this saves buys a third K and V ring slot (3 + 3).
 //    K and V are never dequantised.
-//  * BF16 cache, kind::f16, M=64 (packed row 16q + i in lane 32q + i).
+//  * BF16 cache, kind::f16, M=64 (packed row 16q + i in lane 32q + i); P goes
+//    through four smem buffers; rings 3 K + 2 V.
 // V is the MN-major B operand of O += P V. The k/v descales fold into the
 // logit scale and the output scale.
 //
 // Roles (416 threads):
-//  warps 0,2,3 TMA producers: warp 0 streams K tiles into a K ring (freed
+//  warps 0,2,3 TMA producers: warp 0 streams K tiles into the K ring (freed
 //              once Q K^T has read them), warps 2 and 3 alternate on V tiles
 //              (V ring, freed after P V). Block-table walk with 32 page ids
-//              per lane load; one 2 KB box per lane.
-//  warp 1      TMEM owner; one thread issues Q K^T into four S buffers.
-//  warp 12     one thread issues P V into O (P has four smem buffers).
+//              per lane load, read before waiting for the ring slot; one
+//              2 KB box per lane.
+//  warp 1      TMEM owner; one thread issues Q K^T into the S buffers.
+//  warp 12     one thread issues P V into O.
 //  warps 4-11  softmax, two warps per TMEM lane quadrant q = w % 4 (both on
-//              the same SMSP). Warp half kh = (w - 4) / 4 takes keys
-//              [32 kh, 32 kh + 32) of each tile and O columns
-//              [128 kh, 128 kh + 128); lane bit 4 splits those again, so a
-//              thread owns 16 keys of one packed row. The two warps of a
-//              quadrant combine row maxima and sums through shared memory
-//              around a per-quadrant named barrier.
+//              the same SMSP). Warp half kh = (w - 4) / 4 takes half of each
+//              tile's keys and O columns [128 kh, 128 kh + 128); lane bit 4
+//              splits those again. The two warps of a quadrant combine row
+//              maxima and sums through shared memory around a per-quadrant
+//              named barrier. They also stage Q (the next item's during the
+//              current item's last tile) and write the epilogue.
 // Online softmax in log2 units keeps a per-row reference m_ref and computes
 // P = 2^(s - m_ref + 6) <= 2^8.5; m_ref moves (and O, l are rescaled in
 // TMEM) only when a tile's max exceeds it by more than 2.5, so rescales are
-// rare. Waits are bounded in time and warp-uniform: on a timeout the kernel
-// sets the workspace status word, stops issuing work, drains and frees its
-// TMEM.
+// rare. The VAR instantiation adds the generic attention's variants (sliding
+// window, logit soft cap, sinks). Waits are bounded in time and warp-uniform:
+// on a timeout the kernel sets the workspace status word, stops issuing
+// work, drains and frees its TMEM.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -83,7 +90,8 @@ struct Cfg {
   static constexpr int kM = FP8 ? 128 : 64;                // MMA rows
   static constexpr int kQRegion = kM * 128;                // one 128-byte d chunk of Q
   static constexpr int kPRowBytes = kT * kEsize;           // 128 bytes
-  static constexpr int kPSbo = 8 * kPRowBytes;             // 8-row group stride, no swizzle
+  static constexpr int kPSbo = 8 * kPRowBytes;             // 8-row group stride, no swizzle (smem P)
+  static_assert(kPSbo % 128 == 0, "P core-matrix group stride");
   static constexpr int kPBuf = kM * kPRowBytes;            // 16 KB (fp8) / 8 KB (bf16)
   static constexpr int kQkSteps = 4 * kChunks;             // K-steps of 32 bytes over d
   static constexpr int kPvSteps = kT * kEsize / 32;        // K-steps of 32 bytes over keys
