@@ -675,7 +675,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (VAR) {
             if (p.softcap_log2 > 0.f) {
               // soft cap in log2 units, c tanh(x / c), before masking, with
-              // tanh(y) = 1 - 2 / (1 + e^(2y)) (ends at -1 and 1 without overflow)
+              // tanh(y) = 1 - 2 / (1 + e^(2y)) (ends at -1 and 1 without
+              // overflow). A Taylor polynomial for small |y| measured no
+              // faster: the extra instructions per key, not the special-
+              // function unit, bound this path.
               const float c = p.softcap_log2;
               const float k2 = 2.f * kLog2e / c;
 #pragma unroll

@@ -127,3 +127,35 @@ def test_options_are_validated():
     for kw in bad:
         with pytest.raises(va.VerifyAttnError):
             run_opt(w, **kw)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_shapes_and_variants(seed):
+    """Seeded random batches: ragged lengths (including 0, 1 and page/tile
+    edges), query lengths 1-4, head groupings, both KV types, random variant
+    settings and forced split counts."""
+    g = torch.Generator().manual_seed(1000 + seed)
+    B = int(torch.randint(1, 9, (1,), generator=g))
+    hkv = [1, 2, 4][int(torch.randint(0, 3, (1,), generator=g))]
+    group = [1, 2, 4, 8, 16][int(torch.randint(0, 5, (1,), generator=g))]
+    qmax = min(4, 64 // group)
+    q_lens = torch.randint(1, qmax + 1, (B,), generator=g).tolist()
+    choices = [0, 1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 500, 1000, 2500]
+    kv_lens = [choices[int(i)] for i in torch.randint(0, len(choices), (B,), generator=g)]
+    dt = ["fp8_e4m3", "bf16"][seed % 2]
+    kd = float(torch.rand(1, generator=g) * 1.5 + 0.5) if dt == "fp8_e4m3" else None
+    w = make_workload(q_lens, kv_lens, group * hkv, hkv, dt, seed=2000 + seed, k_descale=kd,
+                      v_descale=kd).to("cuda")
+    kw = {}
+    if seed % 3 == 0:
+        kw["window_left"] = int(torch.randint(0, 300, (1,), generator=g))
+    if seed % 4 == 1:
+        kw["softcap"] = float(torch.rand(1, generator=g) * 40 + 2)
+    if seed % 2 == 1:
+        kw["sinks"] = (torch.rand(group * hkv, generator=g) * 6 - 3).to("cuda")
+    splits = [0, 1, 3, 200][seed % 4]
+    n = va.workspace_size(w.q, w.k_cache, w.seqused_k, w.max_seqlen_q, w.max_seqlen_k, splits)
+    ws = torch.zeros(n + 256, dtype=torch.uint8, device="cuda")
+    got = run_opt(w, workspace=ws, num_splits=splits, **kw)
+    compare(got, oracle(w, **kw))
+    assert va.workspace_status(ws) == 0
