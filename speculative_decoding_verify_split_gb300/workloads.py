@@ -306,3 +306,174 @@ def workload_sizes(name: str, seed: int = 0) -> dict:
     return dict(num_seqs=len(st["q_lens"]), q_lens=st["q_lens"], kv_lens=st["kv_lens"],
                 Hq=st["Hq"], Hkv=st["Hkv"], kv_dtype=st["kv_dtype"], kv_bytes=kv,
                 algorithmic_bytes=kv + qo)
+
+
+# ----------------------------------------------------------------------------
+# Absorbed-MLA latent-cache workloads (sglang PR 34517 digest, "Implementation
+# breakdown" item 1: one TP-local KV head that is the MLA latent, NOPE_DIM
+# latent columns plus PE_DIM = 64 RoPE columns). Same recipe as above: one
+# CPU generator draws q_lens, kv_lens, the page permutation and descales; a
+# value generator seeded with seed + 1 draws Q then the cache rows, N(0, 1)
+# rounded to bf16 (then cast to e4m3 for an FP8 cache). The latent width is
+# not on the pages: 512, as in the DeepSeek-V3 / Kimi-K2 MLA family. The
+# default softmax scale is that family's, 1 / sqrt(128 + 64) (the query-key
+# head width before absorption).
+# ----------------------------------------------------------------------------
+
+MLA_NOPE_DIM = 512
+MLA_PE_DIM = 64
+
+
+@dataclass
+class MlaWorkload:
+    """One batch of verify-attention inputs over a latent cache."""
+
+    name: str
+    q: torch.Tensor                 # [total_q, Hq, NOPE + PE] bf16: [q_nope | q_pe]
+    kv_cache: torch.Tensor          # [num_blocks, 16, 1, NOPE + PE]: [latent | rope key]
+    block_table: torch.Tensor       # [B, W] int32
+    cu_seqlens_q: torch.Tensor      # [B + 1] int32
+    seqused_k: torch.Tensor         # [B] int32
+    max_seqlen_q: int
+    max_seqlen_k: int
+    softmax_scale: float
+    k_descale: Optional[torch.Tensor]
+    v_descale: Optional[torch.Tensor]
+    q_lens: list = field(default_factory=list)
+    kv_lens: list = field(default_factory=list)
+    poison_page: int = -1
+    nope_dim: int = MLA_NOPE_DIM
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.q_lens)
+
+    @property
+    def num_q_heads(self) -> int:
+        return int(self.q.shape[1])
+
+    @property
+    def kv_dtype(self) -> str:
+        return FP8 if self.kv_cache.dtype == torch.float8_e4m3fn else BF16
+
+    def algorithmic_bytes(self) -> int:
+        """Each cache row read once (its latent serves as K and V), plus Q
+        read and out (NOPE_DIM wide) written."""
+        e = 1 if self.kv_dtype == FP8 else 2
+        dq = int(self.q.shape[2])
+        tq = int(self.q.shape[0])
+        return sum(self.kv_lens) * dq * e + tq * self.num_q_heads * (dq + self.nope_dim) * 2
+
+    def algorithmic_flops(self) -> int:
+        dq = int(self.q.shape[2])
+        tot = 0
+        for L, S in zip(self.q_lens, self.kv_lens):
+            for t in range(L):
+                tot += max(0, min(S, S - L + t + 1))
+        return 2 * (dq + self.nope_dim) * self.num_q_heads * tot
+
+    def to(self, device) -> "MlaWorkload":
+        def mv(x):
+            return None if x is None else x.to(device)
+        return MlaWorkload(self.name, mv(self.q), mv(self.kv_cache), mv(self.block_table),
+                           mv(self.cu_seqlens_q), mv(self.seqused_k), self.max_seqlen_q,
+                           self.max_seqlen_k, self.softmax_scale, mv(self.k_descale),
+                           mv(self.v_descale), list(self.q_lens), list(self.kv_lens),
+                           self.poison_page, self.nope_dim)
+
+
+def make_mla_workload(
+    q_lens: Sequence[int],
+    kv_lens: Sequence[int],
+    num_q_heads: int,
+    kv_dtype: str = FP8,
+    *,
+    seed: int = 0,
+    permute: bool = True,
+    poison: bool = True,
+    k_descale: Optional[float] = None,
+    v_descale: Optional[float] = None,
+    softmax_scale: Optional[float] = None,
+    max_seqlen_k: Optional[int] = None,
+    value_device: str = "cpu",
+    name: str = "custom_mla",
+    nope_dim: int = MLA_NOPE_DIM,
+    pe_dim: int = MLA_PE_DIM,
+    _gen: Optional[torch.Generator] = None,
+) -> MlaWorkload:
+    """Builds a latent-cache workload with explicit per-sequence lengths."""
+    q_lens = [int(x) for x in q_lens]
+    kv_lens = [int(x) for x in kv_lens]
+    B = len(q_lens)
+    g = _gen if _gen is not None else torch.Generator().manual_seed(seed)
+    pages_per_seq = [math.ceil(s / PAGE_SIZE) for s in kv_lens]
+    n_used = sum(pages_per_seq)
+    perm = torch.randperm(n_used, generator=g) if permute else torch.arange(n_used)
+    if k_descale == "uniform":
+        k_descale = float(torch.rand(1, generator=g) * 1.5 + 0.5)
+        v_descale = float(torch.rand(1, generator=g) * 1.5 + 0.5)
+    W = max([1] + pages_per_seq)
+    poison_page = n_used
+    num_blocks = n_used + 1
+    block_table = torch.full((B, W), poison_page, dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(pages_per_seq):
+        block_table[b, :n] = perm[off:off + n].to(torch.int32)
+        off += n
+    cu = torch.zeros(B + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(q_lens, dtype=torch.int64), 0).to(torch.int32)
+    total_q = int(cu[-1])
+    D = nope_dim + pe_dim
+    gv = torch.Generator(device=value_device).manual_seed(seed + 1)
+    q = _randn(total_q * num_q_heads * D, gv, value_device).view(total_q, num_q_heads, D)
+    kv = _randn(num_blocks * PAGE_SIZE * D, gv, value_device).view(num_blocks, PAGE_SIZE, 1, D)
+    if kv_dtype == FP8:
+        kv = kv.to(torch.float8_e4m3fn)
+        bits, pv = torch.uint8, _POISON_FP8
+    elif kv_dtype == BF16:
+        bits, pv = torch.int16, _POISON_BF16
+    else:
+        raise ValueError(f"unknown kv dtype {kv_dtype}")
+    kv.view(bits)[poison_page].fill_(pv)
+    if poison:
+        for b in range(B):
+            S, n = kv_lens[b], pages_per_seq[b]
+            tail = S - (n - 1) * PAGE_SIZE
+            if n > 0 and tail < PAGE_SIZE:
+                kv.view(bits)[int(block_table[b, n - 1]), tail:].fill_(pv)
+    kd = None if k_descale is None else torch.tensor([k_descale], dtype=torch.float32)
+    vd = None if v_descale is None else torch.tensor([v_descale], dtype=torch.float32)
+    msk = max_seqlen_k if max_seqlen_k is not None else max([0] + kv_lens)
+    scale = softmax_scale if softmax_scale is not None else (128 + 64) ** -0.5
+    return MlaWorkload(name, q, kv, block_table, cu, torch.tensor(kv_lens, dtype=torch.int32),
+                       max([0] + q_lens), msk, scale, kd, vd, q_lens, kv_lens, poison_page,
+                       nope_dim)
+
+
+MLA_WORKLOADS = (
+    "mla_tiny",                # 2 seqs, q [4,2], kv [1024,769], 16 heads, fp8 latent
+    "mla_mid_context_fp8",     # 64 seqs, q 3, kv U[8192,32768], 16 heads, descale U[0.5,2]
+    "mla_long_context_fp8",    # 16 seqs, q 4, kv U[65536,131072], 16 heads, fp8 latent
+)
+
+
+def mla_workload_structure(name: str, seed: int = 0) -> dict:
+    """q_lens, kv_lens, heads and descales of a named latent-cache workload
+    (the shapes of the GQA workloads of the same names, on a latent cache)."""
+    g = torch.Generator().manual_seed(seed)
+    if name == "mla_tiny":
+        return dict(q_lens=[4, 2], kv_lens=[1024, 769], Hq=16, gen=g, descale=None)
+    if name == "mla_mid_context_fp8":
+        return dict(q_lens=[3] * 64, kv_lens=torch.randint(8192, 32769, (64,), generator=g).tolist(),
+                    Hq=16, gen=g, descale="uniform")
+    if name == "mla_long_context_fp8":
+        return dict(q_lens=[4] * 16, kv_lens=torch.randint(65536, 131073, (16,), generator=g).tolist(),
+                    Hq=16, gen=g, descale=None)
+    raise KeyError(f"unknown workload {name!r}; known: {MLA_WORKLOADS}")
+
+
+def named_mla_workload(name: str, seed: int = 0, value_device: str = "cpu") -> MlaWorkload:
+    st = mla_workload_structure(name, seed)
+    return make_mla_workload(st["q_lens"], st["kv_lens"], st["Hq"], FP8, seed=seed,
+                             k_descale=st["descale"], value_device=value_device, name=name,
+                             _gen=st["gen"])
