@@ -308,6 +308,59 @@ va_status verify_attn_block_table_from_indptr(const va_tensor* kv_indptr,
                                               va_tensor* seqused_k, int32_t pad_page,
                                               int32_t* status, void* stream);
 
+/*
+ * verify_attn_mla - target-verify attention over an absorbed-MLA latent cache.
+ *
+ * The grouped-head shared-KV verify kernel of the sglang PR 34517 digest
+ * ("Implementation breakdown" item 1, the verify_mla.py excerpt) also serves
+ * an absorbed-MLA layout: the single TP-local KV head is the MLA latent,
+ * NOPE_DIM latent columns plus PE_DIM = 64 RoPE columns, and the logits are
+ * (q_nope . k_nope + q_pe . k_pe) * softmax_scale * k_scale. The values are
+ * the latent columns of the same cache rows. The latent width is not on the
+ * pages; this library takes NOPE_DIM = 512 (the DeepSeek-V3 / Kimi-K2 MLA
+ * family). For sequence b (L draft tokens, S = seqused_k[b]) and query head h
+ * of draft token t, with cache row j = [c_j | r_j] (decoded e4m3):
+ *
+ *   out[cu[b]+t, h, :] = sum_j softmax_j(softmax_scale * k_descale *
+ *                          (q[.., :512] . c_j + q[.., 512:] . r_j)) * v_descale * c_j
+ *
+ * over keys j in [0, S - L + t]; a row that sees no key is 0.
+ *
+ * Arguments (device memory unless stated):
+ *  q            [total_q, Hq, 576] bf16: [q_nope (absorbed, 512) | q_pe (64)].
+ *  kv_cache     [num_blocks, 16, 1, 576] FP8 E4M3 (OCP FN): [latent | rope key].
+ *  block_table, cu_seqlens_q, seqused_k, max_seqlen_q, max_seqlen_k,
+ *  softmax_scale, k_descale, v_descale: as for verify_attn (Hkv = 1, so the
+ *               group is Hq and Hq * max_seqlen_q <= 64). A cache with one
+ *               scale passes it as both descales.
+ *  out          [total_q, Hq, 512] bf16, written.
+ *  workspace    device memory of at least verify_attn_mla_workspace_size()
+ *               bytes, 256-byte aligned; NULL uses the library's per-device
+ *               workspace (grown with cudaMalloc as needed).
+ *  num_splits   0 = the library's choice (one CTA per SM, fewer for small
+ *               batches); > 0 forces that many CTAs.
+ *
+ * Layout: innermost strides 1 and every other stride a multiple of 16 bytes;
+ * q, out, kv_cache 16-byte aligned.
+ * Errors (before any launch): VA_ERR_NULL, VA_ERR_SHAPE, VA_ERR_DTYPE,
+ * VA_ERR_LAYOUT as for verify_attn; VA_ERR_UNSUPPORTED for a BF16 cache,
+ * more than one KV head, other row widths or Hq * max_seqlen_q > 64;
+ * VA_ERR_WORKSPACE for a short or misaligned workspace; VA_ERR_CUDA for a
+ * failed launch or allocation. Device-side timeouts set the workspace
+ * status word as for verify_attn_ex.
+ */
+va_status verify_attn_mla(const va_tensor* q, const va_tensor* kv_cache, const va_tensor* block_table,
+                          const va_tensor* cu_seqlens_q, const va_tensor* seqused_k,
+                          int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
+                          const va_tensor* k_descale, const va_tensor* v_descale, va_tensor* out,
+                          void* workspace, size_t workspace_bytes, int32_t num_splits,
+                          void* stream);
+
+/* Workspace bytes verify_attn_mla needs for these shapes on the current
+ * device (0 if they are unsupported). */
+size_t verify_attn_mla_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_seqlen_q,
+                                      int32_t max_seqlen_k, int32_t num_splits);
+
 /* Static, NUL-terminated name of a status code. */
 const char* verify_attn_status_string(int32_t status);
 

@@ -29,7 +29,11 @@ _DTYPES = {torch.bfloat16: VA_BF16, torch.float8_e4m3fn: VA_FP8_E4M3,
 # Every symbol include/verify_attn.h declares.
 EXPORTS = ("verify_attn", "verify_attn_ex", "verify_attn_check", "verify_attn_plan",
            "verify_attn_workspace_size", "verify_attn_status_string", "verify_attn_noalloc",
-           "verify_attn_block_table_from_indptr", "verify_attn_opt")
+           "verify_attn_block_table_from_indptr", "verify_attn_opt", "verify_attn_mla",
+           "verify_attn_mla_workspace_size")
+
+# Absorbed-MLA latent cache: row = [latent (MLA_NOPE) | rope key (MLA_PE)].
+MLA_NOPE, MLA_PE = 512, 64
 
 # Status bits of verify_attn_block_table_from_indptr.
 BT_BAD_PAGE, BT_TRUNCATED, BT_BAD_INDPTR = 1, 2, 4
@@ -95,6 +99,12 @@ def _lib():
                                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32,
                                                ctypes.c_void_p]
         lib.verify_attn_opt.restype = ctypes.c_int32
+        lib.verify_attn_mla.argtypes = [P] * 5 + [ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                                  P, P, P, ctypes.c_void_p, ctypes.c_size_t,
+                                                  ctypes.c_int32, ctypes.c_void_p]
+        lib.verify_attn_mla.restype = ctypes.c_int32
+        lib.verify_attn_mla_workspace_size.argtypes = [ctypes.c_int32] * 5
+        lib.verify_attn_mla_workspace_size.restype = ctypes.c_size_t
         lib.verify_attn_status_string.argtypes = [ctypes.c_int32]
         lib.verify_attn_status_string.restype = ctypes.c_char_p
         _LIB = lib
@@ -340,3 +350,50 @@ def draft_extend_attn(q, k_cache, v_cache, kv_indptr, kv_indices, cu_seqlens_q,
     return verify_attn_opt(q, k_cache, v_cache, bt, cu_seqlens_q, sk, max_seqlen_q,
                            int(width) * 16, softmax_scale, k_descale, v_descale, out=out,
                            window_left=window_left, softcap=softcap, sinks=sinks, stream=stream)
+
+
+def verify_attn_mla(q, kv_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q: int,
+                    max_seqlen_k: int, softmax_scale: float, k_descale=None, v_descale=None,
+                    out=None, workspace: Optional[torch.Tensor] = None, num_splits: int = 0,
+                    stream=None):
+    """Target-verify attention over an absorbed-MLA latent cache (see
+    include/verify_attn.h): q [total_q, Hq, 576] bf16, kv_cache
+    [num_blocks, 16, 1, 576] e4m3, out [total_q, Hq, 512] bf16. ``workspace``
+    None uses the library's own."""
+    if out is None:
+        out = torch.empty(q.shape[0], q.shape[1], MLA_NOPE, dtype=torch.bfloat16, device=q.device)
+    ds = [desc(x) for x in (q, kv_cache, block_table, cu_seqlens_q, seqused_k, k_descale,
+                            v_descale, out)]
+    r = [_ref(d) for d in ds]
+    if workspace is None:
+        addr, nbytes = 0, 0
+    else:
+        a = workspace.data_ptr()
+        off = (-a) % 256
+        addr, nbytes = a + off, workspace.numel() - off
+    with torch.cuda.device(q.device):
+        s = _lib().verify_attn_mla(r[0], r[1], r[2], r[3], r[4], int(max_seqlen_q),
+                                   int(max_seqlen_k), float(softmax_scale), r[5], r[6], r[7],
+                                   ctypes.c_void_p(addr), nbytes, int(num_splits),
+                                   ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if s != VA_OK:
+        raise VerifyAttnError(s, "verify_attn_mla")
+    return out
+
+
+def mla_workspace_size(q, seqused_k, max_seqlen_q, max_seqlen_k, num_splits=0) -> int:
+    with torch.cuda.device(q.device):
+        n = _lib().verify_attn_mla_workspace_size(int(seqused_k.shape[0]), int(q.shape[1]),
+                                                  int(max_seqlen_q), int(max_seqlen_k),
+                                                  int(num_splits))
+    if n == 0:
+        raise VerifyAttnError(4, "verify_attn_mla_workspace_size")
+    return int(n)
+
+
+def run_mla_workload(w, out=None, workspace=None, num_splits=0, stream=None):
+    """verify_attn_mla on a ``workloads.MlaWorkload`` whose tensors are on the GPU."""
+    return verify_attn_mla(w.q, w.kv_cache, w.block_table, w.cu_seqlens_q, w.seqused_k,
+                           w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale, w.k_descale,
+                           w.v_descale, out=out, workspace=workspace, num_splits=num_splits,
+                           stream=stream)

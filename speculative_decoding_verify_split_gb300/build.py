@@ -22,7 +22,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libverify_attn.so")
 
-SOURCES = ["va_host.cpp", "va_main_tc.cu", "va_merge.cu", "va_noalloc.cu", "va_pagetable.cu"]
+SOURCES = ["va_host.cpp", "va_main_tc.cu", "va_mla_tc.cu", "va_merge.cu", "va_noalloc.cu",
+           "va_pagetable.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler",

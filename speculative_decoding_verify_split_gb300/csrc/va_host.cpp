@@ -226,7 +226,7 @@ static va_status device_state(DeviceState** out) {
   if (!st.ready) {
     if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return VA_ERR_CUDA;
-    if (prepare_main_tc() != cudaSuccess) return VA_ERR_CUDA;
+    if (prepare_main_tc() != cudaSuccess || prepare_mla_tc() != cudaSuccess) return VA_ERR_CUDA;
     st.ready = true;
   }
   *out = &st;
@@ -297,6 +297,7 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
   p.max_rows = plan.max_rows;
   p.num_work = plan.num_work;
   p.piece_cost = kPieceCostTiles;
+  p.dv = kHeadDim;
   const WorkspaceLayout lay = workspace_layout(plan.num_work, plan.num_splits, plan.max_rows);
   char* base = static_cast<char*>(ws);
   p.ws_meta = reinterpret_cast<int32_t*>(base + lay.meta_off);
@@ -312,6 +313,155 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
   }
   if (launch_main_tc(p, tm_k, tm_v, stream) != cudaSuccess) return VA_ERR_CUDA;
   if (ev_mid && cudaEventRecord(ev_mid, stream) != cudaSuccess) return VA_ERR_CUDA;
+  if (launch_merge(p, stream) != cudaSuccess) return VA_ERR_CUDA;
+  return VA_OK;
+}
+
+// ---- absorbed-MLA latent cache ------------------------------------------------
+
+va_status validate_mla(const va_tensor* q, const va_tensor* kv, const va_tensor* bt,
+                       const va_tensor* cu, const va_tensor* su, int32_t max_seqlen_q,
+                       int32_t max_seqlen_k, const va_tensor* kd, const va_tensor* vd,
+                       const va_tensor* out, Shapes* sh) {
+  if (!q || !kv || !bt || !cu || !su || !out) return VA_ERR_NULL;
+  if (!dims_ok(q, 3) || !dims_ok(kv, 4) || !dims_ok(bt, 2) || !dims_ok(cu, 1) || !dims_ok(su, 1) ||
+      !dims_ok(out, 3))
+    return VA_ERR_SHAPE;
+  if (q->dtype != VA_BF16 || out->dtype != VA_BF16) return VA_ERR_DTYPE;
+  if (kv->dtype != VA_FP8_E4M3 && kv->dtype != VA_BF16) return VA_ERR_DTYPE;
+  if (bt->dtype != VA_INT32 || cu->dtype != VA_INT32 || su->dtype != VA_INT32) return VA_ERR_DTYPE;
+  // one latent KV head (the digest's k_extend.shape[1] != 1 rejection), rows
+  // [latent | rope], an FP8 cache (the only one this kernel reads)
+  if (kv->dtype != VA_FP8_E4M3) return VA_ERR_UNSUPPORTED;
+  if (kv->shape[1] != kPageSize || kv->shape[2] != 1 || kv->shape[3] != kMlaRow) return VA_ERR_UNSUPPORTED;
+  if (q->shape[2] != kMlaRow || out->shape[2] != kMlaNope) return VA_ERR_UNSUPPORTED;
+  if (out->shape[0] != q->shape[0] || out->shape[1] != q->shape[1]) return VA_ERR_SHAPE;
+  const int64_t hq = q->shape[1];
+  if (hq < 1) return VA_ERR_SHAPE;
+  const int64_t B = su->shape[0];
+  if (cu->shape[0] != B + 1 || bt->shape[0] != B) return VA_ERR_SHAPE;
+  if (max_seqlen_q < 1 || max_seqlen_k < 0) return VA_ERR_UNSUPPORTED;
+  if (hq * (int64_t)max_seqlen_q > kMaxRows) return VA_ERR_UNSUPPORTED;
+  if (B > 0 && bt->shape[1] * kPageSize < (int64_t)max_seqlen_k) return VA_ERR_SHAPE;
+  if (q->shape[0] > INT32_MAX || kv->shape[0] > INT32_MAX || B > INT32_MAX / 2 ||
+      bt->shape[1] > INT32_MAX / kPageSize)
+    return VA_ERR_UNSUPPORTED;
+  if (!rows_16b(q) || !rows_16b(out) || !rows_16b(kv)) return VA_ERR_LAYOUT;
+  if (cu->stride[0] != 1 || su->stride[0] != 1) return VA_ERR_LAYOUT;
+  if (numel(q) > 0 && (!q->data || !out->data)) return VA_ERR_NULL;
+  if (numel(kv) > 0 && !kv->data) return VA_ERR_NULL;
+  if (!cu->data) return VA_ERR_NULL;
+  if (B > 0 && !su->data) return VA_ERR_NULL;
+  if (numel(bt) > 0 && !bt->data) return VA_ERR_NULL;
+  if ((q->data && !aligned16(q->data)) || (out->data && !aligned16(out->data)) ||
+      (kv->data && !aligned16(kv->data)))
+    return VA_ERR_LAYOUT;
+  va_status s = check_descale(kd);
+  if (s != VA_OK) return s;
+  s = check_descale(vd);
+  if (s != VA_OK) return s;
+  sh->total_q = q->shape[0];
+  sh->hq = hq;
+  sh->hkv = 1;
+  sh->num_blocks = kv->shape[0];
+  sh->num_seqs = B;
+  sh->width = bt->shape[1];
+  sh->kv_dtype = kv->dtype;
+  return VA_OK;
+}
+
+// The split heuristic of make_plan on 64-key latent tiles, value width 512.
+va_status make_mla_plan(int64_t B, int64_t hq, int32_t max_q, int32_t max_k, int32_t num_sms,
+                        int32_t force, va_plan* plan) {
+  if (!plan) return VA_ERR_NULL;
+  if (B < 0 || hq < 1 || max_q < 1 || max_k < 0 || num_sms < 1) return VA_ERR_UNSUPPORTED;
+  if (hq * max_q > kMaxRows) return VA_ERR_UNSUPPORTED;
+  const int64_t item_tiles = ((int64_t)max_k + kMlaTileKeys - 1) / kMlaTileKeys;
+  const int64_t tiles_bound = B * item_tiles;
+  if (tiles_bound + B * kMlaPieceCostTiles > INT32_MAX / 2) return VA_ERR_UNSUPPORTED;
+  int64_t splits = force > 0 ? force : num_sms;
+  if (splits > tiles_bound) splits = tiles_bound;
+  if (splits < 1) splits = 1;
+  std::memset(plan, 0, sizeof(*plan));
+  plan->tile_keys = kMlaTileKeys;
+  plan->num_splits = (int32_t)splits;
+  plan->max_rows = (int32_t)(hq * max_q);
+  plan->num_work = (int32_t)B;
+  plan->kernel = kKernelTc;
+  plan->workspace_bytes = (int64_t)workspace_layout(B, splits, hq * max_q, kMlaNope).total;
+  return VA_OK;
+}
+
+// 4-D map over a latent cache [num_blocks, 16, 1, 576] (e4m3): box = one page,
+// 128 bytes of the row, 128-byte swizzle. The box at column 512 holds the
+// 64 rope bytes; its other 64 lie past the row end and are zero-filled.
+static bool make_mla_map(CUtensorMap* m, const va_tensor* t, int64_t nb) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)kMlaRow, 1, (cuuint64_t)kPageSize, (cuuint64_t)nb};
+  cuuint64_t strides[3] = {(cuuint64_t)t->stride[2], (cuuint64_t)t->stride[1], (cuuint64_t)t->stride[0]};
+  if (strides[0] == 0 || strides[0] % 16 != 0) strides[0] = (cuuint64_t)kMlaRow;  // one head: unused
+  cuuint32_t box[4] = {128, 1, (cuuint32_t)kPageSize, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, t->data, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+va_status launch_mla(const va_tensor* q, const va_tensor* kv, const va_tensor* bt, const va_tensor* cu,
+                     const va_tensor* su, int32_t max_q, int32_t max_k, float scale,
+                     const va_tensor* kd, const va_tensor* vd, va_tensor* out, const Shapes& sh,
+                     const va_plan& plan, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;
+  if ((size_t)plan.workspace_bytes > ws_bytes || !ws) return VA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return VA_ERR_WORKSPACE;
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const uint16_t*>(q->data);
+  p.q_s0 = q->stride[0];
+  p.q_s1 = q->stride[1];
+  p.k = p.v = kv->data;
+  p.k_s0 = p.v_s0 = kv->stride[0];
+  p.k_s1 = p.v_s1 = kv->stride[1];
+  p.k_s2 = p.v_s2 = kv->stride[2];
+  p.block_table = static_cast<const int32_t*>(bt->data);
+  p.bt_s0 = bt->stride[0];
+  p.bt_s1 = bt->stride[1];
+  p.bt_width = (int32_t)sh.width;
+  p.cu_q = static_cast<const int32_t*>(cu->data);
+  p.seqused_k = static_cast<const int32_t*>(su->data);
+  p.k_descale = kd ? static_cast<const float*>(kd->data) : nullptr;
+  p.v_descale = vd ? static_cast<const float*>(vd->data) : nullptr;
+  p.out = static_cast<uint16_t*>(out->data);
+  p.o_s0 = out->stride[0];
+  p.o_s1 = out->stride[1];
+  p.num_seqs = (int32_t)sh.num_seqs;
+  p.hq = (int32_t)sh.hq;
+  p.hkv = 1;
+  p.group = (int32_t)sh.hq;
+  p.num_blocks = (int32_t)sh.num_blocks;
+  p.total_q = (int32_t)sh.total_q;
+  p.max_seqlen_q = max_q;
+  p.max_seqlen_k = max_k;
+  p.kv_fp8 = 1;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.window_left = -1;
+  p.tile_keys = plan.tile_keys;
+  p.num_splits = plan.num_splits;
+  p.max_rows = plan.max_rows;
+  p.num_work = plan.num_work;
+  p.piece_cost = kMlaPieceCostTiles;
+  p.dv = kMlaNope;
+  const WorkspaceLayout lay = workspace_layout(plan.num_work, plan.num_splits, plan.max_rows, kMlaNope);
+  char* base = static_cast<char*>(ws);
+  p.ws_status = reinterpret_cast<int32_t*>(base + lay.status_off);
+  p.ws_meta = reinterpret_cast<int32_t*>(base + lay.meta_off);
+  p.ws_ml = reinterpret_cast<float*>(base + lay.ml_off);
+  p.ws_acc = reinterpret_cast<float*>(base + lay.acc_off);
+  CUtensorMap tm;
+  std::memset(&tm, 0, sizeof(tm));
+  if (sh.num_blocks > 0 && !make_mla_map(&tm, kv, sh.num_blocks)) return VA_ERR_LAYOUT;
+  if (launch_mla_tc(p, tm, stream) != cudaSuccess) return VA_ERR_CUDA;
   if (launch_merge(p, stream) != cudaSuccess) return VA_ERR_CUDA;
   return VA_OK;
 }
@@ -480,6 +630,61 @@ VA_EXPORT va_status verify_attn_block_table_from_indptr(const va_tensor* kv_indp
       static_cast<int32_t*>(seqused_k->data), seqused_k->stride[0], pad_page, status,
       static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+}
+
+VA_EXPORT va_status verify_attn_mla(const va_tensor* q, const va_tensor* kv_cache,
+                                    const va_tensor* block_table, const va_tensor* cu_seqlens_q,
+                                    const va_tensor* seqused_k, int32_t max_seqlen_q,
+                                    int32_t max_seqlen_k, float softmax_scale,
+                                    const va_tensor* k_descale, const va_tensor* v_descale,
+                                    va_tensor* out, void* workspace, size_t workspace_bytes,
+                                    int32_t num_splits, void* stream) {
+  Shapes sh;
+  va_status s = validate_mla(q, kv_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
+                             max_seqlen_k, k_descale, v_descale, out, &sh);
+  if (s != VA_OK) return s;
+  if (num_splits < 0) return VA_ERR_UNSUPPORTED;
+  std::unique_lock<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  s = device_state(&st);
+  if (s != VA_OK) return s;
+  va_plan plan;
+  s = make_mla_plan(sh.num_seqs, sh.hq, max_seqlen_q, max_seqlen_k, st->sms, num_splits, &plan);
+  if (s != VA_OK) return s;
+  if (!workspace) {
+    if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;
+    if ((size_t)plan.workspace_bytes > st->ws_bytes) {
+      if (st->ws) cudaFree(st->ws);
+      st->ws = nullptr;
+      st->ws_bytes = 0;
+      if (cudaMalloc(&st->ws, (size_t)plan.workspace_bytes) != cudaSuccess) {
+        st->ws = nullptr;
+        return VA_ERR_CUDA;
+      }
+      if (cudaMemset(st->ws, 0, (size_t)plan.workspace_bytes) != cudaSuccess) return VA_ERR_CUDA;
+      st->ws_bytes = (size_t)plan.workspace_bytes;
+    }
+    workspace = st->ws;
+    workspace_bytes = st->ws_bytes;
+  } else {
+    lk.unlock();
+  }
+  return launch_mla(q, kv_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q, max_seqlen_k,
+                    softmax_scale, k_descale, v_descale, out, sh, plan, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream));
+}
+
+VA_EXPORT size_t verify_attn_mla_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                                int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                                int32_t num_splits) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  if (device_state(&st) != VA_OK) return 0;
+  va_plan plan;
+  if (make_mla_plan(num_seqs, num_q_heads, max_seqlen_q, max_seqlen_k, st->sms, num_splits, &plan) !=
+      VA_OK)
+    return 0;
+  return (size_t)plan.workspace_bytes;
 }
 
 VA_EXPORT const char* verify_attn_status_string(int32_t status) {

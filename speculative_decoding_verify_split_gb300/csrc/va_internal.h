@@ -11,6 +11,13 @@
 namespace va {
 
 constexpr int kHeadDim = 256;
+// Absorbed-MLA latent cache (sglang PR 34517 digest, "Implementation breakdown"
+// item 1): one KV head whose rows are [latent (NOPE) | rope key (PE)]; the
+// latent is also the value. The latent width is not on the pages: 512, as in
+// the DeepSeek-V3 / Kimi-K2 MLA family.
+constexpr int kMlaNope = 512;
+constexpr int kMlaPe = 64;
+constexpr int kMlaRow = kMlaNope + kMlaPe;  // 576
 constexpr int kPageSize = 16;
 constexpr int kMaxRows = 64;  // G * max_seqlen_q packed rows per (sequence, KV head)
 
@@ -45,10 +52,11 @@ struct Params {
   // epilogue and pipeline refill), so a CTA that starts an item gets fewer
   // tiles.
   int32_t tile_keys, num_splits, max_rows, num_work, piece_cost;
+  int32_t dv;          // output (value) columns: kHeadDim, or kMlaNope over a latent cache
   int32_t* ws_status;  // sticky error bits (a bounded wait timed out); never cleared by kernels
   int32_t* ws_meta;  // [num_work + 1]: first tile of each work item (split units), then the total
   float* ws_ml;      // [pieces][max_rows][2]: running max (log2 units), row sum
-  float* ws_acc;     // [pieces][max_rows][256]: unnormalised output rows
+  float* ws_acc;     // [pieces][max_rows][dv]: unnormalised output rows
 };
 
 // Workspace layout. pieces = num_work + num_splits: a work item split over
@@ -60,14 +68,15 @@ struct WorkspaceLayout {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WorkspaceLayout workspace_layout(int64_t num_work, int64_t num_splits, int64_t max_rows) {
+inline WorkspaceLayout workspace_layout(int64_t num_work, int64_t num_splits, int64_t max_rows,
+                                        int64_t dv = kHeadDim) {
   WorkspaceLayout w;
   const int64_t pieces = num_work + num_splits;
   w.status_off = 0;
   w.meta_off = 256;
   w.ml_off = w.meta_off + align_up(sizeof(int32_t) * (size_t)(num_work + 1), 256);
   w.acc_off = w.ml_off + align_up(sizeof(float) * 2 * (size_t)(pieces * max_rows), 256);
-  w.total = w.acc_off + align_up(sizeof(float) * kHeadDim * (size_t)(pieces * max_rows), 256);
+  w.total = w.acc_off + align_up(sizeof(float) * (size_t)dv * (size_t)(pieces * max_rows), 256);
   return w;
 }
 
@@ -92,6 +101,11 @@ cudaError_t launch_block_table(const int32_t* indptr, const int32_t* indices, in
                                int64_t bt_s1, int32_t* seqused, int64_t sk_s0, int32_t pad,
                                int32_t* status, cudaStream_t stream);
 cudaError_t prepare_main_tc();  // once per device: opt in to its shared memory
+// Latent-cache main kernel (va_mla_tc.cu): FP8 cache, 64-key tiles.
+constexpr int kMlaTileKeys = 64;
+constexpr int kMlaPieceCostTiles = 6;
+cudaError_t prepare_mla_tc();
+cudaError_t launch_mla_tc(const Params& p, const CUtensorMap& tm_kv, cudaStream_t stream);
 cudaError_t launch_main_tc(const Params& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            cudaStream_t stream);
 

@@ -51,6 +51,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include "va_fp8.cuh"
 #include "va_ptx.cuh"
 #include "va_split.cuh"
 
@@ -149,71 +150,6 @@ enum : int {
   kNumBars
 };
 static_assert(8 * kNumBars + 16 + 34 * 8 <= 1024, "barrier area");
-
-// One (sequence, KV head) item's share of this CTA. Tile indices are absolute
-// within the sequence: the item's tiles are [tb, nt), this CTA's [lt0, lt1).
-struct Piece {
-  int j, b, kvh, S, L, q0, R, nt, tb, lt0, lt1;
-  bool direct;
-};
-
-// Next (sequence, KV head) item with tiles in this CTA's split range [t0, t1);
-// ts is the split unit of item j's first tile.
-__device__ __forceinline__ bool next_piece(const Params& p, long long t0, long long t1, int& j,
-                                           long long& ts, Piece& pc) {
-  while (j < p.num_work && ts < t1) {
-    const int nt = work_tiles(p, j);
-    if (nt == 0) {
-      ++j;
-      continue;
-    }
-    pc.j = j;
-    pc.b = j / p.hkv;
-    pc.kvh = j - pc.b * p.hkv;
-    pc.S = seq_kv_len(p, pc.b);
-    pc.L = seq_q_len(p, pc.b);
-    pc.q0 = p.cu_q[pc.b];
-    pc.R = p.group * pc.L;
-    pc.tb = first_tile(p, pc.S, pc.L);
-    pc.nt = pc.tb + nt;
-    pc.lt0 = pc.tb + (int)((t0 > ts ? t0 : ts) - ts);
-    pc.lt1 = pc.tb + (int)((t1 < ts + nt ? t1 : ts + nt) - ts);
-    pc.direct = (pc.lt0 == pc.tb && pc.lt1 == pc.nt);
-    ts += work_cost(p, nt);  // the next item's first tile follows its start-up units
-    ++j;
-    return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void fail(const Params& p, volatile int* abort_flag, int code) {
-  *abort_flag = 1;
-  if (p.ws_status) atomicOr(p.ws_status, code);
-}
-
-__device__ __forceinline__ uint32_t pack_fp8x2(float lo, float hi) {
-  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
-}
-
-__device__ __forceinline__ float2 unpack_fp8x2(uint32_t v) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
-  return __half22float2(__half2(h));
-}
-
-// p (two fp32 values, a first) -> e4m3 hi and lo bytes, via f16x2.
-__device__ __forceinline__ void split_p(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(a, b);
-  const __nv_fp8x2_storage_t h8 = __nv_cvt_halfraw2_to_fp8x2(__half2_raw(h), __NV_SATFINITE, __NV_E4M3);
-  const __half2 hh = __half2(__nv_cvt_fp8x2_to_halfraw2(h8, __NV_E4M3));
-  const __half2 r = __hsub2(h, hh);
-  const __nv_fp8x2_storage_t l8 = __nv_cvt_halfraw2_to_fp8x2(__half2_raw(r), __NV_SATFINITE, __NV_E4M3);
-  hi = (uint32_t)h8;
-  lo = (uint32_t)l8;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
-}
 
 template <bool FP8>
 __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {

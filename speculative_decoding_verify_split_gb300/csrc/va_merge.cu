@@ -11,8 +11,9 @@
 // held by one CTA were written by the main kernel; items with no key tiles
 // get zero rows here.
 //
-// 64 threads per packed row, one float4 of the 256 output columns each, so a
-// row's segments are read as coalesced 1 KB lines. Segments are taken eight
+// One thread per float4 of a packed row's output columns (64 threads for the
+// 256 columns of a head, 128 for the 512 of a latent), so a row's segments
+// are read as coalesced lines. Segments are taken eight
 // at a time with all their loads in flight together, and folded into a
 // running (max, denominator, accumulator) triple: the latency of a merge is
 // one L2 round trip per eight segments. Launched as a programmatic dependent
@@ -23,13 +24,14 @@
 namespace va {
 namespace {
 
-constexpr int kRowsPerCta = 4;
-constexpr int kThreadsPerRow = kHeadDim / 4;  // 64
+constexpr int kMergeThreads = 256;
 constexpr int kSegChunk = 8;
 
-// SINKS: compiled with the attention-sink term.
-template <bool SINKS>
-__global__ void __launch_bounds__(kRowsPerCta * kThreadsPerRow, 4) va_merge_kernel(const Params p) {
+// SINKS: compiled with the attention-sink term. DV: output columns per row.
+template <bool SINKS, int DV>
+__global__ void __launch_bounds__(kMergeThreads, 4) va_merge_kernel(const Params p) {
+  constexpr int kThreadsPerRow = DV / 4;
+  constexpr int kRowsPerCta = kMergeThreads / kThreadsPerRow;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int j = blockIdx.x;
   const int r = blockIdx.y * kRowsPerCta + (int)(threadIdx.x / kThreadsPerRow);
@@ -75,7 +77,7 @@ __global__ void __launch_bounds__(kRowsPerCta * kThreadsPerRow, 4) va_merge_kern
         const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + row * 2));
         m[k] = ml.x;
         l[k] = ml.y;
-        a[k] = __ldcg(reinterpret_cast<const float4*>(p.ws_acc + row * kHeadDim) + col4);
+        a[k] = __ldcg(reinterpret_cast<const float4*>(p.ws_acc + row * DV) + col4);
       }
     }
     float mc = M;
@@ -117,9 +119,11 @@ __global__ void __launch_bounds__(kRowsPerCta * kThreadsPerRow, 4) va_merge_kern
 
 cudaError_t launch_merge(const Params& p, cudaStream_t stream) {
   if (p.num_work == 0 || p.max_rows == 0) return cudaSuccess;
+  if (p.dv != kHeadDim && p.dv != kMlaNope) return cudaErrorInvalidValue;
+  const int rows_per_cta = kMergeThreads / (p.dv / 4);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.num_work, (unsigned)((p.max_rows + kRowsPerCta - 1) / kRowsPerCta));
-  cfg.blockDim = dim3(kRowsPerCta * kThreadsPerRow);
+  cfg.gridDim = dim3((unsigned)p.num_work, (unsigned)((p.max_rows + rows_per_cta - 1) / rows_per_cta));
+  cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -127,8 +131,9 @@ cudaError_t launch_merge(const Params& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return p.sinks ? cudaLaunchKernelEx(&cfg, va_merge_kernel<true>, p)
-                 : cudaLaunchKernelEx(&cfg, va_merge_kernel<false>, p);
+  if (p.dv == kMlaNope) return cudaLaunchKernelEx(&cfg, va_merge_kernel<false, kMlaNope>, p);
+  return p.sinks ? cudaLaunchKernelEx(&cfg, va_merge_kernel<true, kHeadDim>, p)
+                 : cudaLaunchKernelEx(&cfg, va_merge_kernel<false, kHeadDim>, p);
 }
 
 }  // namespace va

@@ -1,0 +1,658 @@
+// Split-KV main kernel over an absorbed-MLA latent cache (tcgen05, sm_103a).
+//
+// The grouped-head shared-KV verify kernel of sglang PR 34517 digest
+// ("Implementation breakdown" item 1, the verify_mla.py excerpt) serves an
+// absorbed-MLA layout: one KV head whose cache rows are [latent c (512) |
+// rope key r (64)], logits (q_nope . c + q_pe . r) * sm_scale * k_scale, and
+// the latent c as the value. All Hq heads x L draft tokens (<= 64 rows) of a
+// sequence share every cache row, so each row is read from HBM once.
+//
+// The work split, the per-row online softmax in log2 units with a lazy
+// reference max, the e4m3 hi/lo split of Q and P and the bounded waits are
+// those of the GQA kernel (va_main_tc.cu). What differs is the tensor-memory
+// plan, which a 512-wide value forces. With Q and P split into two e4m3 terms
+// stacked in the MMA's M (hi rows and lo rows), O would need 128 lanes x 512
+// fp32 columns, all of TMEM. So:
+//  * S = Q K^T as before: M = 128 stacked rows (hi and lo of packed row
+//    16q + i in lanes 32q + i and 32q + 16 + i), N = 64 keys, K = 576. The
+//    latent part of Q is the A operand in TMEM (128 columns), the rope part a
+//    no-swizzle A operand in smem (8 KB); K is the cache tile.
+//  * O is kept transposed, O^T = V^T P^T: M = 128 latent columns per chunk,
+//    N = 64 packed rows, K = keys. The two e4m3 terms of P are two MMAs into
+//    the same accumulator (stacked in K, not M), so O^T takes 4 chunks x 64
+//    columns = 256 TMEM columns. V^T is the cache tile's latent part read as
+//    an MN-major A operand; P^T is a K-major B operand in smem.
+//  TMEM: O^T 0-255, two 64-column S tiles 256-383, Q latent 384-511.
+// A cache tile is 64 keys = 4 pages; a page is 5 TMA boxes of 16 rows x 128
+// bytes (four latent chunks and the rope chunk, whose box reaches past the
+// row end and is zero-filled), so a tile fills five 8 KB 128-byte-swizzled
+// regions; five ring slots (200 KB) are in flight. A slot is freed after
+// P V, since the same bytes are K and V.
+// O^T columns are rows, so a rescale of some rows touches every lane: the
+// softmax warps decide together, per tile, with one barrier reduction.
+// FP8 cache only; plain attention (no window, soft cap or sinks).
+#include "va_fp8.cuh"
+#include "va_ptx.cuh"
+#include "va_split.cuh"
+
+namespace va {
+namespace {
+
+using namespace ptx;
+
+constexpr int kT = kMlaTileKeys;               // 64 keys per tile
+constexpr int kPagesPerTile = kT / kPageSize;  // 4
+constexpr int kRegions = 5;                    // latent chunks 0-3, rope chunk 4
+constexpr int kRegion = kT * 128;              // 8 KB: 64 rows x 128 bytes, 128-byte swizzle
+constexpr int kTileBytes = kRegions * kRegion;  // 40 KB
+constexpr int kSlots = 5;
+constexpr int kProducers = 3;                  // warps 0, 2, 3 take every third tile
+// A producer's wait for a slot relies on its own previous wait (kProducers
+// tiles back) to keep that slot's empty barrier within one phase.
+static_assert(kProducers <= kSlots, "producers exceed the ring");
+constexpr int kBoxes = kPagesPerTile * kRegions;  // 20 boxes of 2 KB per tile
+static_assert(kBoxes <= 32, "one box per lane");
+constexpr int kSBufs = 2;
+constexpr int kPBufs = 2;
+constexpr int kPHalf = 64 * kT;                // one e4m3 term of P: 64 rows x 64 keys
+constexpr int kPBuf = 2 * kPHalf;              // hi then lo
+constexpr int kQpeBytes = 128 * kMlaPe;        // 128 stacked rows x 64 bytes
+constexpr int kQkSteps = kMlaNope / 32;        // 16 K-steps from the TMEM A operand
+constexpr int kQkPeSteps = kMlaPe / 32;        // 2 from the smem A operand
+constexpr int kPvSteps = kT / 32;              // 2 K-steps of 32 keys
+constexpr int kChunks = kMlaNope / 128;        // 4 O^T chunks of 128 latent columns
+
+constexpr int kOffQpe = kSlots * kTileBytes;
+constexpr int kOffP = kOffQpe + kQpeBytes;
+constexpr int kOffX = kOffP + kPBufs * kPBuf;  // [2 parity][2 kh][64 rows] floats
+constexpr int kOffBar = kOffX + 1024;
+constexpr int kSmemBytes = kOffBar + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(kTileBytes % 1024 == 0 && kOffQpe % 1024 == 0, "swizzle atoms");
+
+constexpr int kThreads = 416;  // 13 warps
+constexpr int kSoftmaxThreads = 256;
+constexpr int kBarAllSoftmax = 5;  // named barriers: 1-4 per quadrant, 5 and 6 all softmax warps
+constexpr int kBarEpilogue = 6;
+
+constexpr uint32_t kColO = 0;
+constexpr uint32_t kColS = 256;
+constexpr uint32_t kColQ = 384;
+constexpr uint32_t kTmemCols = 512;
+
+constexpr uint32_t kIdQK = instr_desc(0, 0, false, kT, 128);         // e4m3 x e4m3, N = 64 keys
+constexpr uint32_t kIdPV = instr_desc(0, 0, false, 64, 128, true);   // A = V^T MN-major, N = 64 rows
+
+constexpr float kPShift = 6.f;
+constexpr float kHeadroom = 1.f;
+constexpr float kOvershoot = 2.5f;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+enum : int {
+  kBarFull = 0,
+  kBarEmpty = kBarFull + kSlots,
+  kBarSFull = kBarEmpty + kSlots,
+  kBarSFree = kBarSFull + kSBufs,
+  kBarPFull = kBarSFree + kSBufs,
+  kBarPFree = kBarPFull + kPBufs,
+  kBarQFull = kBarPFree + kPBufs,
+  kBarQFree,
+  kBarOFull,
+  kBarOFree,
+  kBarDrain,
+  kNumBars
+};
+// barrier area: mbarriers | TMEM address, abort flag | scan scratch (34 x 8) |
+// per-row factors [2 rounds][64] floats at +512
+constexpr int kOffTmemSlot = 8 * kNumBars;
+constexpr int kOffScratch = 192;
+constexpr int kOffRowVals = 512;
+static_assert(kOffTmemSlot + 8 <= kOffScratch && kOffScratch + 34 * 8 <= kOffRowVals, "barrier area");
+
+// Four bf16 values (two words) times 2^e -> e4m3 hi and lo bytes, in order.
+__device__ __forceinline__ void split_q4(uint32_t wa, uint32_t wb, float up, uint32_t& hi, uint32_t& lo) {
+  const float x0 = __uint_as_float(wa << 16) * up, x1 = __uint_as_float(wa & 0xFFFF0000u) * up;
+  const float x2 = __uint_as_float(wb << 16) * up, x3 = __uint_as_float(wb & 0xFFFF0000u) * up;
+  const uint32_t h01 = pack_fp8x2(x0, x1), h23 = pack_fp8x2(x2, x3);
+  const float2 f01 = unpack_fp8x2(h01), f23 = unpack_fp8x2(h23);
+  hi = h01 | (h23 << 16);
+  lo = pack_fp8x2(x0 - f01.x, x1 - f01.y) | (pack_fp8x2(x2 - f23.x, x3 - f23.y) << 16);
+}
+
+__device__ __forceinline__ float bf16_amax2(uint32_t w) {
+  return fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xFFFF0000u)));
+}
+
+// Byte offset of element (row m, column k) in a no-swizzle K-major operand
+// whose rows are `row_bytes` long: 8-row x 16-byte core matrices, K-adjacent
+// ones 128 bytes apart, 8-row groups 8 * row_bytes apart.
+__device__ __forceinline__ int core_off(int m, int k, int row_bytes) {
+  return (m >> 3) * (8 * row_bytes) + (k >> 4) * 128 + (m & 7) * 16 + (k & 15);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    va_mla_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_kv) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + kOffTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffBar + kOffTmemSlot + 4);
+  long long* scratch = reinterpret_cast<long long*>(sm + kOffBar + kOffScratch);  // 32 slots
+  long long* s_ts = scratch + 32;
+  int* s_j = reinterpret_cast<int*>(scratch + 33);
+  float* xch = reinterpret_cast<float*>(sm + kOffX);
+  float* row_vals = reinterpret_cast<float*>(sm + kOffBar + kOffRowVals);  // [2][64]
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int c = blockIdx.x;
+  const uint32_t sbase = smem_addr(sm);
+  auto bar = [&](int i) { return smem_addr(&bars[i]); };
+
+  // The merge kernel is a programmatic dependent; it waits for this grid.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  long long t0, t1, ts_first = 0;
+  int j_first = 0;
+  locate_work<kThreads>(p, c, scratch, s_j, s_ts, &t0, &t1, &j_first, &ts_first);
+  if (t0 >= t1) return;
+
+  constexpr uint32_t kSwWarps = kSoftmaxThreads / 32;
+  if (tid == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(bar(kBarFull + s), 1);
+      mbar_init(bar(kBarEmpty + s), 1);
+    }
+    for (int i = 0; i < kSBufs; ++i) {
+      mbar_init(bar(kBarSFull + i), 1);
+      mbar_init(bar(kBarSFree + i), kSwWarps);
+    }
+    for (int i = 0; i < kPBufs; ++i) {
+      mbar_init(bar(kBarPFull + i), kSwWarps);
+      mbar_init(bar(kBarPFree + i), 1);
+    }
+    mbar_init(bar(kBarQFull), kSwWarps);
+    mbar_init(bar(kBarQFree), 1);
+    mbar_init(bar(kBarOFull), 1);
+    mbar_init(bar(kBarOFree), kSwWarps);
+    mbar_init(bar(kBarDrain), 2);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 2 && lane == 0 && p.num_blocks > 0) tma_prefetch_desc(&tm_kv);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 || warp == 2 || warp == 3) {
+    // ======================= TMA producers ======================================
+    const int prod = warp == 0 ? 0 : warp - 1;
+    int it = 0;
+    int j = j_first;
+    long long ts = ts_first;
+    Piece pc;
+    bool ok = true;
+    while (ok && next_piece(p, t0, t1, j, ts, pc)) {
+      const int npages = (pc.S + kPageSize - 1) / kPageSize;
+      const int* bt_row = p.block_table + (int64_t)pc.b * p.bt_s0;
+      int win = -1;
+      int my_page = -1;
+      for (int lt = pc.lt0; lt < pc.lt1 && ok; ++lt, ++it) {
+        if (it % kProducers != prod) continue;
+        const int s = it % kSlots;
+        const int pg0 = lt * kPagesPerTile;
+        if (win < 0 || pg0 + kPagesPerTile > win + 32) {
+          win = pg0;
+          const int pg = win + lane;
+          my_page = pg < npages ? bt_row[(int64_t)pg * p.bt_s1] : -1;
+          if (lane == 0 && win + 32 < npages)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(bt_row + (int64_t)(win + 32) * p.bt_s1));
+        }
+        uint32_t nvalid = 0;
+        int ids[kPagesPerTile];
+#pragma unroll
+        for (int i = 0; i < kPagesPerTile; ++i) {
+          ids[i] = __shfl_sync(0xffffffffu, my_page, pg0 + i - win);
+          const bool v = (pg0 + i) < npages && (unsigned)ids[i] < (unsigned)p.num_blocks;
+          ids[i] = v ? ids[i] : -1;
+          nvalid += v ? 1u : 0u;
+        }
+        const bool got = __all_sync(
+            0xffffffffu, mbar_wait(bar(kBarEmpty + s), ((it / kSlots) & 1) ^ 1, abort_flag, kWaitLimitNs));
+        if (!got) {
+          if (lane == 0) fail(p, abort_flag, 1);
+          ok = false;
+          break;
+        }
+        const uint32_t dst = sbase + s * kTileBytes;
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarFull + s), nvalid * (uint32_t)(kRegions * 2048));
+        __syncwarp();
+        if (lane < kBoxes) {  // lane -> (page, 128-byte column chunk)
+          const int i = lane / kRegions, ch = lane % kRegions;
+          int id = ids[0];
+#pragma unroll
+          for (int u = 1; u < kPagesPerTile; ++u)
+            if (i == u) id = ids[u];
+          if (id >= 0) tma_load_4d(dst + ch * kRegion + i * 2048, &tm_kv, ch * 128, 0, 0, id, bar(kBarFull + s));
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok) {  // let copies in flight land before the CTA goes away
+      for (int k = (it > kSlots ? it - kSlots : 0); k < it; ++k) {
+        if (k % kProducers != prod) continue;
+        mbar_wait(bar(kBarFull + k % kSlots), (k / kSlots) & 1, abort_flag, 10000000ull);
+      }
+    }
+  } else if (warp == 1 || warp == 12) {
+    // ======================= MMA issuers ==========================================
+    if (lane == 0) {
+      const bool is_qk = warp == 1;
+      const uint32_t qpe = sbase + kOffQpe;
+      int it = 0, piece_idx = 0;
+      int j = j_first;
+      long long ts = ts_first;
+      Piece pc;
+      bool ok = true;
+      auto wait_or_fail = [&](int b, uint32_t par, int code) {
+        if (!ok) return false;
+        if (!mbar_wait(bar(b), par, abort_flag, kWaitLimitNs)) {
+          fail(p, abort_flag, code);
+          ok = false;
+        }
+        return ok;
+      };
+      while (ok && next_piece(p, t0, t1, j, ts, pc)) {
+        const int first = it;
+        const int ntile = pc.lt1 - pc.lt0;
+        if (is_qk) {
+          if (!wait_or_fail(kBarQFull, piece_idx & 1, 2)) break;
+          tc_fence_after();
+          for (int i = 0; i < ntile && ok; ++i) {
+            const int cur = first + i;
+            const int s = cur % kSlots;
+            const int b = cur & (kSBufs - 1);
+            if (!wait_or_fail(kBarFull + s, (cur / kSlots) & 1, 32)) break;
+            if (cur >= kSBufs && !wait_or_fail(kBarSFree + b, ((cur - kSBufs) / kSBufs) & 1, 64)) break;
+            tc_fence_after();
+            const uint32_t kst = sbase + s * kTileBytes;
+            const uint32_t d = tmem + kColS + b * kT;
+#pragma unroll
+            for (int k = 0; k < kQkSteps; ++k) {
+              const uint64_t bdesc = smem_desc(kst + (k >> 2) * kRegion + (k & 3) * 32, 16, 1024, kLayoutSw128);
+              mma_f8f6f4_ta(d, tmem + kColQ + 8 * k, bdesc, kIdQK, k ? 1u : 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < kQkPeSteps; ++k) {
+              const uint64_t adesc = smem_desc(qpe + k * 256, 128, 8 * kMlaPe, kLayoutNone);
+              const uint64_t bdesc = smem_desc(kst + 4 * kRegion + k * 32, 16, 1024, kLayoutSw128);
+              mma_f8f6f4(d, adesc, bdesc, kIdQK, 1u);
+            }
+            mma_commit(bar(kBarSFull + b));
+            if (i == ntile - 1) mma_commit(bar(kBarQFree));
+          }
+        } else {
+          for (int i = 0; i < ntile && ok; ++i) {
+            const int x = first + i;
+            const int pb = x & (kPBufs - 1);
+            const int s = x % kSlots;
+            if (!wait_or_fail(kBarPFull + pb, (x / kPBufs) & 1, 4)) break;
+            if (!wait_or_fail(kBarFull + s, (x / kSlots) & 1, 8)) break;
+            if (i == 0 && piece_idx > 0 && !wait_or_fail(kBarOFree, (piece_idx - 1) & 1, 16)) break;
+            tc_fence_after();
+            const uint32_t kst = sbase + s * kTileBytes;
+            const uint32_t pbuf = sbase + kOffP + pb * kPBuf;
+#pragma unroll
+            for (int kk = 0; kk < kPvSteps; ++kk) {
+              const uint64_t bhi = smem_desc(pbuf + kk * 256, 128, 8 * kT, kLayoutNone);
+              const uint64_t blo = smem_desc(pbuf + kPHalf + kk * 256, 128, 8 * kT, kLayoutNone);
+#pragma unroll
+              for (int a = 0; a < kChunks; ++a) {
+                // V^T chunk a: latent columns [128 a, +128) of keys [32 kk, +32)
+                const uint64_t adesc = smem_desc(kst + a * kRegion + kk * 4096, kRegion, 1024, kLayoutSw128);
+                const uint32_t d = tmem + kColO + 64 * a;
+                mma_f8f6f4(d, adesc, bhi, kIdPV, (i == 0 && kk == 0) ? 0u : 1u);
+                mma_f8f6f4(d, adesc, blo, kIdPV, 1u);
+              }
+            }
+            mma_commit(bar(kBarPFree + pb));
+            mma_commit(bar(kBarEmpty + s));
+            if (i == ntile - 1) mma_commit(bar(kBarOFull));
+          }
+        }
+        it = first + ntile;
+        ++piece_idx;
+      }
+      mma_commit(bar(kBarDrain));
+      mbar_wait(bar(kBarDrain), 0, abort_flag, 100000000ull);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 12) {
+    // ======================= softmax / epilogue ===================================
+    const int q = warp & 3;              // TMEM lane quadrant
+    const int kh = (warp - 4) >> 2;      // half of each tile's keys, half of the O^T chunks
+    const int sub = lane >> 4;
+    const int rl = lane & 15;
+    const int r = 16 * q + rl;           // packed row
+    const int qtr = 2 * kh + sub;        // key quarter (16 keys) of a tile
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    const float kd = p.k_descale ? *p.k_descale : 1.0f;
+    const float vd = p.v_descale ? *p.v_descale : 1.0f;
+    const float cscale = p.scale_log2 * kd;
+    const int G = p.group;
+    unsigned char* qpe_s = sm + kOffQpe;
+    int it = 0, piece_idx = 0, round = 0;
+    int j = j_first;
+    long long ts = ts_first;
+    Piece pc;
+    bool ok = true;
+    // Waits are warp-uniform; after a failure the warp walks the same pieces
+    // and tiles "dry" so that every named barrier still sees all its threads.
+    auto wait_or_fail = [&](int b, uint32_t par, int code) {
+      if (!ok) return false;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(bar(b), par, abort_flag, kWaitLimitNs));
+      if (!got) {
+        if (lane == 0) fail(p, abort_flag, code);
+        ok = false;
+      }
+      return ok;
+    };
+    // Row-wide combine over the row's four threads (lanes t, t ^ 16 of this
+    // warp and of the quadrant's other warp), as in the GQA kernel.
+    int xround = 0;
+    auto exchange = [&](float v, bool is_max) {
+      v = is_max ? fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16)) : v + __shfl_xor_sync(0xffffffffu, v, 16);
+      const int par = xround & 1;
+      ++xround;
+      if (sub == 0) xch[(par * 2 + kh) * 64 + r] = v;
+      named_bar(1 + q, 64);
+      const float other = xch[(par * 2 + (kh ^ 1)) * 64 + r];
+      return is_max ? fmaxf(v, other) : v + other;
+    };
+    // Q of piece pq: latent columns [128 qtr, +128) and rope columns
+    // [16 qtr, +16) of row r, scaled by 2^e and split into e4m3 hi and lo.
+    // The latent part goes to the TMEM A operand (hi row in lane 32q + rl, lo
+    // row in lane 32q + 16 + rl, four columns a word), the rope part to the
+    // smem A operand. Returns the row's logit scale.
+    auto stage_q = [&](const Piece& pq, int qidx) -> float {
+      if (qidx > 0) wait_or_fail(kBarQFree, (qidx - 1) & 1, 128);
+      const bool row_ok = r < pq.R;
+      const int tq = row_ok ? r / G : 0;
+      const int gq = row_ok ? r - tq * G : 0;
+      const uint16_t* src = p.q + (int64_t)(pq.q0 + tq) * p.q_s0 + (int64_t)gq * p.q_s1;
+      // the row's largest |value| first (over its four threads), then the
+      // conversion, re-reading the 288 bytes (cache hits)
+      const bool ld = ok && row_ok;
+      const uint4* nsrc = reinterpret_cast<const uint4*>(src + 128 * qtr);
+      const uint4* psrc = reinterpret_cast<const uint4*>(src + kMlaNope + 16 * qtr);
+      float amax = 0.f;
+      if (ld) {
+#pragma unroll
+        for (int i = 0; i < 18; ++i) {
+          const uint4 a = i < 16 ? nsrc[i] : psrc[i - 16];
+          amax = fmaxf(amax, fmaxf(fmaxf(bf16_amax2(a.x), bf16_amax2(a.y)),
+                                   fmaxf(bf16_amax2(a.z), bf16_amax2(a.w))));
+        }
+      }
+      amax = exchange(amax, true);
+      int e = 0;
+      if (amax > 0.f && amax < INFINITY) {
+        const int E = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+        e = 7 - E;
+        e = e < -120 ? -120 : (e > 120 ? 120 : e);
+      }
+      const float up = __uint_as_float((uint32_t)(e + 127) << 23);
+      const float down = __uint_as_float((uint32_t)(127 - e) << 23);
+      if (ok) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          // own columns [128 qtr + 64 hf, +64): 16 words of hi and of lo
+          uint32_t hw[16], lw[16];
+#pragma unroll
+          for (int w = 0; w < 16; w += 2) {
+            const uint4 a = ld ? nsrc[8 * hf + (w >> 1)] : make_uint4(0, 0, 0, 0);
+            split_q4(a.x, a.y, up, hw[w], lw[w]);
+            split_q4(a.z, a.w, up, hw[w + 1], lw[w + 1]);
+          }
+          // sub 0 (hi lane) takes the hi terms of both threads' columns, sub 1
+          // (lo lane) the lo terms: trade the part the partner's lane takes
+          uint32_t d1[16], d2[16];
+#pragma unroll
+          for (int w = 0; w < 16; ++w) {
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, sub ? hw[w] : lw[w], 16);
+            d1[w] = sub ? recv : hw[w];   // columns of sub 0's span
+            d2[w] = sub ? lw[w] : recv;   // columns of sub 1's span
+          }
+          tmem_st_32x32b_x16(tmem + lane_base + kColQ + 64 * kh + 16 * hf, d1);
+          tmem_st_32x32b_x16(tmem + lane_base + kColQ + 64 * kh + 32 + 16 * hf, d2);
+        }
+        uint32_t ph[4], pl[4];
+#pragma unroll
+        for (int w = 0; w < 4; w += 2) {
+          const uint4 a = ld ? psrc[w >> 1] : make_uint4(0, 0, 0, 0);
+          split_q4(a.x, a.y, up, ph[w], pl[w]);
+          split_q4(a.z, a.w, up, ph[w + 1], pl[w + 1]);
+        }
+        const int mh = 32 * q + rl, ml = mh + 16;
+        *reinterpret_cast<uint4*>(qpe_s + core_off(mh, 16 * qtr, kMlaPe)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+        *reinterpret_cast<uint4*>(qpe_s + core_off(ml, 16 * qtr, kMlaPe)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarQFull));
+      }
+      return row_ok ? cscale * down : 0.f;
+    };
+    auto prefetch_q = [&](const Piece& pq) {
+      if (r < pq.R) {
+        const int tq = r / G, gq = r - tq * G;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q + (int64_t)(pq.q0 + tq) * p.q_s0 +
+                                                       (int64_t)gq * p.q_s1 + 128 * qtr));
+      }
+    };
+    float rs_next = 0.f;
+    bool staged_next = false;
+    while (next_piece(p, t0, t1, j, ts, pc)) {
+      Piece pn;
+      int jn = j;
+      long long tsn = ts;
+      const bool has_next = next_piece(p, t0, t1, jn, tsn, pn);
+      const float rs = staged_next ? rs_next : stage_q(pc, piece_idx);
+      staged_next = false;
+      if (has_next) prefetch_q(pn);
+      const bool row_ok = r < pc.R;
+      const int tq = row_ok ? r / G : 0;
+
+      float m_ref = -INFINITY;
+      float l = 0.f;
+      const int vis_end = pc.S - pc.L + tq;  // last visible key of this row
+      const int first = it;
+      for (int lt = pc.lt0; lt < pc.lt1; ++lt, ++it) {
+        const int cur = it;
+        const int b = cur & (kSBufs - 1);
+        const int pb = cur & (kPBufs - 1);
+        if (lt == pc.lt1 - 1 && has_next) {
+          rs_next = stage_q(pn, piece_idx + 1);
+          staged_next = true;
+        }
+        float x[16];  // logits of keys [16 qtr, +16) of this tile, this row
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = -INFINITY;
+        if (wait_or_fail(kBarSFull + b, (cur / kSBufs) & 1, 256)) {
+          tc_fence_after();
+          // own lane: the hi (sub 0) or lo (sub 1) part of row r, keys
+          // [32 kh, +32); sub 0 keeps the first 16 keys, sub 1 the second,
+          // each adding the partner lane's part
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + kColS + b * kT + 32 * kh, v);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarSFree + b));
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float mine = __uint_as_float(sub ? v[16 + i] : v[i]);
+            const float give = __uint_as_float(sub ? v[i] : v[16 + i]);
+            x[i] = (mine + __shfl_xor_sync(0xffffffffu, give, 16)) * rs;
+          }
+          const int key0 = lt * kT + 16 * qtr;
+          if (lt * kT + kT - 1 > pc.S - pc.L) {  // tail tile: causal mask
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (key0 + i > vis_end) x[i] = -INFINITY;
+          }
+        }
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) tmax = fmaxf(tmax, fmaxf(x[i], x[i + 1]));
+        tmax = exchange(tmax, true);
+
+        const bool need = ok && tmax > m_ref + kOvershoot;
+        const float m_new = need ? tmax + kHeadroom : m_ref;
+        const bool rescale = need && (m_ref != -INFINITY) && (cur > first);
+        const float alpha = rescale ? ex2(m_ref - m_new) : 1.f;
+        // O^T keeps a row in a column across all 128 lanes: every softmax
+        // warp scales its lanes' part of the rows that moved, so the decision
+        // is taken by all of them at once
+        float* al = row_vals + (round & 1) * 64;
+        ++round;
+        if (kh == 0 && sub == 0) al[r] = alpha;
+        const bool any = named_bar_or(kBarAllSoftmax, kSoftmaxThreads, rescale);
+        if (!ok) continue;
+        if (any) {
+          const int xp = cur - 1;  // O holds P V(xp) once that has completed
+          if (!wait_or_fail(kBarPFree + (xp & (kPBufs - 1)), (xp / kPBufs) & 1, 1024)) continue;
+          tc_fence_after();
+#pragma unroll 1
+          for (int k = 0; k < 4; ++k) {
+            uint32_t o[32];
+            const uint32_t ta = tmem + lane_base + kColO + 64 * (2 * kh + (k >> 1)) + 32 * (k & 1);
+            tmem_ld_32x32b_x32(ta, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al[32 * (k & 1) + i]);
+            tmem_st_32x32b_x32(ta, o);
+          }
+          tmem_wait_st();
+        }
+        l *= alpha;
+        m_ref = m_new;
+
+        // P buffer pb was last read by P V(cur - kPBufs)
+        if (cur >= kPBufs && !wait_or_fail(kBarPFree + pb, ((cur - kPBufs) / kPBufs) & 1, 512)) continue;
+        const float mref_s = m_ref - kPShift;
+        const bool live = m_ref != -INFINITY;
+        uint32_t ph[4], pl[4];
+        float ls = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float a = live ? ex2(x[2 * i] - mref_s) : 0.f;
+          const float bb = live ? ex2(x[2 * i + 1] - mref_s) : 0.f;
+          ls += a + bb;
+          uint32_t h2, l2;
+          split_p(a, bb, h2, l2);
+          if (i & 1) {
+            ph[i >> 1] |= h2 << 16;
+            pl[i >> 1] |= l2 << 16;
+          } else {
+            ph[i >> 1] = h2;
+            pl[i >> 1] = l2;
+          }
+        }
+        // P^T operand: row r, keys [16 qtr, +16) = one core-matrix row
+        unsigned char* pbuf = sm + kOffP + pb * kPBuf;
+        const int off = core_off(r, 16 * qtr, kT);
+        *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+        *reinterpret_cast<uint4*>(pbuf + kPHalf + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        l += ls;
+        // latent rows past S in the item's last tile (a partial page, pages
+        // never loaded) are zeroed so that 0 * garbage cannot reach O; Q K^T
+        // of this tile has completed (S was full)
+        const int zt0 = (lt == pc.nt - 1 && (pc.S % kT) != 0) ? pc.S - lt * kT : kT;
+        if (zt0 < kT) {
+          unsigned char* vst = sm + (cur % kSlots) * kTileBytes;
+          for (int idx = tid - 128; idx < (kT - zt0) * kChunks * 8; idx += kSoftmaxThreads) {
+            const int row = zt0 + idx / (kChunks * 8);
+            const int rem = idx % (kChunks * 8);
+            *reinterpret_cast<uint4*>(vst + (rem >> 3) * kRegion + row * 128 + (rem & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        tc_fence_before();  // the O^T rescale, before the arrive
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarPFull + pb));
+      }
+
+      // -- epilogue: this thread's lanes hold latent columns 128 a + 32 q + lane
+      // of chunks a = 2 kh, 2 kh + 1, for all packed rows (the columns)
+      wait_or_fail(kBarOFull, piece_idx & 1, 4096);
+      tc_fence_after();
+      const float lrow = exchange(l, false);
+      float* lr = row_vals + (round & 1) * 64;
+      ++round;
+      if (kh == 0 && sub == 0) lr[r] = lrow;
+      named_bar(kBarEpilogue, kSoftmaxThreads);
+      ++piece_idx;
+      if (!ok) continue;
+      const int64_t piece = (int64_t)pc.j + c;
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k) {
+        const int a = 2 * kh + (k >> 1);
+        const int col = 128 * a + 32 * q + lane;
+        const int r0 = 32 * (k & 1);
+        if (r0 >= pc.R) continue;  // warp-uniform
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + kColO + 64 * a + r0, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int rr = r0 + i;
+          if (rr >= pc.R) break;
+          const int t = rr / G, g = rr - t * G;
+          if (pc.direct) {
+            const float den = lr[rr];
+            const float inv = den > 0.f ? vd / den : 0.f;
+            p.out[(int64_t)(pc.q0 + t) * p.o_s0 + (int64_t)g * p.o_s1 + col] =
+                float_to_bf16_bits(__uint_as_float(o[i]) * inv);
+          } else {
+            p.ws_acc[(piece * p.max_rows + rr) * kMlaNope + col] = __uint_as_float(o[i]);
+          }
+        }
+      }
+      if (row_ok && !pc.direct && kh == 0 && sub == 0) {
+        p.ws_ml[(piece * p.max_rows + r) * 2 + 0] = (m_ref == -INFINITY) ? -INFINITY : m_ref - kPShift;
+        p.ws_ml[(piece * p.max_rows + r) * 2 + 1] = lrow;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarOFree));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t prepare_mla_tc() {
+  return cudaFuncSetAttribute(va_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
+cudaError_t launch_mla_tc(const Params& p, const CUtensorMap& tm_kv, cudaStream_t stream) {
+  va_mla_tc_kernel<<<dim3(p.num_splits), kThreads, kSmemBytes, stream>>>(p, tm_kv);
+  return cudaGetLastError();
+}
+
+}  // namespace va

@@ -143,9 +143,9 @@ constexpr uint32_t kLayoutSw128 = 2;
 // Instruction descriptor for kind::f16 / kind::f8f6f4: f32 accumulate,
 // A/B formats, B transposed (MN-major) flag, N and M.
 __host__ __device__ constexpr uint32_t instr_desc(uint32_t a_fmt, uint32_t b_fmt, bool b_mn_major,
-                                                  uint32_t n, uint32_t m) {
-  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((n >> 3) << 17) | ((m >> 4) << 24);
+                                                  uint32_t n, uint32_t m, bool a_mn_major = false) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -268,6 +268,18 @@ __device__ __forceinline__ float ex2(float x) {
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier that also ORs a predicate over its `count` threads.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 template <int SPLIT>

@@ -193,6 +193,47 @@ __device__ long long locate_work(const Params& p, int c, long long* scratch, int
   return N;
 }
 
+// One (sequence, KV head) item's share of this CTA. Tile indices are absolute
+// within the sequence: the item's tiles are [tb, nt), this CTA's [lt0, lt1).
+struct Piece {
+  int j, b, kvh, S, L, q0, R, nt, tb, lt0, lt1;
+  bool direct;
+};
+
+// Next (sequence, KV head) item with tiles in this CTA's split range [t0, t1);
+// ts is the split unit of item j's first tile.
+__device__ __forceinline__ bool next_piece(const Params& p, long long t0, long long t1, int& j,
+                                           long long& ts, Piece& pc) {
+  while (j < p.num_work && ts < t1) {
+    const int nt = work_tiles(p, j);
+    if (nt == 0) {
+      ++j;
+      continue;
+    }
+    pc.j = j;
+    pc.b = j / p.hkv;
+    pc.kvh = j - pc.b * p.hkv;
+    pc.S = seq_kv_len(p, pc.b);
+    pc.L = seq_q_len(p, pc.b);
+    pc.q0 = p.cu_q[pc.b];
+    pc.R = p.group * pc.L;
+    pc.tb = first_tile(p, pc.S, pc.L);
+    pc.nt = pc.tb + nt;
+    pc.lt0 = pc.tb + (int)((t0 > ts ? t0 : ts) - ts);
+    pc.lt1 = pc.tb + (int)((t1 < ts + nt ? t1 : ts + nt) - ts);
+    pc.direct = (pc.lt0 == pc.tb && pc.lt1 == pc.nt);
+    ts += work_cost(p, nt);  // the next item's first tile follows its start-up units
+    ++j;
+    return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void fail(const Params& p, volatile int* abort_flag, int code) {
+  *abort_flag = 1;
+  if (p.ws_status) atomicOr(p.ws_status, code);
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(((uint32_t)b) << 16);
 }

@@ -1,0 +1,119 @@
+"""The latent-cache (absorbed-MLA) path on the GPU, through the C-ABI
+(verify_attn_mla), against the CPU oracle oracle/mla_fp64.py with the parity
+tolerance (atol = rtol = 1e-2 on the bf16 output):
+
+* the small workload whole, at the library's split and at forced split
+  counts from 1 CTA to more CTAs than tiles;
+* seeded random batches: ragged lengths (0, 1, page and tile edges), 1-4
+  draft tokens, 4 / 8 / 16 heads, descales, forced splits;
+* bit-identical results run to run and under a relabelling of the physical
+  pages;
+* the long-context workload (16 sequences of 64K-128K keys), its shortest
+  and longest sequences, in the launch configuration the benchmark times."""
+import numpy as np
+import pytest
+import torch
+
+import speculative_decoding_verify_split_gb300 as va
+from speculative_decoding_verify_split_gb300.workloads import make_mla_workload, named_mla_workload
+from oracle.mla_fp64 import mla_oracle_from_torch
+from gpu_util import compare, rows_of
+
+pytestmark = pytest.mark.gpu
+
+
+def run(w, num_splits=0, ws=True):
+    out = torch.full((w.q.shape[0], w.q.shape[1], va.MLA_NOPE), float("nan"), dtype=torch.bfloat16,
+                     device="cuda")
+    workspace = None
+    if ws:
+        n = va.mla_workspace_size(w.q, w.seqused_k, w.max_seqlen_q, w.max_seqlen_k, num_splits)
+        workspace = torch.zeros(n + 256, dtype=torch.uint8, device="cuda")
+    va.run_mla_workload(w, out=out, workspace=workspace, num_splits=num_splits)
+    torch.cuda.synchronize()
+    if workspace is not None:
+        assert va.workspace_status(workspace) == 0
+    return out
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    w = named_mla_workload("mla_tiny")
+    return w, w.to("cuda"), mla_oracle_from_torch(w)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 2, 7, 64, 1000])
+def test_tiny_whole(tiny, splits):
+    w, wg, ref = tiny
+    compare(run(wg, splits), ref)
+
+
+def test_library_workspace(tiny):
+    w, wg, ref = tiny
+    compare(run(wg, ws=False), ref)
+
+
+def test_run_to_run_and_page_relabelling_bit_identical():
+    w = make_mla_workload([4, 3, 1], [3000, 700, 129], 16, seed=21, k_descale=0.8, v_descale=1.7)
+    wg = w.to("cuda")
+    a = run(wg)
+    for _ in range(3):
+        assert torch.equal(run(wg).view(torch.int16), a.view(torch.int16))
+    # move every page to a new physical slot
+    nb = wg.kv_cache.shape[0]
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(3)).to("cuda")
+    kv2 = torch.empty_like(wg.kv_cache)
+    kv2[perm] = wg.kv_cache
+    w2 = w.to("cuda")
+    w2.kv_cache = kv2
+    w2.block_table = perm.to(torch.int32)[wg.block_table.long()]
+    assert torch.equal(run(w2).view(torch.int16), a.view(torch.int16))
+    compare(a, mla_oracle_from_torch(w))
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_shapes(seed):
+    g = torch.Generator().manual_seed(500 + seed)
+    B = int(torch.randint(1, 7, (1,), generator=g))
+    hq = [4, 8, 16][int(torch.randint(0, 3, (1,), generator=g))]
+    qmax = min(4, 64 // hq)
+    q_lens = torch.randint(1, qmax + 1, (B,), generator=g).tolist()
+    choices = [0, 1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 500, 1000, 2500]
+    kv_lens = [choices[int(i)] for i in torch.randint(0, len(choices), (B,), generator=g)]
+    kd = float(torch.rand(1, generator=g) * 1.5 + 0.5)
+    vd = float(torch.rand(1, generator=g) * 1.5 + 0.5)
+    w = make_mla_workload(q_lens, kv_lens, hq, seed=600 + seed, k_descale=kd, v_descale=vd)
+    splits = [0, 1, 3, 200][seed % 4]
+    compare(run(w.to("cuda"), splits), mla_oracle_from_torch(w))
+
+
+def test_peaked_softmax_and_rescales():
+    """Queries scaled up so that row maxima jump across tiles (O^T rescales)
+    and single keys dominate (P near the top of its range)."""
+    w = make_mla_workload([4, 2, 3], [2000, 4100, 600], 16, seed=31)
+    w.q = (w.q.to(torch.float32) * 6).to(torch.bfloat16)
+    for splits in (1, 0, 11):
+        compare(run(w.to("cuda"), splits), mla_oracle_from_torch(w))
+
+
+def test_long_context_sampled():
+    w = named_mla_workload("mla_long_context_fp8", value_device="cuda")
+    wg = w.to("cuda")
+    got = run(wg)
+    kv = w.kv_lens
+    seqs = [int(np.argmin(kv)), int(np.argmax(kv))]
+    ref = mla_oracle_from_torch(w.to("cpu"), seqs)
+    r = rows_of(w.to("cpu"), seqs)
+    compare(got[torch.as_tensor(r, device="cuda")], ref[r])
+
+
+def test_errors():
+    w = make_mla_workload([2], [100], 16, seed=41).to("cuda")
+    with pytest.raises(va.VerifyAttnError) as e:   # 16 heads x 5 tokens > 64 rows
+        va.verify_attn_mla(w.q, w.kv_cache, w.block_table, w.cu_seqlens_q, w.seqused_k, 5,
+                           w.max_seqlen_k, w.softmax_scale)
+    assert e.value.status == 4
+    with pytest.raises(va.VerifyAttnError) as e:   # a BF16 latent cache is not read by this kernel
+        va.verify_attn_mla(w.q, w.kv_cache.to(torch.bfloat16), w.block_table, w.cu_seqlens_q,
+                           w.seqused_k, w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale)
+    assert e.value.status == 4

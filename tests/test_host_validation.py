@@ -144,3 +144,44 @@ def test_block_table_builder_rejects_bad_descriptors_before_launch():
     assert _bt_call(ip, torch.zeros(20, dtype=i32)[::2], bt, sk) == 7        # strided indices
     big = torch.zeros(65537, dtype=i32)
     assert _bt_call(big, ix, torch.zeros(65536, 1, dtype=i32), torch.zeros(65536, dtype=i32)) == 4
+
+
+# ---- the latent-cache entry point (validation runs before any CUDA call) ----
+
+def _mla_status(w, **over):
+    """verify_attn_mla's status for invalid arguments: returned by the host
+    checks before the library touches CUDA."""
+    import ctypes
+    a = dict(q=w.q, kv=w.kv_cache, bt=w.block_table, cu=w.cu_seqlens_q, su=w.seqused_k,
+             mq=w.max_seqlen_q, mk=w.max_seqlen_k, kd=w.k_descale, vd=w.v_descale,
+             out=torch.empty(w.q.shape[0], w.q.shape[1], 512, dtype=torch.bfloat16))
+    a.update(over)
+    ds = [va.desc(a[k]) for k in ("q", "kv", "bt", "cu", "su", "kd", "vd", "out")]
+    r = [None if d is None else ctypes.byref(d) for d in ds]
+    return va.library().verify_attn_mla(r[0], r[1], r[2], r[3], r[4], int(a["mq"]), int(a["mk"]),
+                                        0.1, r[5], r[6], r[7], None, 0, 0, None)
+
+
+@pytest.fixture(scope="module")
+def wm():
+    from speculative_decoding_verify_split_gb300.workloads import make_mla_workload
+    return make_mla_workload([4, 2], [100, 37], 16, seed=1, k_descale=1.0, v_descale=2.0)
+
+
+def test_mla_validation(wm):
+    assert _mla_status(wm, q=None) == NULL
+    assert _mla_status(wm, out=None) == NULL
+    assert _mla_status(wm, kv=wm.kv_cache.to(torch.bfloat16)) == UNSUP    # FP8 latent only
+    assert _mla_status(wm, kv=wm.kv_cache.view(torch.uint8).to(torch.int32)) == DTYPE
+    two = torch.cat([wm.kv_cache, wm.kv_cache], dim=2)
+    assert _mla_status(wm, kv=two) == UNSUP                                # one latent head
+    assert _mla_status(wm, kv=wm.kv_cache[..., :512].contiguous()) == UNSUP
+    assert _mla_status(wm, q=wm.q[..., :512].contiguous()) == UNSUP
+    assert _mla_status(wm, out=torch.empty(6, 16, 576, dtype=torch.bfloat16)) == UNSUP
+    assert _mla_status(wm, out=torch.empty(6, 8, 512, dtype=torch.bfloat16)) == SHAPE
+    assert _mla_status(wm, mq=5) == UNSUP                                  # 16 heads x 5 > 64 rows
+    assert _mla_status(wm, mk=100000) == SHAPE                             # table too narrow
+    assert _mla_status(wm, kd=torch.ones(2)) == SHAPE
+    shifted = torch.empty(wm.q.numel() + 1, dtype=torch.bfloat16)[1:].view(wm.q.shape)
+    assert _mla_status(wm, q=shifted) == LAYOUT                            # not 16-byte aligned
+    assert _mla_status(wm, cu=wm.cu_seqlens_q[:2]) == SHAPE
