@@ -33,7 +33,13 @@ METRIC = "verify-attn µs/call and achieved HBM GB/s (fraction of ~8 TB/s) on 1 
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-MAIN_KERNEL = {"fp8_e4m3": "va_main_tc_kernel<true>", "bf16": "va_main_tc_kernel<false>"}
+MAIN_KERNEL = {"fp8_e4m3": "va_main_tc_kernel<true, false>", "bf16": "va_main_tc_kernel<false, false>",
+               "mla": "va_mla_tc_kernel"}
+
+
+def is_mla(name):
+    """Workloads over an absorbed-MLA latent cache (verify_attn_mla)."""
+    return name.startswith("mla_")
 
 
 def parse():
@@ -180,9 +186,11 @@ def throughput(alg_bytes: int, world: int, ms_per_step: float) -> float:
 
 
 def workload_config(w, name, world):
+    layout = ({"layout": "absorbed-MLA latent cache, rows [latent 512 | rope 64], values = latent",
+               "row_width": 576, "value_dim": 512} if is_mla(name) else {"head_dim": 256})
     return {"workload": name, "num_seqs": w.num_seqs, "q_lens": sorted(set(w.q_lens)),
             "kv_len_range": [min(w.kv_lens), max(w.kv_lens)], "kv_tokens": sum(w.kv_lens),
-            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": 256,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, **layout,
             "page_size": 16, "kv_dtype": w.kv_dtype, "algorithmic_bytes": w.algorithmic_bytes(),
             "l2": ("inputs under 2x the 129 MB L2: a 256 MB buffer is written before every step, "
                    "outside the per-step CUDA events" if needs_flush(w) else
@@ -191,19 +199,29 @@ def workload_config(w, name, world):
             "parallelism": f"replicas x{world}", "seed": 0}
 
 
-def cpu_baseline(w_cpu, seconds):
+def seq_bytes(w, b, mla):
+    """Algorithmic bytes of sequence b of a workload (its share of
+    Workload.algorithmic_bytes / MlaWorkload.algorithmic_bytes)."""
+    e = 1 if w.kv_dtype == "fp8_e4m3" else 2
+    if mla:
+        return w.kv_lens[b] * 576 * e + w.q_lens[b] * w.num_q_heads * (576 + 512) * 2
+    return w.kv_lens[b] * w.num_kv_heads * 256 * 2 * e + 2 * w.q_lens[b] * w.num_q_heads * 256 * 2
+
+
+def cpu_baseline(w_cpu, seconds, mla=False):
     """The fp64 oracle as it stands, on sequences of the workload in order,
     until `seconds` of wall time have passed (at least one sequence)."""
-    from oracle.attention_fp64 import oracle_from_torch
+    if mla:
+        from oracle.mla_fp64 import mla_oracle_from_torch as run_oracle
+    else:
+        from oracle.attention_fp64 import oracle_from_torch as run_oracle
     done, nbytes = [], 0
-    e = 1 if w_cpu.kv_dtype == "fp8_e4m3" else 2
     t0 = time.perf_counter()
     c0 = time.process_time()
     for b in range(w_cpu.num_seqs):
-        oracle_from_torch(w_cpu, [b])
+        run_oracle(w_cpu, [b])
         done.append(b)
-        nbytes += (w_cpu.kv_lens[b] * w_cpu.num_kv_heads * 256 * 2 * e
-                   + 2 * w_cpu.q_lens[b] * w_cpu.num_q_heads * 256 * 2)
+        nbytes += seq_bytes(w_cpu, b, mla)
         if time.perf_counter() - t0 >= seconds:
             break
     wall = time.perf_counter() - t0
@@ -289,17 +307,37 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     import speculative_decoding_verify_split_gb300 as va
-    from speculative_decoding_verify_split_gb300.workloads import named_workload
+    from speculative_decoding_verify_split_gb300.workloads import named_mla_workload, named_workload
 
-    w = named_workload(args.workload, seed=0, value_device=str(dev)).to(dev)
-    alg = w.algorithmic_bytes()
-    out = torch.empty_like(w.q)
-    n_ws = va.workspace_size(w.q, w.k_cache, w.seqused_k, w.max_seqlen_q, w.max_seqlen_k)
-    ws = torch.empty(n_ws + 256, dtype=torch.uint8, device=dev)
+    mla = is_mla(args.workload)
     stream = torch.cuda.current_stream(dev)
+    if mla:
+        w = named_mla_workload(args.workload, seed=0, value_device=str(dev)).to(dev)
+        out = torch.empty(w.q.shape[0], w.q.shape[1], va.MLA_NOPE, dtype=torch.bfloat16, device=dev)
+        n_ws = va.mla_workspace_size(w.q, w.seqused_k, w.max_seqlen_q, w.max_seqlen_k)
+        inputs = ("q", "kv_cache", "block_table", "cu_seqlens_q", "seqused_k")
+        kernel = MAIN_KERNEL["mla"]
+    else:
+        w = named_workload(args.workload, seed=0, value_device=str(dev)).to(dev)
+        out = torch.empty_like(w.q)
+        n_ws = va.workspace_size(w.q, w.k_cache, w.seqused_k, w.max_seqlen_q, w.max_seqlen_k)
+        inputs = ("q", "k_cache", "v_cache", "block_table", "cu_seqlens_q", "seqused_k")
+        kernel = MAIN_KERNEL[w.kv_dtype]
+    alg = w.algorithmic_bytes()
+    ws = torch.empty(n_ws + 256, dtype=torch.uint8, device=dev)
 
     def step(ev_mid=None):
-        va.run_workload_ex(w, out=out, workspace=ws, stream=stream, event_after_main=ev_mid)
+        if mla:
+            va.run_mla_workload(w, out=out, workspace=ws, stream=stream, event_after_main=ev_mid)
+        else:
+            va.run_workload_ex(w, out=out, workspace=ws, stream=stream, event_after_main=ev_mid)
+
+    def public_call():
+        # the plain entry points, library-owned workspace
+        if mla:
+            va.run_mla_workload(w, out=out, stream=stream)
+        else:
+            va.run_workload(w, out=out, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -367,8 +405,7 @@ def run_ours(args):
 
     # End to end through the public API with host buffers: every step copies
     # all inputs from pinned host memory and reads the output back.
-    host = {k: getattr(w, k).cpu().pin_memory() for k in
-            ("q", "k_cache", "v_cache", "block_table", "cu_seqlens_q", "seqused_k")}
+    host = {k: getattr(w, k).cpu().pin_memory() for k in inputs}
     for k in ("k_descale", "v_descale"):
         if getattr(w, k) is not None:
             host[k] = getattr(w, k).cpu().pin_memory()
@@ -379,7 +416,7 @@ def run_ours(args):
     def e2e_step():
         for k, t in host.items():
             getattr(w, k).copy_(t, non_blocking=True)
-        va.run_workload(w, out=out, stream=stream)
+        public_call()
         out_host.copy_(out, non_blocking=True)
 
     e2e_step()
@@ -396,7 +433,7 @@ def run_ours(args):
     e2e_ms = ea.elapsed_time(eb) / E
     e2e_ms = max_over_ranks(e2e_ms, world, dist if world > 1 else None, dev)
 
-    draft = draft_extend_timing(va, w, stream, torch, min(K, 200))
+    draft = None if mla else draft_extend_timing(va, w, stream, torch, min(K, 200))
 
     peak, peak_src = peak_hbm()
     achieved = alg / (main_ms / 1e3) / 1e9
@@ -409,7 +446,7 @@ def run_ours(args):
         "us_per_call": round(ms_per_step * 1e3, 2),
         "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "main_kernel_us": round(main_ms * 1e3, 2),
-        "roofline": {"bound": "hbm", "kernel": MAIN_KERNEL[w.kv_dtype], "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_src} (HBM copy bandwidth)",
                      "traffic": recorded_traffic(args.workload),
@@ -418,12 +455,12 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": 2 * K,
-        "draft_extend": draft,
+        **({} if draft is None else {"draft_extend": draft}),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         w_cpu = w.to("cpu")
-        line["cpu_baseline"] = cpu_baseline(w_cpu, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w_cpu, args.cpu_seconds, mla)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -437,18 +474,27 @@ def run_reference(args):
     rank = env_int("RANK", 0)
     if rank != 0:
         return
-    from oracle.attention_fp64 import oracle_from_torch
-    from speculative_decoding_verify_split_gb300.workloads import make_workload, workload_structure
-
-    st = workload_structure(args.workload, 0)
+    from speculative_decoding_verify_split_gb300.workloads import (make_mla_workload, make_workload,
+                                                                   mla_workload_structure,
+                                                                   workload_structure)
+    mla = is_mla(args.workload)
+    if mla:
+        from oracle.mla_fp64 import mla_oracle_from_torch as oracle_from_torch
+        st = dict(mla_workload_structure(args.workload, 0), Hkv=1, kv_dtype="fp8_e4m3")
+    else:
+        from oracle.attention_fp64 import oracle_from_torch
+        st = workload_structure(args.workload, 0)
     q_lens, kv_lens = st["q_lens"], st["kv_lens"]
     e = 1 if st["kv_dtype"] == "fp8_e4m3" else 2
+    key_bytes = 576 * e if mla else st["Hkv"] * 512 * e  # cache bytes per key
 
     def sample(b, cap, seed):
         S = min(kv_lens[b], cap)
-        w = make_workload([q_lens[b]], [S], st["Hq"], st["Hkv"], st["kv_dtype"], seed=seed)
-        nbytes = S * st["Hkv"] * 256 * 2 * e + 2 * q_lens[b] * st["Hq"] * 256 * 2
-        return w, nbytes
+        if mla:
+            w = make_mla_workload([q_lens[b]], [S], st["Hq"], seed=seed)
+        else:
+            w = make_workload([q_lens[b]], [S], st["Hq"], st["Hkv"], st["kv_dtype"], seed=seed)
+        return w, seq_bytes(w, 0, mla)
 
     # calibrate the cap so that all steps fit in about two minutes
     w, nb = sample(0, 4096, 1000)
@@ -456,7 +502,7 @@ def run_reference(args):
     oracle_from_torch(w)
     rate = nb / (time.perf_counter() - t)
     budget = max(0.05, min(20.0, 120.0 / (args.steps + args.warmup)))
-    cap = int(max(256, min(max(kv_lens), budget * rate / (st["Hkv"] * 512 * e))))
+    cap = int(max(256, min(max(kv_lens), budget * rate / key_bytes)))
 
     times, nbytes_total = [], 0
     for i in range(args.warmup + args.steps):
@@ -476,7 +522,8 @@ def run_reference(args):
             "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "num_seqs": len(q_lens), "q_len": q_lens[0],
-                       "num_q_heads": st["Hq"], "num_kv_heads": st["Hkv"], "head_dim": 256,
+                       "num_q_heads": st["Hq"], "num_kv_heads": st["Hkv"],
+                       **({"row_width": 576, "value_dim": 512} if mla else {"head_dim": 256}),
                        "page_size": 16, "kv_dtype": st["kv_dtype"]},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"each step one sequence of the workload's shape with kv_len "

@@ -339,6 +339,9 @@ va_status verify_attn_block_table_from_indptr(const va_tensor* kv_indptr,
  *               workspace (grown with cudaMalloc as needed).
  *  num_splits   0 = the library's choice (one CTA per SM, fewer for small
  *               batches); > 0 forces that many CTAs.
+ *  event_after_main  optional cudaEvent_t (NULL: none) recorded on stream
+ *               between the main kernel and the merge kernel, as in
+ *               verify_attn_ex.
  *
  * Layout: innermost strides 1 and every other stride a multiple of 16 bytes;
  * q, out, kv_cache 16-byte aligned.
@@ -354,7 +357,7 @@ va_status verify_attn_mla(const va_tensor* q, const va_tensor* kv_cache, const v
                           int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
                           const va_tensor* k_descale, const va_tensor* v_descale, va_tensor* out,
                           void* workspace, size_t workspace_bytes, int32_t num_splits,
-                          void* stream);
+                          void* event_after_main, void* stream);
 
 /* Workspace bytes verify_attn_mla needs for these shapes on the current
  * device (0 if they are unsupported). */

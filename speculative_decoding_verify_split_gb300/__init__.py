@@ -101,7 +101,7 @@ def _lib():
         lib.verify_attn_opt.restype = ctypes.c_int32
         lib.verify_attn_mla.argtypes = [P] * 5 + [ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
                                                   P, P, P, ctypes.c_void_p, ctypes.c_size_t,
-                                                  ctypes.c_int32, ctypes.c_void_p]
+                                                  ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
         lib.verify_attn_mla.restype = ctypes.c_int32
         lib.verify_attn_mla_workspace_size.argtypes = [ctypes.c_int32] * 5
         lib.verify_attn_mla_workspace_size.restype = ctypes.c_size_t
@@ -355,11 +355,12 @@ def draft_extend_attn(q, k_cache, v_cache, kv_indptr, kv_indices, cu_seqlens_q,
 def verify_attn_mla(q, kv_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q: int,
                     max_seqlen_k: int, softmax_scale: float, k_descale=None, v_descale=None,
                     out=None, workspace: Optional[torch.Tensor] = None, num_splits: int = 0,
-                    stream=None):
+                    stream=None, event_after_main=None):
     """Target-verify attention over an absorbed-MLA latent cache (see
     include/verify_attn.h): q [total_q, Hq, 576] bf16, kv_cache
     [num_blocks, 16, 1, 576] e4m3, out [total_q, Hq, 512] bf16. ``workspace``
-    None uses the library's own."""
+    None uses the library's own; ``event_after_main`` (a torch.cuda.Event) is
+    recorded between the two kernels when given."""
     if out is None:
         out = torch.empty(q.shape[0], q.shape[1], MLA_NOPE, dtype=torch.bfloat16, device=q.device)
     ds = [desc(x) for x in (q, kv_cache, block_table, cu_seqlens_q, seqused_k, k_descale,
@@ -375,6 +376,7 @@ def verify_attn_mla(q, kv_cache, block_table, cu_seqlens_q, seqused_k, max_seqle
         s = _lib().verify_attn_mla(r[0], r[1], r[2], r[3], r[4], int(max_seqlen_q),
                                    int(max_seqlen_k), float(softmax_scale), r[5], r[6], r[7],
                                    ctypes.c_void_p(addr), nbytes, int(num_splits),
+                                   ctypes.c_void_p(_event_handle(event_after_main)),
                                    ctypes.c_void_p(_stream_handle(stream, q.device)))
     if s != VA_OK:
         raise VerifyAttnError(s, "verify_attn_mla")
@@ -391,9 +393,10 @@ def mla_workspace_size(q, seqused_k, max_seqlen_q, max_seqlen_k, num_splits=0) -
     return int(n)
 
 
-def run_mla_workload(w, out=None, workspace=None, num_splits=0, stream=None):
+def run_mla_workload(w, out=None, workspace=None, num_splits=0, stream=None,
+                     event_after_main=None):
     """verify_attn_mla on a ``workloads.MlaWorkload`` whose tensors are on the GPU."""
     return verify_attn_mla(w.q, w.kv_cache, w.block_table, w.cu_seqlens_q, w.seqused_k,
                            w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale, w.k_descale,
                            w.v_descale, out=out, workspace=workspace, num_splits=num_splits,
-                           stream=stream)
+                           stream=stream, event_after_main=event_after_main)

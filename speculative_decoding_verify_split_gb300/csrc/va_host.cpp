@@ -388,7 +388,10 @@ va_status make_mla_plan(int64_t B, int64_t hq, int32_t max_q, int32_t max_k, int
   plan->max_rows = (int32_t)(hq * max_q);
   plan->num_work = (int32_t)B;
   plan->kernel = kKernelTc;
-  plan->workspace_bytes = (int64_t)workspace_layout(B, splits, hq * max_q, kMlaNope).total;
+  // the partials' rows are padded to mla_row_stride; the layout is sized with
+  // that row count (launch_mla takes the same offsets)
+  plan->workspace_bytes =
+      (int64_t)workspace_layout(B, splits, mla_row_stride((int)(hq * max_q)), kMlaNope).total;
   return VA_OK;
 }
 
@@ -411,7 +414,8 @@ static bool make_mla_map(CUtensorMap* m, const va_tensor* t, int64_t nb) {
 va_status launch_mla(const va_tensor* q, const va_tensor* kv, const va_tensor* bt, const va_tensor* cu,
                      const va_tensor* su, int32_t max_q, int32_t max_k, float scale,
                      const va_tensor* kd, const va_tensor* vd, va_tensor* out, const Shapes& sh,
-                     const va_plan& plan, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                     const va_plan& plan, void* ws, size_t ws_bytes, cudaEvent_t ev_mid,
+                     cudaStream_t stream) {
   if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;
   if ((size_t)plan.workspace_bytes > ws_bytes || !ws) return VA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return VA_ERR_WORKSPACE;
@@ -452,7 +456,8 @@ va_status launch_mla(const va_tensor* q, const va_tensor* kv, const va_tensor* b
   p.num_work = plan.num_work;
   p.piece_cost = kMlaPieceCostTiles;
   p.dv = kMlaNope;
-  const WorkspaceLayout lay = workspace_layout(plan.num_work, plan.num_splits, plan.max_rows, kMlaNope);
+  const WorkspaceLayout lay =
+      workspace_layout(plan.num_work, plan.num_splits, mla_row_stride(plan.max_rows), kMlaNope);
   char* base = static_cast<char*>(ws);
   p.ws_status = reinterpret_cast<int32_t*>(base + lay.status_off);
   p.ws_meta = reinterpret_cast<int32_t*>(base + lay.meta_off);
@@ -462,6 +467,7 @@ va_status launch_mla(const va_tensor* q, const va_tensor* kv, const va_tensor* b
   std::memset(&tm, 0, sizeof(tm));
   if (sh.num_blocks > 0 && !make_mla_map(&tm, kv, sh.num_blocks)) return VA_ERR_LAYOUT;
   if (launch_mla_tc(p, tm, stream) != cudaSuccess) return VA_ERR_CUDA;
+  if (ev_mid && cudaEventRecord(ev_mid, stream) != cudaSuccess) return VA_ERR_CUDA;
   if (launch_merge(p, stream) != cudaSuccess) return VA_ERR_CUDA;
   return VA_OK;
 }
@@ -638,7 +644,7 @@ VA_EXPORT va_status verify_attn_mla(const va_tensor* q, const va_tensor* kv_cach
                                     int32_t max_seqlen_k, float softmax_scale,
                                     const va_tensor* k_descale, const va_tensor* v_descale,
                                     va_tensor* out, void* workspace, size_t workspace_bytes,
-                                    int32_t num_splits, void* stream) {
+                                    int32_t num_splits, void* event_after_main, void* stream) {
   Shapes sh;
   va_status s = validate_mla(q, kv_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
                              max_seqlen_k, k_descale, v_descale, out, &sh);
@@ -671,7 +677,7 @@ VA_EXPORT va_status verify_attn_mla(const va_tensor* q, const va_tensor* kv_cach
   }
   return launch_mla(q, kv_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q, max_seqlen_k,
                     softmax_scale, k_descale, v_descale, out, sh, plan, workspace, workspace_bytes,
-                    static_cast<cudaStream_t>(stream));
+                    static_cast<cudaEvent_t>(event_after_main), static_cast<cudaStream_t>(stream));
 }
 
 VA_EXPORT size_t verify_attn_mla_workspace_size(int32_t num_seqs, int32_t num_q_heads,

@@ -18,6 +18,14 @@ constexpr int kHeadDim = 256;
 constexpr int kMlaNope = 512;
 constexpr int kMlaPe = 64;
 constexpr int kMlaRow = kMlaNope + kMlaPe;  // 576
+// Row stride of the latent path's column-major partials (a multiple of 4
+// rows, so that 4 rows are one 16-byte store).
+__host__ __device__ constexpr int mla_row_stride(int max_rows) { return (max_rows + 3) & ~3; }
+// Index of (row, column) of piece `piece` in those partials, laid out in
+// groups of four rows: [piece][row / 4][column][row % 4].
+__host__ __device__ constexpr int64_t mla_acc_index(int64_t piece, int row, int col, int ldr) {
+  return ((piece * (ldr / 4) + row / 4) * kMlaNope + col) * 4 + (row % 4);
+}
 constexpr int kPageSize = 16;
 constexpr int kMaxRows = 64;  // G * max_seqlen_q packed rows per (sequence, KV head)
 
@@ -103,7 +111,11 @@ cudaError_t launch_block_table(const int32_t* indptr, const int32_t* indices, in
 cudaError_t prepare_main_tc();  // once per device: opt in to its shared memory
 // Latent-cache main kernel (va_mla_tc.cu): FP8 cache, 64-key tiles.
 constexpr int kMlaTileKeys = 64;
-constexpr int kMlaPieceCostTiles = 6;
+// Split cost of starting an item on the latent path, in 64-key tiles: Q
+// staging (576 columns) and the 128 KB partial of the previous piece, both
+// through a memory system saturated by the ring. Swept over 6/12/18/24/32 on
+// the mid- and long-context latent workloads: 18.
+constexpr int kMlaPieceCostTiles = 18;
 cudaError_t prepare_mla_tc();
 cudaError_t launch_mla_tc(const Params& p, const CUtensorMap& tm_kv, cudaStream_t stream);
 cudaError_t launch_main_tc(const Params& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,

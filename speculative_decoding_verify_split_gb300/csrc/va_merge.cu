@@ -115,11 +115,129 @@ __global__ void __launch_bounds__(kMergeThreads, 4) va_merge_kernel(const Params
   *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
 }
 
+// The latent-cache path's merge. Its partials come in groups of four rows,
+// partial[piece][row / 4][column][row % 4] (mla_acc_index), and every piece
+// has one, also when a single CTA held the whole item. One thread per output
+// column (512), one group of four packed rows per CTA: a thread reads one
+// 16-byte group per segment, a warp's loads are 512 contiguous bytes, and two
+// CTAs fit on an SM. Segments go eight at a time: every thread issues all its partial loads at once (one L2 round trip
+// per group), while warp 0, one lane per (segment, row), reads the group's
+// (m, l), moves each row's running max and publishes the group's weights
+// 2^(m_s - M) and the rescale of the earlier sum in shared memory. Each output row is written as
+// one coalesced 1 KB line.
+constexpr int kMlaMergeRows = 4;  // one 16-byte row group per thread and segment
+constexpr int kMlaSegChunk = 8;
+
+__global__ void __launch_bounds__(kMlaNope, 2) va_merge_mla_kernel(const Params p) {
+  __shared__ float s_w[kMlaSegChunk][kMlaMergeRows];
+  __shared__ float s_sc[kMlaMergeRows];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int j = blockIdx.x;  // one KV head: item j is sequence j
+  const int r0 = blockIdx.y * kMlaMergeRows;
+  static_assert(kMlaMergeRows == 4 && kMlaSegChunk * kMlaMergeRows == 32, "one row group per thread; warp 0 holds a group's (m, l)");
+  const int d = threadIdx.x;
+  const int L = seq_q_len(p, j);
+  const int G = p.group;
+  const int R = G * L;
+  if (r0 >= R) return;  // CTA-uniform
+  const int nrow = R - r0 < kMlaMergeRows ? R - r0 : kMlaMergeRows;
+  const int q0 = p.cu_q[j];
+  auto dst = [&](int rr) {
+    const int t = (r0 + rr) / G, g = (r0 + rr) - t * G;
+    return p.out + (int64_t)(q0 + t) * p.o_s0 + (int64_t)g * p.o_s1 + d;
+  };
+  const int nt = work_tiles(p, j);
+  if (nt == 0) {
+    for (int rr = 0; rr < nrow; ++rr) *dst(rr) = 0;
+    return;
+  }
+  const long long N = p.ws_meta[p.num_work];
+  const long long ts = p.ws_meta[j];
+  const int c0 = split_of(ts, N, p.num_splits);
+  const int c1 = split_of(ts + nt - 1, N, p.num_splits);
+  const int ns = c1 - c0 + 1;
+  const bool may_be_empty = N < (long long)p.num_splits;
+  const int ldr = mla_row_stride(p.max_rows);
+  // a CTA range can be empty only with fewer split units than CTAs; such a
+  // segment wrote nothing and is never read
+  auto exists = [&](int k) {
+    const int c = c0 + k;
+    return k < ns && (!may_be_empty || split_begin(N, c, p.num_splits) != split_begin(N, c + 1, p.num_splits));
+  };
+
+  float acc[kMlaMergeRows];
+#pragma unroll
+  for (int i = 0; i < kMlaMergeRows; ++i) acc[i] = 0.f;
+  float M = -INFINITY, den = 0.f;  // row (d & 3)'s, in warp 0
+  for (int base = 0; base < ns; base += kMlaSegChunk) {
+    float4 a[kMlaSegChunk];
+#pragma unroll
+    for (int k = 0; k < kMlaSegChunk; ++k) {
+      const int64_t piece = (int64_t)j + c0 + base + k;
+      a[k] = exists(base + k) ? __ldcg(reinterpret_cast<const float4*>(p.ws_acc + mla_acc_index(piece, r0, d, ldr)))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (d < 32) {
+      // warp 0: lane 4k + i holds segment base + k, row r0 + i; rows reduce
+      // over the lanes with the same i (xor 4, 8, 16)
+      const int k = d >> 2, i = d & 3;
+      float2 ml = make_float2(-INFINITY, 0.f);
+      if (i < nrow && exists(base + k))
+        ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (((int64_t)j + c0 + base + k) * p.max_rows + r0 + i) * 2));
+      float mc = ml.x;
+      mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 4));
+      mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 8));
+      mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 16));
+      mc = fmaxf(mc, M);
+      const float sc = (M == -INFINITY || mc == -INFINITY) ? 0.f : exp2f(M - mc);
+      const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mc);
+      float wl = w * ml.y;
+      wl += __shfl_xor_sync(0xffffffffu, wl, 4);
+      wl += __shfl_xor_sync(0xffffffffu, wl, 8);
+      wl += __shfl_xor_sync(0xffffffffu, wl, 16);
+      den = den * sc + wl;  // each lane keeps its row's (M, den)
+      if (mc != -INFINITY) M = mc;
+      s_w[k][i] = w;
+      if (k == 0) s_sc[i] = sc;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kMlaMergeRows; ++i) {
+      float x = acc[i] * s_sc[i];
+#pragma unroll
+      for (int k = 0; k < kMlaSegChunk; ++k) {
+        const float4 v = a[k];
+        x = fmaf(s_w[k][i], i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w)), x);
+      }
+      acc[i] = x;
+    }
+    __syncthreads();  // s_w and s_sc are rewritten by the next group
+  }
+  const float vd = p.v_descale ? *p.v_descale : 1.0f;
+  if (d < kMlaMergeRows) s_sc[d] = (M == -INFINITY || !(den > 0.f)) ? 0.f : vd / den;  // lanes 0-3
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kMlaMergeRows; ++i)
+    if (i < nrow) *dst(i) = float_to_bf16_bits(acc[i] * s_sc[i]);
+}
+
 }  // namespace
 
 cudaError_t launch_merge(const Params& p, cudaStream_t stream) {
   if (p.num_work == 0 || p.max_rows == 0) return cudaSuccess;
   if (p.dv != kHeadDim && p.dv != kMlaNope) return cudaErrorInvalidValue;
+  if (p.dv == kMlaNope) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.num_work, (unsigned)((p.max_rows + kMlaMergeRows - 1) / kMlaMergeRows));
+    cfg.blockDim = dim3(kMlaNope);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, va_merge_mla_kernel, p);
+  }
   const int rows_per_cta = kMergeThreads / (p.dv / 4);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.num_work, (unsigned)((p.max_rows + rows_per_cta - 1) / rows_per_cta));
@@ -131,7 +249,6 @@ cudaError_t launch_merge(const Params& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.dv == kMlaNope) return cudaLaunchKernelEx(&cfg, va_merge_kernel<false, kMlaNope>, p);
   return p.sinks ? cudaLaunchKernelEx(&cfg, va_merge_kernel<true, kHeadDim>, p)
                  : cudaLaunchKernelEx(&cfg, va_merge_kernel<false, kHeadDim>, p);
 }

@@ -72,8 +72,7 @@ static_assert(kTileBytes % 1024 == 0 && kOffQpe % 1024 == 0, "swizzle atoms");
 
 constexpr int kThreads = 416;  // 13 warps
 constexpr int kSoftmaxThreads = 256;
-constexpr int kBarAllSoftmax = 5;  // named barriers: 1-4 per quadrant, 5 and 6 all softmax warps
-constexpr int kBarEpilogue = 6;
+constexpr int kBarAllSoftmax = 5;  // named barriers: 1-4 per quadrant, 5 all softmax warps
 
 constexpr uint32_t kColO = 0;
 constexpr uint32_t kColS = 256;
@@ -83,9 +82,18 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdQK = instr_desc(0, 0, false, kT, 128);         // e4m3 x e4m3, N = 64 keys
 constexpr uint32_t kIdPV = instr_desc(0, 0, false, 64, 128, true);   // A = V^T MN-major, N = 64 rows
 
+// P = 2^(s - m_ref + kPShift) as in the GQA kernel. The reference max moves
+// only when a tile's max passes m_ref + kOvershoot (2.8: P stays <= 2^8.8,
+// under e4m3's 448), to that max + kHeadroom. A row's first reference takes
+// kHeadroomFirst instead: MLA logits are wide (sd ~2.5 log2 units on random
+// data), so the running max keeps growing for many tiles after the first,
+// and every move here costs a CTA-wide pass over O^T; with 4 the moves all
+// but vanish, and m_ref still ends near the row's max, so that the keys
+// flushed to zero below m_ref - 16 carry no more mass than with 1.
 constexpr float kPShift = 6.f;
 constexpr float kHeadroom = 1.f;
-constexpr float kOvershoot = 2.5f;
+constexpr float kHeadroomFirst = 4.f;
+constexpr float kOvershoot = 2.8f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 enum : int {
@@ -158,6 +166,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   int j_first = 0;
   locate_work<kThreads>(p, c, scratch, s_j, s_ts, &t0, &t1, &j_first, &ts_first);
   if (t0 >= t1) return;
+  if (warp >= 4 && warp < 12) {
+    // the first item's Q rows into L2 before the ring's first loads flood HBM
+    int jq = j_first;
+    long long tq = ts_first;
+    Piece pq;
+    if (next_piece(p, t0, t1, jq, tq, pq)) {
+      const int r = 16 * (warp & 3) + (lane & 15), qtr = 2 * ((warp - 4) >> 2) + (lane >> 4);
+      if (r < pq.R) {
+        const uint16_t* src = p.q + (int64_t)(pq.q0 + r / p.group) * p.q_s0 + (int64_t)(r % p.group) * p.q_s1;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128 * qtr));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128 * qtr + 64));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + kMlaNope + 16 * qtr));
+      }
+    }
+  }
 
   constexpr uint32_t kSwWarps = kSoftmaxThreads / 32;
   if (tid == 0) {
@@ -344,7 +367,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qtr = 2 * kh + sub;        // key quarter (16 keys) of a tile
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const float kd = p.k_descale ? *p.k_descale : 1.0f;
-    const float vd = p.v_descale ? *p.v_descale : 1.0f;
     const float cscale = p.scale_log2 * kd;
     const int G = p.group;
     unsigned char* qpe_s = sm + kOffQpe;
@@ -451,11 +473,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return row_ok ? cscale * down : 0.f;
     };
+    // The next piece's Q segments of this thread (three 128-byte lines) into
+    // L2, a piece ahead: under full HBM load a round trip to DRAM takes
+    // several microseconds, and staging Q sits on the softmax's path.
     auto prefetch_q = [&](const Piece& pq) {
       if (r < pq.R) {
         const int tq = r / G, gq = r - tq * G;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q + (int64_t)(pq.q0 + tq) * p.q_s0 +
-                                                       (int64_t)gq * p.q_s1 + 128 * qtr));
+        const uint16_t* src = p.q + (int64_t)(pq.q0 + tq) * p.q_s0 + (int64_t)gq * p.q_s1;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128 * qtr));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128 * qtr + 64));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + kMlaNope + 16 * qtr));
       }
     };
     float rs_next = 0.f;
@@ -516,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmax = exchange(tmax, true);
 
         const bool need = ok && tmax > m_ref + kOvershoot;
-        const float m_new = need ? tmax + kHeadroom : m_ref;
+        const float m_new = need ? tmax + (m_ref == -INFINITY ? kHeadroomFirst : kHeadroom) : m_ref;
         const bool rescale = need && (m_ref != -INFINITY) && (cur > first);
         const float alpha = rescale ? ex2(m_ref - m_new) : 1.f;
         // O^T keeps a row in a column across all 128 lanes: every softmax
@@ -527,29 +554,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kh == 0 && sub == 0) al[r] = alpha;
         const bool any = named_bar_or(kBarAllSoftmax, kSoftmaxThreads, rescale);
         if (!ok) continue;
-        if (any) {
-          const int xp = cur - 1;  // O holds P V(xp) once that has completed
-          if (!wait_or_fail(kBarPFree + (xp & (kPBufs - 1)), (xp / kPBufs) & 1, 1024)) continue;
-          tc_fence_after();
-#pragma unroll 1
-          for (int k = 0; k < 4; ++k) {
-            uint32_t o[32];
-            const uint32_t ta = tmem + lane_base + kColO + 64 * (2 * kh + (k >> 1)) + 32 * (k & 1);
-            tmem_ld_32x32b_x32(ta, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al[32 * (k & 1) + i]);
-            tmem_st_32x32b_x32(ta, o);
-          }
-          tmem_wait_st();
-        }
-        l *= alpha;
-        m_ref = m_new;
 
         // P buffer pb was last read by P V(cur - kPBufs)
         if (cur >= kPBufs && !wait_or_fail(kBarPFree + pb, ((cur - kPBufs) / kPBufs) & 1, 512)) continue;
-        const float mref_s = m_ref - kPShift;
-        const bool live = m_ref != -INFINITY;
+        const float mref_s = m_new - kPShift;
+        const bool live = m_new != -INFINITY;
         uint32_t ph[4], pl[4];
         float ls = 0.f;
 #pragma unroll
@@ -572,7 +581,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int off = core_off(r, 16 * qtr, kT);
         *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
         *reinterpret_cast<uint4*>(pbuf + kPHalf + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-        l += ls;
+        // then the rows that moved (P V(cur - 1) has to be in O^T first; the
+        // wait overlaps the work above)
+        if (any) {
+          const int xp = cur - 1;
+          if (!wait_or_fail(kBarPFree + (xp & (kPBufs - 1)), (xp / kPBufs) & 1, 1024)) continue;
+          tc_fence_after();
+#pragma unroll 1
+          for (int k = 0; k < 4; ++k) {
+            uint32_t o[32];
+            const uint32_t ta = tmem + lane_base + kColO + 64 * (2 * kh + (k >> 1)) + 32 * (k & 1);
+            tmem_ld_32x32b_x32(ta, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al[32 * (k & 1) + i]);
+            tmem_st_32x32b_x32(ta, o);
+          }
+          tmem_wait_st();
+        }
+        l = l * alpha + ls;
+        m_ref = m_new;
         // latent rows past S in the item's last tile (a partial page, pages
         // never loaded) are zeroed so that 0 * garbage cannot reach O; Q K^T
         // of this tile has completed (S was full)
@@ -592,43 +620,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(kBarPFull + pb));
       }
 
-      // -- epilogue: this thread's lanes hold latent columns 128 a + 32 q + lane
-      // of chunks a = 2 kh, 2 kh + 1, for all packed rows (the columns)
+      // -- epilogue: this thread's lane holds latent column 128 a + 32 q + lane
+      // of chunks a = 2 kh, 2 kh + 1, for all packed rows (the TMEM columns).
+      // Every piece leaves (m, l) and its unnormalised O^T in groups of four
+      // rows, partial[piece][row / 4][column][row % 4] (mla_acc_index): a
+      // lane's four rows are one 16-byte store and a warp's stores of a group
+      // are 512 contiguous bytes. The merge kernel writes the output rows.
       wait_or_fail(kBarOFull, piece_idx & 1, 4096);
       tc_fence_after();
       const float lrow = exchange(l, false);
-      float* lr = row_vals + (round & 1) * 64;
-      ++round;
-      if (kh == 0 && sub == 0) lr[r] = lrow;
-      named_bar(kBarEpilogue, kSoftmaxThreads);
       ++piece_idx;
       if (!ok) continue;
       const int64_t piece = (int64_t)pc.j + c;
+      const int ldr = mla_row_stride(p.max_rows);
 #pragma unroll 1
       for (int k = 0; k < 4; ++k) {
         const int a = 2 * kh + (k >> 1);
-        const int col = 128 * a + 32 * q + lane;
         const int r0 = 32 * (k & 1);
         if (r0 >= pc.R) continue;  // warp-uniform
         uint32_t o[32];
         tmem_ld_32x32b_x32(tmem + lane_base + kColO + 64 * a + r0, o);
         tmem_wait_ld();
+        const int col = 128 * a + 32 * q + lane;
+        const int nrow = ldr - r0 < 32 ? ldr - r0 : 32;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int rr = r0 + i;
-          if (rr >= pc.R) break;
-          const int t = rr / G, g = rr - t * G;
-          if (pc.direct) {
-            const float den = lr[rr];
-            const float inv = den > 0.f ? vd / den : 0.f;
-            p.out[(int64_t)(pc.q0 + t) * p.o_s0 + (int64_t)g * p.o_s1 + col] =
-                float_to_bf16_bits(__uint_as_float(o[i]) * inv);
-          } else {
-            p.ws_acc[(piece * p.max_rows + rr) * kMlaNope + col] = __uint_as_float(o[i]);
-          }
-        }
+        for (int w = 0; w < 8; ++w)
+          if (4 * w < nrow)
+            *reinterpret_cast<float4*>(p.ws_acc + mla_acc_index(piece, r0 + 4 * w, col, ldr)) =
+                make_float4(__uint_as_float(o[4 * w]), __uint_as_float(o[4 * w + 1]),
+                            __uint_as_float(o[4 * w + 2]), __uint_as_float(o[4 * w + 3]));
       }
-      if (row_ok && !pc.direct && kh == 0 && sub == 0) {
+      if (row_ok && kh == 0 && sub == 0) {
         p.ws_ml[(piece * p.max_rows + r) * 2 + 0] = (m_ref == -INFINITY) ? -INFINITY : m_ref - kPShift;
         p.ws_ml[(piece * p.max_rows + r) * 2 + 1] = lrow;
       }

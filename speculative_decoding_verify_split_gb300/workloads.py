@@ -353,6 +353,10 @@ class MlaWorkload:
         return int(self.q.shape[1])
 
     @property
+    def num_kv_heads(self) -> int:
+        return 1
+
+    @property
     def kv_dtype(self) -> str:
         return FP8 if self.kv_cache.dtype == torch.float8_e4m3fn else BF16
 

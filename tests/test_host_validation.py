@@ -159,7 +159,7 @@ def _mla_status(w, **over):
     ds = [va.desc(a[k]) for k in ("q", "kv", "bt", "cu", "su", "kd", "vd", "out")]
     r = [None if d is None else ctypes.byref(d) for d in ds]
     return va.library().verify_attn_mla(r[0], r[1], r[2], r[3], r[4], int(a["mq"]), int(a["mk"]),
-                                        0.1, r[5], r[6], r[7], None, 0, 0, None)
+                                        0.1, r[5], r[6], r[7], None, 0, 0, None, None)
 
 
 @pytest.fixture(scope="module")
