@@ -41,9 +41,9 @@
 //              named barrier. They also stage Q (the next item's during the
 //              current item's last tile) and write the epilogue.
 // Online softmax in log2 units keeps a per-row reference m_ref and computes
-// P = 2^(s - m_ref + 6) <= 2^8.5; m_ref moves (and O, l are rescaled in
-// TMEM) only when a tile's max exceeds it by more than 2.5, so rescales are
-// rare. The VAR instantiation adds the generic attention's variants (sliding
+// P = 2^(s - m_ref + 6) <= 2^8.8; m_ref moves (and O, l are rescaled in
+// TMEM) only when a tile's max exceeds it by more than 2.8, and a row's first
+// m_ref sits 4 above its first tile's max, so rescales are rare. The VAR instantiation adds the generic attention's variants (sliding
 // window, logit soft cap, sinks). Waits are bounded in time and warp-uniform:
 // on a timeout the kernel sets the workspace status word, stops issuing
 // work, drains and frees its TMEM.
@@ -127,7 +127,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kPShift = 6.f;      // P = 2^(s - m_ref + kPShift)
 constexpr float kHeadroom = 1.f;    // m_ref = tile max + kHeadroom when it moves
-constexpr float kOvershoot = 2.5f;  // move only if the tile max > m_ref + kOvershoot
+constexpr float kHeadroomFirst = 4.f;  // ... and + kHeadroomFirst for a row's first reference
+constexpr float kOvershoot = 2.8f;  // move only if the tile max > m_ref + kOvershoot (P <= 2^8.8 < 448)
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -648,7 +649,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
 
         const bool need = tmax > m_ref + kOvershoot;
-        const float m_new = need ? tmax + kHeadroom : m_ref;
+        // A row's first reference takes more headroom: its running max keeps
+        // growing over the next tiles (by ~sd * (sqrt(2 ln n) - sqrt(2 ln T))),
+        // and every later move waits for P V of the previous tile.
+        const float m_new = need ? tmax + (m_ref == -INFINITY ? kHeadroomFirst : kHeadroom) : m_ref;
         const bool rescale = need && (m_ref != -INFINITY) && (cur > first);
         const float alpha = rescale ? ex2(m_ref - m_new) : 1.f;
         if (__any_sync(0xffffffffu, rescale)) {
