@@ -5,9 +5,9 @@ tolerance (atol = rtol = 1e-2 on the bf16 output):
 * the small workload whole, at the library's split and at forced split
   counts from 1 CTA to more CTAs than tiles;
 * seeded random batches: ragged lengths (0, 1, page and tile edges), 1-4
-  draft tokens, 4 / 8 / 16 heads, descales, forced splits;
-* bit-identical results run to run and under a relabelling of the physical
-  pages;
+  draft tokens, 1 to 64 heads, descales, forced splits;
+* bit-identical results run to run, under a relabelling of the physical
+  pages, and between CUDA-graph replays and eager calls;
 * the long-context workload (16 sequences of 64K-128K keys), its shortest
   and longest sequences, in the launch configuration the benchmark times."""
 import numpy as np
@@ -71,11 +71,11 @@ def test_run_to_run_and_page_relabelling_bit_identical():
     compare(a, mla_oracle_from_torch(w))
 
 
-@pytest.mark.parametrize("seed", range(10))
+@pytest.mark.parametrize("seed", range(14))
 def test_random_shapes(seed):
     g = torch.Generator().manual_seed(500 + seed)
     B = int(torch.randint(1, 7, (1,), generator=g))
-    hq = [4, 8, 16][int(torch.randint(0, 3, (1,), generator=g))]
+    hq = [1, 2, 4, 8, 16, 32, 64][int(torch.randint(0, 7, (1,), generator=g))]
     qmax = min(4, 64 // hq)
     q_lens = torch.randint(1, qmax + 1, (B,), generator=g).tolist()
     choices = [0, 1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 500, 1000, 2500]
@@ -117,3 +117,43 @@ def test_errors():
         va.verify_attn_mla(w.q, w.kv_cache.to(torch.bfloat16), w.block_table, w.cu_seqlens_q,
                            w.seqused_k, w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale)
     assert e.value.status == 4
+
+
+@pytest.mark.parametrize("hq,q_lens", [(64, [1, 1, 1]), (32, [2, 1]), (1, [4, 3, 1]), (2, [1, 4])])
+def test_head_counts(hq, q_lens):
+    """Group sizes from 1 to 64 query heads on the one latent (rows = heads x
+    draft tokens <= 64), at the library's split and split over many CTAs."""
+    w = make_mla_workload(q_lens, [700, 129, 2000][:len(q_lens)], hq, seed=50 + hq, k_descale=1.2,
+                          v_descale=0.9)
+    ref = mla_oracle_from_torch(w)
+    for splits in (0, 37):
+        compare(run(w.to("cuda"), splits), ref)
+
+
+def test_cuda_graph_replay_bit_identical():
+    """With a caller workspace the call allocates and synchronises nothing, so
+    it can be captured; replays on new query values match eager calls bit
+    for bit."""
+    w = make_mla_workload([4, 2, 3], [3000, 200, 1100], 16, seed=61).to("cuda")
+    n = va.mla_workspace_size(w.q, w.seqused_k, w.max_seqlen_q, w.max_seqlen_k)
+    ws = torch.zeros(n + 256, dtype=torch.uint8, device="cuda")
+    out = torch.empty(w.q.shape[0], w.q.shape[1], va.MLA_NOPE, dtype=torch.bfloat16, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        va.run_mla_workload(w, out=out, workspace=ws, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        va.run_mla_workload(w, out=out, workspace=ws, stream=torch.cuda.current_stream())
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    for _ in range(3):
+        w.q.copy_(torch.randn(w.q.shape, generator=gen, device="cuda").to(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        got = out.clone()
+        ref = torch.empty_like(out)
+        va.run_mla_workload(w, out=ref, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
