@@ -481,3 +481,31 @@ def named_mla_workload(name: str, seed: int = 0, value_device: str = "cpu") -> M
     return make_mla_workload(st["q_lens"], st["kv_lens"], st["Hq"], FP8, seed=seed,
                              k_descale=st["descale"], value_device=value_device, name=name,
                              _gen=st["gen"])
+
+
+def split_kv_shards(w: Workload, n: int, seed: int = 0):
+    """Input construction for the sharded (context-parallel) path: each
+    sequence's keys cut into n contiguous, page-aligned shards of random sizes
+    (some may be empty). Returns a list of n (block_table, seqused_k,
+    kv_extent) triples on the workload's device: shard i of sequence b holds
+    the keys [o, o + S_i) of the sequence through its own table rows (the
+    sequence's pages [o / 16, ...)), and kv_extent = S_b - o."""
+    g = torch.Generator().manual_seed(seed)
+    bt = w.block_table.cpu()
+    B, W = bt.shape
+    dev = w.block_table.device
+    tables = [torch.full((B, W), max(w.poison_page, 0), dtype=torch.int32) for _ in range(n)]
+    used = [torch.zeros(B, dtype=torch.int32) for _ in range(n)]
+    ext = [torch.zeros(B, dtype=torch.int32) for _ in range(n)]
+    for b, S in enumerate(w.kv_lens):
+        pages = (S + PAGE_SIZE - 1) // PAGE_SIZE
+        cuts = sorted(torch.randint(0, pages + 1, (n - 1,), generator=g).tolist()) if n > 1 else []
+        bounds = [0] + [c * PAGE_SIZE for c in cuts] + [S]
+        for i in range(n):
+            lo, hi = min(bounds[i], S), min(bounds[i + 1], S)
+            hi = max(hi, lo)
+            p0, p1 = lo // PAGE_SIZE, (hi + PAGE_SIZE - 1) // PAGE_SIZE
+            tables[i][b, :p1 - p0] = bt[b, p0:p1]
+            used[i][b] = hi - lo
+            ext[i][b] = S - lo
+    return [(t.to(dev), u.to(dev), e.to(dev)) for t, u, e in zip(tables, used, ext)]
