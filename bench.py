@@ -292,6 +292,66 @@ def draft_extend_timing(va, w, stream, torch, K):
                     "(20 builder launches, or 4 builder+attention calls, per graph)"}
 
 
+def shard_timing(va, w, torch, K):
+    """The same workload with each sequence's keys cut into two page-aligned
+    shards (verify_attn_partial twice, then verify_attn_merge_partials), from
+    CUDA-graph replays so that host marshalling is not in the figure. Also the
+    shard merge alone."""
+    from speculative_decoding_verify_split_gb300.workloads import split_kv_shards
+    shards = split_kv_shards(w, 2, seed=0)
+    width = w.block_table.shape[1]
+    o = [torch.empty(w.q.shape, dtype=torch.float32, device=w.q.device) for _ in shards]
+    lse = [torch.empty(w.q.shape[:2], dtype=torch.float32, device=w.q.device) for _ in shards]
+    out = torch.empty_like(w.q)
+    wss = []
+    for bt, su, ext in shards:
+        n = va.workspace_size(w.q, w.k_cache, su, w.max_seqlen_q, width * 16)
+        wss.append(torch.zeros(n + 256, dtype=torch.uint8, device=w.q.device))
+
+    def partials():
+        for i, (bt, su, ext) in enumerate(shards):
+            va.verify_attn_partial(w.q, w.k_cache, w.v_cache, bt, w.cu_seqlens_q, su, w.max_seqlen_q,
+                                   width * 16, w.softmax_scale, w.k_descale, w.v_descale, kv_extent=ext,
+                                   o=o[i], lse=lse[i], workspace=wss[i],
+                                   stream=torch.cuda.current_stream())
+
+    def merge():
+        va.merge_partials(list(zip(o, lse)), out=out, stream=torch.cuda.current_stream())
+
+    def both():
+        partials()
+        merge()
+
+    res = {}
+    for name, fn, reps in (("two_shards_and_merge", both, 2), ("merge", merge, 20)):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                both()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_rep = max(K // reps, 5)
+        a.record()
+        for _ in range(n_rep):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        res[name] = a.elapsed_time(b) / (n_rep * reps) * 1e3
+    merge_bytes = 2 * (w.q.numel() * 4 + w.q.shape[0] * w.q.shape[1] * 4) + w.q.numel() * 2
+    return {"two_shards_and_merge_us": round(res["two_shards_and_merge"], 2),
+            "shard_merge_us": round(res["merge"], 2), "shard_merge_bytes": merge_bytes,
+            "note": "each sequence's keys cut into two page-aligned shards (verify_attn_partial on each, "
+                    "then verify_attn_merge_partials); device time from CUDA-graph replays"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -434,6 +494,7 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e2e_ms, world, dist if world > 1 else None, dev)
 
     draft = None if mla else draft_extend_timing(va, w, stream, torch, min(K, 200))
+    shards = None if mla else shard_timing(va, w, torch, min(K, 200))
 
     peak, peak_src = peak_hbm()
     achieved = alg / (main_ms / 1e3) / 1e9
@@ -456,6 +517,7 @@ def run_ours(args):
                 "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": 2 * K,
         **({} if draft is None else {"draft_extend": draft}),
+        **({} if shards is None else {"kv_shards": shards}),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

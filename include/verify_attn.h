@@ -364,6 +364,54 @@ va_status verify_attn_mla(const va_tensor* q, const va_tensor* kv_cache, const v
 size_t verify_attn_mla_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_seqlen_q,
                                       int32_t max_seqlen_k, int32_t num_splits);
 
+/*
+ * verify_attn_partial - verify attention over one shard of each sequence's
+ * keys, for splitting a sequence's KV over several parts (context
+ * parallelism across ranks; a shared prefix in one cache and per-sequence
+ * suffixes in another). The pages name a decode-context-parallel degree
+ * (sglang PR 34517 digest, attn_dcp_size) and merge split-KV segments by log-sum-exp
+ * (sglang PR 36330 digest, "reduce segments"); this entry computes one
+ * shard's result and verify_attn_merge_partials combines shards. The
+ * exchange of shard results between GPUs is the caller's.
+ *
+ * A shard holds the keys of global positions [o_b, o_b + S_b) of sequence b,
+ * reached through its own block_table row (S_b = seqused_k[b]). With
+ * E_b = kv_extent[b] = (the sequence's total keys) - o_b, draft token t of L
+ * sees the shard's local keys j <= E_b - L + t (and j < S_b). NULL kv_extent
+ * means E_b = S_b, the last shard (or the whole sequence).
+ *
+ * Arguments as verify_attn_ex, except:
+ *  kv_extent  [B] int32 (nullable), contiguous; values below S_b count as S_b.
+ *  o          [total_q, Hq, 256] fp32, written: the shard's attention output,
+ *             normalised over the shard's visible keys, times v_descale.
+ *  lse        [total_q, Hq] fp32, written: ln(sum over the visible keys of
+ *             exp(softmax_scale * k_descale * q . k)); -inf (and o = 0) for a
+ *             row that sees no key of the shard.
+ *  workspace  as verify_attn_ex; NULL uses the library's per-device workspace.
+ * The variants of verify_attn_opt are not available here. Errors as
+ * verify_attn_ex (o and lse: VA_ERR_DTYPE unless fp32, VA_ERR_SHAPE, and
+ * VA_ERR_LAYOUT for o rows that are not 16-byte aligned).
+ */
+va_status verify_attn_partial(const va_tensor* q, const va_tensor* k_cache, const va_tensor* v_cache,
+                              const va_tensor* block_table, const va_tensor* cu_seqlens_q,
+                              const va_tensor* seqused_k, const va_tensor* kv_extent,
+                              int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
+                              const va_tensor* k_descale, const va_tensor* v_descale, va_tensor* o,
+                              va_tensor* lse, void* workspace, size_t workspace_bytes,
+                              int32_t num_splits, void* stream);
+
+/*
+ * verify_attn_merge_partials - combines n (1..16) shard results of
+ * verify_attn_partial: out = sum_i exp(lse_i - LSE) o_i with
+ * LSE = ln sum_i exp(lse_i), rounded to bf16; a row whose lse are all -inf
+ * is 0. o_parts and lse_parts are HOST arrays of n descriptors (fp32
+ * [total_q, Hq, 256] and [total_q, Hq], device memory); out is bf16
+ * [total_q, Hq, 256]. One launch on stream. Returns VA_ERR_UNSUPPORTED for n
+ * outside 1..16, and the usual shape / dtype / layout errors.
+ */
+va_status verify_attn_merge_partials(int32_t n, const va_tensor* o_parts, const va_tensor* lse_parts,
+                                     va_tensor* out, void* stream);
+
 /* Static, NUL-terminated name of a status code. */
 const char* verify_attn_status_string(int32_t status);
 

@@ -30,7 +30,7 @@ _DTYPES = {torch.bfloat16: VA_BF16, torch.float8_e4m3fn: VA_FP8_E4M3,
 EXPORTS = ("verify_attn", "verify_attn_ex", "verify_attn_check", "verify_attn_plan",
            "verify_attn_workspace_size", "verify_attn_status_string", "verify_attn_noalloc",
            "verify_attn_block_table_from_indptr", "verify_attn_opt", "verify_attn_mla",
-           "verify_attn_mla_workspace_size")
+           "verify_attn_mla_workspace_size", "verify_attn_partial", "verify_attn_merge_partials")
 
 # Absorbed-MLA latent cache: row = [latent (MLA_NOPE) | rope key (MLA_PE)].
 MLA_NOPE, MLA_PE = 512, 64
@@ -105,6 +105,12 @@ def _lib():
         lib.verify_attn_mla.restype = ctypes.c_int32
         lib.verify_attn_mla_workspace_size.argtypes = [ctypes.c_int32] * 5
         lib.verify_attn_mla_workspace_size.restype = ctypes.c_size_t
+        lib.verify_attn_partial.argtypes = [P] * 7 + [ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                                      P, P, P, P, ctypes.c_void_p, ctypes.c_size_t,
+                                                      ctypes.c_int32, ctypes.c_void_p]
+        lib.verify_attn_partial.restype = ctypes.c_int32
+        lib.verify_attn_merge_partials.argtypes = [ctypes.c_int32, P, P, P, ctypes.c_void_p]
+        lib.verify_attn_merge_partials.restype = ctypes.c_int32
         lib.verify_attn_status_string.argtypes = [ctypes.c_int32]
         lib.verify_attn_status_string.restype = ctypes.c_char_p
         _LIB = lib
@@ -400,3 +406,52 @@ def run_mla_workload(w, out=None, workspace=None, num_splits=0, stream=None,
                            w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale, w.k_descale,
                            w.v_descale, out=out, workspace=workspace, num_splits=num_splits,
                            stream=stream, event_after_main=event_after_main)
+
+
+def verify_attn_partial(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q: int,
+                        max_seqlen_k: int, softmax_scale: float, k_descale=None, v_descale=None,
+                        kv_extent=None, o=None, lse=None, workspace: Optional[torch.Tensor] = None,
+                        num_splits: int = 0, stream=None):
+    """One shard of each sequence's keys (see include/verify_attn.h): returns
+    (o [total_q, Hq, 256] fp32, lse [total_q, Hq] fp32). ``kv_extent`` [B]
+    int32: the sequence's total keys minus the shard's first key position
+    (None: the shard ends the sequence)."""
+    if o is None:
+        o = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    ds = [desc(x) for x in (q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, kv_extent,
+                            k_descale, v_descale, o, lse)]
+    r = [_ref(d) for d in ds]
+    if workspace is None:
+        addr, nbytes = 0, 0
+    else:
+        a = workspace.data_ptr()
+        off = (-a) % 256
+        addr, nbytes = a + off, workspace.numel() - off
+    with torch.cuda.device(q.device):
+        s = _lib().verify_attn_partial(r[0], r[1], r[2], r[3], r[4], r[5], r[6], int(max_seqlen_q),
+                                       int(max_seqlen_k), float(softmax_scale), r[7], r[8], r[9],
+                                       r[10], ctypes.c_void_p(addr), nbytes, int(num_splits),
+                                       ctypes.c_void_p(_stream_handle(stream, q.device)))
+    if s != VA_OK:
+        raise VerifyAttnError(s, "verify_attn_partial")
+    return o, lse
+
+
+def merge_partials(parts, out=None, stream=None):
+    """Log-sum-exp merge of shard results: ``parts`` is a list of (o, lse)
+    pairs from verify_attn_partial; returns out [total_q, Hq, 256] bf16."""
+    o0 = parts[0][0]
+    if out is None:
+        out = torch.empty(o0.shape, dtype=torch.bfloat16, device=o0.device)
+    n = len(parts)
+    oa = (VaTensor * n)(*[desc(o) for o, _ in parts])
+    la = (VaTensor * n)(*[desc(l) for _, l in parts])
+    d = desc(out)
+    with torch.cuda.device(o0.device):
+        s = _lib().verify_attn_merge_partials(n, oa, la, _ref(d),
+                                              ctypes.c_void_p(_stream_handle(stream, o0.device)))
+    if s != VA_OK:
+        raise VerifyAttnError(s, "verify_attn_merge_partials")
+    return out

@@ -251,7 +251,8 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
                  const va_tensor* cu, const va_tensor* su, int32_t max_q, int32_t max_k,
                  float scale, const va_tensor* kd, const va_tensor* vd, va_tensor* out,
                  const Shapes& sh, const va_plan& plan, void* ws, size_t ws_bytes,
-                 cudaEvent_t ev_mid, cudaStream_t stream, const va_options* opts) {
+                 cudaEvent_t ev_mid, cudaStream_t stream, const va_options* opts,
+                 const PartialOut* part) {
   if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;  // no output rows
   if ((size_t)plan.workspace_bytes > ws_bytes || !ws) return VA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return VA_ERR_WORKSPACE;
@@ -298,6 +299,16 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
   p.num_work = plan.num_work;
   p.piece_cost = kPieceCostTiles;
   p.dv = kHeadDim;
+  if (part) {
+    p.partial = 1;
+    p.kv_extent = part->kv_extent ? static_cast<const int32_t*>(part->kv_extent->data) : nullptr;
+    p.o_part = static_cast<float*>(part->o->data);
+    p.op_s0 = part->o->stride[0];
+    p.op_s1 = part->o->stride[1];
+    p.lse_part = static_cast<float*>(part->lse->data);
+    p.lse_s0 = part->lse->stride[0];
+    p.lse_s1 = part->lse->stride[1];
+  }
   const WorkspaceLayout lay = workspace_layout(plan.num_work, plan.num_splits, plan.max_rows);
   char* base = static_cast<char*>(ws);
   p.ws_meta = reinterpret_cast<int32_t*>(base + lay.meta_off);
@@ -691,6 +702,118 @@ VA_EXPORT size_t verify_attn_mla_workspace_size(int32_t num_seqs, int32_t num_q_
       VA_OK)
     return 0;
   return (size_t)plan.workspace_bytes;
+}
+
+// ---- one shard of each sequence's keys, and the merge of shards ---------------
+
+// Checks of verify_attn_partial's own arguments (the rest as verify_attn).
+static va_status validate_partial_outputs(const va_tensor* ext, const va_tensor* o,
+                                          const va_tensor* lse, const Shapes& sh) {
+  if (!o || !lse) return VA_ERR_NULL;
+  if (o->dtype != VA_FP32 || lse->dtype != VA_FP32) return VA_ERR_DTYPE;
+  if (!dims_ok(o, 3) || !dims_ok(lse, 2)) return VA_ERR_SHAPE;
+  if (o->shape[0] != sh.total_q || o->shape[1] != sh.hq || o->shape[2] != kHeadDim) return VA_ERR_SHAPE;
+  if (lse->shape[0] != sh.total_q || lse->shape[1] != sh.hq) return VA_ERR_SHAPE;
+  if (!rows_16b(o)) return VA_ERR_LAYOUT;
+  if (sh.total_q > 0 && (!o->data || !lse->data)) return VA_ERR_NULL;
+  if ((o->data && !aligned16(o->data)) || (lse->data && (reinterpret_cast<uintptr_t>(lse->data) & 3u)))
+    return VA_ERR_LAYOUT;
+  if (ext) {
+    if (ext->dtype != VA_INT32) return VA_ERR_DTYPE;
+    if (!dims_ok(ext, 1) || ext->shape[0] != sh.num_seqs) return VA_ERR_SHAPE;
+    if (sh.num_seqs > 1 && ext->stride[0] != 1) return VA_ERR_LAYOUT;
+    if (sh.num_seqs > 0 && !ext->data) return VA_ERR_NULL;
+  }
+  return VA_OK;
+}
+
+VA_EXPORT va_status verify_attn_partial(const va_tensor* q, const va_tensor* k_cache,
+                                        const va_tensor* v_cache, const va_tensor* block_table,
+                                        const va_tensor* cu_seqlens_q, const va_tensor* seqused_k,
+                                        const va_tensor* kv_extent, int32_t max_seqlen_q,
+                                        int32_t max_seqlen_k, float softmax_scale,
+                                        const va_tensor* k_descale, const va_tensor* v_descale,
+                                        va_tensor* o, va_tensor* lse, void* workspace,
+                                        size_t workspace_bytes, int32_t num_splits, void* stream) {
+  // q stands in for the bf16 out that validate() checks: the shard writes o and lse
+  Shapes sh;
+  va_status s = validate(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
+                         max_seqlen_k, k_descale, v_descale, q, &sh);
+  if (s != VA_OK) return s;
+  s = validate_partial_outputs(kv_extent, o, lse, sh);
+  if (s != VA_OK) return s;
+  if (num_splits < 0) return VA_ERR_UNSUPPORTED;
+  std::unique_lock<std::mutex> lk(g_mu);
+  DeviceState* st = nullptr;
+  s = device_state(&st);
+  if (s != VA_OK) return s;
+  va_plan plan;
+  s = make_plan(sh.num_seqs, sh.hkv, sh.hq, max_seqlen_q, max_seqlen_k, sh.kv_dtype, st->sms,
+                num_splits, &plan);
+  if (s != VA_OK) return s;
+  if (!workspace) {
+    if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;
+    if ((size_t)plan.workspace_bytes > st->ws_bytes) {
+      if (st->ws) cudaFree(st->ws);
+      st->ws = nullptr;
+      st->ws_bytes = 0;
+      if (cudaMalloc(&st->ws, (size_t)plan.workspace_bytes) != cudaSuccess) {
+        st->ws = nullptr;
+        return VA_ERR_CUDA;
+      }
+      if (cudaMemset(st->ws, 0, (size_t)plan.workspace_bytes) != cudaSuccess) return VA_ERR_CUDA;
+      st->ws_bytes = (size_t)plan.workspace_bytes;
+    }
+    workspace = st->ws;
+    workspace_bytes = st->ws_bytes;
+  } else {
+    lk.unlock();
+  }
+  const PartialOut part{kv_extent, o, lse};
+  va_tensor unused_out = *q;  // no piece writes bf16 rows in partial mode
+  return launch(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
+                max_seqlen_k, softmax_scale, k_descale, v_descale, &unused_out, sh, plan, workspace,
+                workspace_bytes, nullptr, static_cast<cudaStream_t>(stream), nullptr, &part);
+}
+
+VA_EXPORT va_status verify_attn_merge_partials(int32_t n, const va_tensor* o_parts,
+                                               const va_tensor* lse_parts, va_tensor* out,
+                                               void* stream) {
+  if (!o_parts || !lse_parts || !out) return VA_ERR_NULL;
+  if (n < 1 || n > kMaxShards) return VA_ERR_UNSUPPORTED;
+  if (out->dtype != VA_BF16) return VA_ERR_DTYPE;
+  if (!dims_ok(out, 3) || out->shape[2] != kHeadDim) return VA_ERR_SHAPE;
+  if (!rows_16b(out)) return VA_ERR_LAYOUT;
+  if (out->shape[0] > INT32_MAX || out->shape[1] > INT32_MAX) return VA_ERR_UNSUPPORTED;
+  ShardMergeParams m;
+  std::memset(&m, 0, sizeof(m));
+  m.n = n;
+  m.total_q = (int32_t)out->shape[0];
+  m.hq = (int32_t)out->shape[1];
+  const bool any = m.total_q > 0 && m.hq > 0;
+  if (any && (!out->data || !aligned16(out->data))) return out->data ? VA_ERR_LAYOUT : VA_ERR_NULL;
+  m.out = static_cast<uint16_t*>(out->data);
+  m.out_s0 = out->stride[0];
+  m.out_s1 = out->stride[1];
+  for (int i = 0; i < n; ++i) {
+    const va_tensor* o = &o_parts[i];
+    const va_tensor* l = &lse_parts[i];
+    if (o->dtype != VA_FP32 || l->dtype != VA_FP32) return VA_ERR_DTYPE;
+    if (!dims_ok(o, 3) || !dims_ok(l, 2)) return VA_ERR_SHAPE;
+    for (int d = 0; d < 3; ++d)
+      if (o->shape[d] != out->shape[d]) return VA_ERR_SHAPE;
+    if (l->shape[0] != out->shape[0] || l->shape[1] != out->shape[1]) return VA_ERR_SHAPE;
+    if (!rows_16b(o)) return VA_ERR_LAYOUT;
+    if (any && (!o->data || !l->data)) return VA_ERR_NULL;
+    if (any && (!aligned16(o->data) || (reinterpret_cast<uintptr_t>(l->data) & 3u))) return VA_ERR_LAYOUT;
+    m.o[i] = static_cast<const float*>(o->data);
+    m.o_s0[i] = o->stride[0];
+    m.o_s1[i] = o->stride[1];
+    m.lse[i] = static_cast<const float*>(l->data);
+    m.lse_s0[i] = l->stride[0];
+    m.lse_s1[i] = l->stride[1];
+  }
+  return launch_merge_shards(m, static_cast<cudaStream_t>(stream)) == cudaSuccess ? VA_OK : VA_ERR_CUDA;
 }
 
 VA_EXPORT const char* verify_attn_status_string(int32_t status) {

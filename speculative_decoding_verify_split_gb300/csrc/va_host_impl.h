@@ -30,13 +30,22 @@ va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t m
 // Checks the variant options against the shapes (NULL = all off).
 va_status validate_options(const va_options* opts, const Shapes& sh);
 
+// A shard's outputs (verify_attn_partial): fp32 o, natural-log lse, and the
+// optional per-sequence causal extent.
+struct PartialOut {
+  const va_tensor* kv_extent;  // nullable
+  va_tensor* o;
+  va_tensor* lse;
+};
+
 // Launches the main and merge kernels with the given workspace and options
-// (NULL = all off).
+// (NULL = all off); with `part`, the merge writes the shard's o and lse.
 va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, const va_tensor* bt,
                  const va_tensor* cu, const va_tensor* su, int32_t max_q, int32_t max_k,
                  float scale, const va_tensor* kd, const va_tensor* vd, va_tensor* out,
                  const Shapes& sh, const va_plan& plan, void* ws, size_t ws_bytes,
-                 cudaEvent_t ev_mid, cudaStream_t stream, const va_options* opts = nullptr);
+                 cudaEvent_t ev_mid, cudaStream_t stream, const va_options* opts = nullptr,
+                 const PartialOut* part = nullptr);
 
 // SM count of the current device (initialises the per-device state once).
 va_status current_device_sms(int* sms);

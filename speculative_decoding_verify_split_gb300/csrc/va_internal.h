@@ -53,6 +53,17 @@ struct Params {
   int32_t window_left;     // -1: none; else position i sees keys [i - window_left, i]
   float softcap_log2;      // 0: none; else softcap * log2(e): x -> c tanh(x / c) in log2 units
   const float* sinks;      // nullable, [hq]: per-head sink logits (natural log)
+  // One shard of each sequence's keys (verify_attn_partial): with kv_extent,
+  // draft token t of sequence b sees the shard's local keys j <= extent_b - L + t
+  // (extent_b = the sequence's total keys - the shard's first key position);
+  // with partial, every item goes through the merge, which writes o (fp32,
+  // normalised) and lse (natural log) instead of out.
+  const int32_t* kv_extent;  // nullable: extent = seqused_k
+  int32_t partial;
+  float* o_part;             // [total_q, hq, 256]
+  int64_t op_s0, op_s1;
+  float* lse_part;           // [total_q, hq]
+  int64_t lse_s0, lse_s1;
 
   // Split-KV decomposition: one stream of key tiles over all work items
   // j = b * hkv + kvh, cut into num_splits equal ranges (one per CTA). Each
@@ -99,6 +110,19 @@ constexpr int kTcTileKeysBf16 = 64;  // keys per tile, BF16 KV
 constexpr int kPieceCostTiles = 4;
 
 cudaError_t launch_merge(const Params& p, cudaStream_t stream);
+
+// Log-sum-exp merge of shard results (verify_attn_merge_partials).
+constexpr int kMaxShards = 16;
+struct ShardMergeParams {
+  int32_t n, total_q, hq;
+  const float* o[kMaxShards];
+  int64_t o_s0[kMaxShards], o_s1[kMaxShards];
+  const float* lse[kMaxShards];
+  int64_t lse_s0[kMaxShards], lse_s1[kMaxShards];
+  uint16_t* out;  // bf16 [total_q, hq, 256]
+  int64_t out_s0, out_s1;
+};
+cudaError_t launch_merge_shards(const ShardMergeParams& m, cudaStream_t stream);
 
 // Block table from the flat token-slot form (va_pagetable.cu). Status bits:
 constexpr int32_t kBtBadPage = 1;     // a page's slots are not one aligned page in order

@@ -565,7 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // -- key tiles
       float m_ref = -INFINITY;
       float l = 0.f;
-      const int vis_end = pc.S - pc.L + tq;  // last visible key of this row
+      // last visible key of this row: S - L + t, or for a shard of the
+      // sequence's keys E - L + t, never past the shard's own keys
+      const int vis_end = min(pc.E - pc.L + tq, pc.S - 1);
+      const int mask_from = min(pc.E - pc.L, pc.S - 1);  // tiles past this key hold masked keys
       // first visible key of this row (sliding window), and the largest over rows
       const int vis_lo = VAR && p.window_left >= 0 ? pc.S - pc.L + tq - p.window_left : 0;
       const int vis_lo_max = VAR && p.window_left >= 0 ? pc.S - 1 - p.window_left : 0;
@@ -623,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           const int key0 = lt * kT + kKpt * qtr;
-          if (lt * kT + kT - 1 > pc.S - pc.L) {  // tail tile: causal mask
+          if (lt * kT + kT - 1 > mask_from) {  // tail tile: causal mask
 #pragma unroll
             for (int i = 0; i < kKpt; ++i)
               if (key0 + i > vis_end) x[i] = -INFINITY;

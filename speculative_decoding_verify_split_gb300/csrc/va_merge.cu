@@ -28,7 +28,10 @@ constexpr int kMergeThreads = 256;
 constexpr int kSegChunk = 8;
 
 // SINKS: compiled with the attention-sink term. DV: output columns per row.
-template <bool SINKS, int DV>
+// PARTIAL: a shard's result (verify_attn_partial): every item is merged here,
+// also one held by a single CTA, and the row is written as fp32 o and its
+// natural-log lse instead of bf16 out.
+template <bool SINKS, int DV, bool PARTIAL>
 __global__ void __launch_bounds__(kMergeThreads, 4) va_merge_kernel(const Params p) {
   constexpr int kThreadsPerRow = DV / 4;
   constexpr int kRowsPerCta = kMergeThreads / kThreadsPerRow;
@@ -44,17 +47,25 @@ __global__ void __launch_bounds__(kMergeThreads, 4) va_merge_kernel(const Params
   const int t = r / G, g = r - t * G;
   const int q0 = p.cu_q[b];
   uint16_t* dst = p.out + (int64_t)(q0 + t) * p.o_s0 + (int64_t)(kvh * G + g) * p.o_s1 + 4 * col4;
+  // a shard's row: o (fp32) and, from the row's first thread, lse
+  auto put_partial = [&](float4 o, float lse) {
+    *reinterpret_cast<float4*>(p.o_part + (int64_t)(q0 + t) * p.op_s0 + (int64_t)(kvh * G + g) * p.op_s1 + 4 * col4) = o;
+    if (col4 == 0) p.lse_part[(int64_t)(q0 + t) * p.lse_s0 + (int64_t)(kvh * G + g) * p.lse_s1] = lse;
+  };
 
   const int nt = work_tiles(p, j);
   if (nt == 0) {
-    *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
+    if constexpr (PARTIAL)
+      put_partial(make_float4(0.f, 0.f, 0.f, 0.f), -INFINITY);
+    else
+      *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
     return;
   }
   const long long N = p.ws_meta[p.num_work];
   const long long ts = p.ws_meta[j];
   const int c0 = split_of(ts, N, p.num_splits);
   const int c1 = split_of(ts + nt - 1, N, p.num_splits);
-  if (c0 == c1) return;  // one CTA held the whole item and wrote it
+  if (!PARTIAL && c0 == c1) return;  // one CTA held the whole item and wrote it
   const int ns = c1 - c0 + 1;
   // A CTA range can only be empty when there are fewer split units than CTAs;
   // otherwise skip the two 64-bit divisions per segment.
@@ -103,13 +114,22 @@ __global__ void __launch_bounds__(kMergeThreads, 4) va_merge_kernel(const Params
     M = mc;
   }
   if (M == -INFINITY) {
-    *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
+    if constexpr (PARTIAL)
+      put_partial(make_float4(0.f, 0.f, 0.f, 0.f), -INFINITY);
+    else
+      *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
     return;
   }
   if constexpr (SINKS)  // the attention sink's share of the normaliser, once per row
     den += exp2f(p.sinks[kvh * G + g] * 1.4426950408889634f - M);
   const float vd = p.v_descale ? *p.v_descale : 1.0f;
   const float inv = vd / den;
+  if constexpr (PARTIAL) {
+    // the rows' logits are in log2 units: sum 2^x = 2^M den
+    put_partial(make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv),
+                (M + log2f(den)) * 0.6931471805599453f);
+    return;
+  }
   const uint32_t w0 = (uint32_t)float_to_bf16_bits(acc.x * inv) | ((uint32_t)float_to_bf16_bits(acc.y * inv) << 16);
   const uint32_t w1 = (uint32_t)float_to_bf16_bits(acc.z * inv) | ((uint32_t)float_to_bf16_bits(acc.w * inv) << 16);
   *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
@@ -221,6 +241,48 @@ __global__ void __launch_bounds__(kMlaNope, 2) va_merge_mla_kernel(const Params 
     if (i < nrow) *dst(i) = float_to_bf16_bits(acc[i] * s_sc[i]);
 }
 
+// Log-sum-exp merge of shard results (verify_attn_merge_partials):
+// out = sum_i exp(lse_i - LSE) o_i, LSE = ln sum_i exp(lse_i), as bf16; rows
+// whose lse are all -inf are 0. 64 threads per row, one float4 of the 256
+// columns each; the shards' loads go out together.
+__global__ void __launch_bounds__(kMergeThreads) va_merge_shards_kernel(const ShardMergeParams m) {
+  constexpr int kThreadsPerRow = kHeadDim / 4;
+  constexpr int kRowsPerCta = kMergeThreads / kThreadsPerRow;
+  const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + threadIdx.x / kThreadsPerRow;
+  const int col4 = threadIdx.x % kThreadsPerRow;
+  if (row >= (int64_t)m.total_q * m.hq) return;
+  const int t = (int)(row / m.hq), h = (int)(row - (int64_t)t * m.hq);
+  float lse[kMaxShards];
+  float M = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kMaxShards; ++i) {
+    lse[i] = i < m.n ? m.lse[i][(int64_t)t * m.lse_s0[i] + (int64_t)h * m.lse_s1[i]] : -INFINITY;
+    M = fmaxf(M, lse[i]);
+  }
+  uint16_t* dst = m.out + (int64_t)t * m.out_s0 + (int64_t)h * m.out_s1 + 4 * col4;
+  if (M == -INFINITY) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
+    return;
+  }
+  float den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < kMaxShards; ++i) {
+    if (i >= m.n || lse[i] == -INFINITY) continue;  // a shard with no visible key is never read
+    const float w = __expf(lse[i] - M);
+    const float4 o = *reinterpret_cast<const float4*>(m.o[i] + (int64_t)t * m.o_s0[i] + (int64_t)h * m.o_s1[i] + 4 * col4);
+    den += w;
+    acc.x = fmaf(w, o.x, acc.x);
+    acc.y = fmaf(w, o.y, acc.y);
+    acc.z = fmaf(w, o.z, acc.z);
+    acc.w = fmaf(w, o.w, acc.w);
+  }
+  const float inv = 1.f / den;
+  *reinterpret_cast<uint2*>(dst) =
+      make_uint2((uint32_t)float_to_bf16_bits(acc.x * inv) | ((uint32_t)float_to_bf16_bits(acc.y * inv) << 16),
+                 (uint32_t)float_to_bf16_bits(acc.z * inv) | ((uint32_t)float_to_bf16_bits(acc.w * inv) << 16));
+}
+
 }  // namespace
 
 cudaError_t launch_merge(const Params& p, cudaStream_t stream) {
@@ -249,8 +311,21 @@ cudaError_t launch_merge(const Params& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return p.sinks ? cudaLaunchKernelEx(&cfg, va_merge_kernel<true, kHeadDim>, p)
-                 : cudaLaunchKernelEx(&cfg, va_merge_kernel<false, kHeadDim>, p);
+  if (p.partial) return cudaLaunchKernelEx(&cfg, va_merge_kernel<false, kHeadDim, true>, p);
+  return p.sinks ? cudaLaunchKernelEx(&cfg, va_merge_kernel<true, kHeadDim, false>, p)
+                 : cudaLaunchKernelEx(&cfg, va_merge_kernel<false, kHeadDim, false>, p);
+}
+
+}  // namespace va
+
+namespace va {
+
+cudaError_t launch_merge_shards(const ShardMergeParams& m, cudaStream_t stream) {
+  const int64_t rows = (int64_t)m.total_q * m.hq;
+  if (rows == 0) return cudaSuccess;
+  constexpr int kRowsPerCta = kMergeThreads / (kHeadDim / 4);
+  va_merge_shards_kernel<<<(unsigned)((rows + kRowsPerCta - 1) / kRowsPerCta), kMergeThreads, 0, stream>>>(m);
+  return cudaGetLastError();
 }
 
 }  // namespace va

@@ -197,6 +197,7 @@ __device__ long long locate_work(const Params& p, int c, long long* scratch, int
 // within the sequence: the item's tiles are [tb, nt), this CTA's [lt0, lt1).
 struct Piece {
   int j, b, kvh, S, L, q0, R, nt, tb, lt0, lt1;
+  int E;  // the causal extent: S, or the shard's kv_extent (>= S)
   bool direct;
 };
 
@@ -215,13 +216,18 @@ __device__ __forceinline__ bool next_piece(const Params& p, long long t0, long l
     pc.kvh = j - pc.b * p.hkv;
     pc.S = seq_kv_len(p, pc.b);
     pc.L = seq_q_len(p, pc.b);
+    pc.E = pc.S;
+    if (p.kv_extent) {
+      const int e = p.kv_extent[pc.b];
+      pc.E = e > pc.S ? e : pc.S;
+    }
     pc.q0 = p.cu_q[pc.b];
     pc.R = p.group * pc.L;
     pc.tb = first_tile(p, pc.S, pc.L);
     pc.nt = pc.tb + nt;
     pc.lt0 = pc.tb + (int)((t0 > ts ? t0 : ts) - ts);
     pc.lt1 = pc.tb + (int)((t1 < ts + nt ? t1 : ts + nt) - ts);
-    pc.direct = (pc.lt0 == pc.tb && pc.lt1 == pc.nt);
+    pc.direct = !p.partial && (pc.lt0 == pc.tb && pc.lt1 == pc.nt);
     ts += work_cost(p, nt);  // the next item's first tile follows its start-up units
     ++j;
     return true;
