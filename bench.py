@@ -352,6 +352,51 @@ def shard_timing(va, w, torch, K):
                     "then verify_attn_merge_partials); device time from CUDA-graph replays"}
 
 
+def variant_timing(va, w, torch, K):
+    """The generic attention's variants on the same workload (verify_attn_opt
+    with a caller workspace): a 4096-key sliding window, a logit soft cap of
+    30, per-head sinks, and all three, from CUDA-graph replays."""
+    hq = w.q.shape[1]
+    sinks = torch.linspace(-2.0, 2.0, hq, device=w.q.device)
+    out = torch.empty_like(w.q)
+    cases = {"window_4096": dict(window_left=4096), "softcap_30": dict(softcap=30.0),
+             "sinks": dict(sinks=sinks), "all_three": dict(window_left=4096, softcap=30.0, sinks=sinks)}
+    res = {}
+    for name, kw in cases.items():
+        n = va.workspace_size(w.q, w.k_cache, w.seqused_k, w.max_seqlen_q, w.max_seqlen_k)
+        ws = torch.zeros(n + 256, dtype=torch.uint8, device=w.q.device)
+
+        def call():
+            va.verify_attn_opt(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q, w.seqused_k,
+                               w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale, w.k_descale,
+                               w.v_descale, out=out, workspace=ws, stream=torch.cuda.current_stream(),
+                               **kw)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                call()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(4):
+                call()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_rep = max(K // 4, 5)
+        a.record()
+        for _ in range(n_rep):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        res[name + "_us"] = round(a.elapsed_time(b) / (n_rep * 4) * 1e3, 2)
+    res["note"] = ("verify_attn_opt per call (main kernel with the variant code + merge), device time "
+                   "from CUDA-graph replays; the window reads only the keys it sees")
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -495,6 +540,7 @@ def run_ours(args):
 
     draft = None if mla else draft_extend_timing(va, w, stream, torch, min(K, 200))
     shards = None if mla else shard_timing(va, w, torch, min(K, 200))
+    variants = None if mla else variant_timing(va, w, torch, min(K, 200))
 
     peak, peak_src = peak_hbm()
     achieved = alg / (main_ms / 1e3) / 1e9
@@ -518,6 +564,7 @@ def run_ours(args):
         "gpu_launches": 2 * K,
         **({} if draft is None else {"draft_extend": draft}),
         **({} if shards is None else {"kv_shards": shards}),
+        **({} if variants is None else {"variants": variants}),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
