@@ -194,13 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // waits for this grid's completion before reading the workspace.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // ---- work range (all threads) -------------------------------------------------
-  long long t0, t1, ts_first = 0;
-  int j_first = 0;
-  locate_work<kThreads>(p, c, scratch, s_j, s_ts, &t0, &t1, &j_first, &ts_first);
-  if (t0 >= t1) return;
-
-  // ---- setup --------------------------------------------------------------------
+  // ---- setup (no global memory: runs while the stream's previous kernel ends) ---
   constexpr uint32_t kSwWarps = kSoftmaxThreads / 32;
   if (tid == 0) {
     for (int s = 0; s < C::kKSlots; ++s) {
@@ -239,6 +233,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // This kernel is itself a programmatic dependent of the stream's previous
+  // kernel (which may write Q, the block table or the lengths, and may still
+  // read this workspace): nothing global is read or written before its
+  // completion.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // ---- work range (all threads) -------------------------------------------------
+  long long t0, t1, ts_first = 0;
+  int j_first = 0;
+  locate_work<kThreads>(p, c, scratch, s_j, s_ts, &t0, &t1, &j_first, &ts_first);
+  if (t0 >= t1) {  // CTA-uniform
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
 
   if (warp == 0 || warp == 2 || warp == 3) {
     // ======================= TMA producers ======================================
@@ -875,19 +884,23 @@ cudaError_t prepare_main_tc() {
 cudaError_t launch_main_tc(const Params& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            cudaStream_t stream) {
   const bool var = p.window_left >= 0 || p.softcap_log2 > 0.f || p.sinks != nullptr;
-  const dim3 grid(p.num_splits);
-  if (p.kv_fp8) {
-    if (var)
-      va_main_tc_kernel<true, true><<<grid, kThreads, Cfg<true>::kSmemBytes, stream>>>(p, tm_k, tm_v);
-    else
-      va_main_tc_kernel<true, false><<<grid, kThreads, Cfg<true>::kSmemBytes, stream>>>(p, tm_k, tm_v);
-  } else {
-    if (var)
-      va_main_tc_kernel<false, true><<<grid, kThreads, Cfg<false>::kSmemBytes, stream>>>(p, tm_k, tm_v);
-    else
-      va_main_tc_kernel<false, false><<<grid, kThreads, Cfg<false>::kSmemBytes, stream>>>(p, tm_k, tm_v);
-  }
-  return cudaGetLastError();
+  // a programmatic dependent of the stream's previous kernel: its launch and
+  // setup overlap that kernel's tail (it waits before touching memory)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = p.kv_fp8 ? Cfg<true>::kSmemBytes : Cfg<false>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (p.kv_fp8)
+    return var ? cudaLaunchKernelEx(&cfg, va_main_tc_kernel<true, true>, p, tm_k, tm_v)
+               : cudaLaunchKernelEx(&cfg, va_main_tc_kernel<true, false>, p, tm_k, tm_v);
+  return var ? cudaLaunchKernelEx(&cfg, va_main_tc_kernel<false, true>, p, tm_k, tm_v)
+             : cudaLaunchKernelEx(&cfg, va_main_tc_kernel<false, false>, p, tm_k, tm_v);
 }
 
 }  // namespace va

@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(kMergeThreads, 4) va_merge_kernel(const Params
   constexpr int kThreadsPerRow = DV / 4;
   constexpr int kRowsPerCta = kMergeThreads / kThreadsPerRow;
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next call's main kernel may be scheduled now (it waits for this grid)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int j = blockIdx.x;
   const int r = blockIdx.y * kRowsPerCta + (int)(threadIdx.x / kThreadsPerRow);
   const int col4 = (int)(threadIdx.x % kThreadsPerRow);
@@ -152,6 +154,7 @@ __global__ void __launch_bounds__(kMlaNope, 2) va_merge_mla_kernel(const Params 
   __shared__ float s_w[kMlaSegChunk][kMlaMergeRows];
   __shared__ float s_sc[kMlaMergeRows];
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int j = blockIdx.x;  // one KV head: item j is sequence j
   const int r0 = blockIdx.y * kMlaMergeRows;
   static_assert(kMlaMergeRows == 4 && kMlaSegChunk * kMlaMergeRows == 32, "one row group per thread; warp 0 holds a group's (m, l)");

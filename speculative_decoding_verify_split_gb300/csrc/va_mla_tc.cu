@@ -162,26 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The merge kernel is a programmatic dependent; it waits for this grid.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  long long t0, t1, ts_first = 0;
-  int j_first = 0;
-  locate_work<kThreads>(p, c, scratch, s_j, s_ts, &t0, &t1, &j_first, &ts_first);
-  if (t0 >= t1) return;
-  if (warp >= 4 && warp < 12) {
-    // the first item's Q rows into L2 before the ring's first loads flood HBM
-    int jq = j_first;
-    long long tq = ts_first;
-    Piece pq;
-    if (next_piece(p, t0, t1, jq, tq, pq)) {
-      const int r = 16 * (warp & 3) + (lane & 15), qtr = 2 * ((warp - 4) >> 2) + (lane >> 4);
-      if (r < pq.R) {
-        const uint16_t* src = p.q + (int64_t)(pq.q0 + r / p.group) * p.q_s0 + (int64_t)(r % p.group) * p.q_s1;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128 * qtr));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128 * qtr + 64));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + kMlaNope + 16 * qtr));
-      }
-    }
-  }
-
+  // ---- setup (no global memory: runs while the stream's previous kernel ends) ---
   constexpr uint32_t kSwWarps = kSoftmaxThreads / 32;
   if (tid == 0) {
     for (int s = 0; s < kSlots; ++s) {
@@ -213,6 +194,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // A programmatic dependent of the stream's previous kernel (which may write
+  // Q, the block table or the lengths, and may still read this workspace):
+  // nothing global is read or written before its completion.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  long long t0, t1, ts_first = 0;
+  int j_first = 0;
+  locate_work<kThreads>(p, c, scratch, s_j, s_ts, &t0, &t1, &j_first, &ts_first);
+  if (t0 >= t1) {  // CTA-uniform
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
+  if (warp >= 4 && warp < 12) {
+    // the first item's Q rows into L2 before the ring's first loads flood HBM
+    int jq = j_first;
+    long long tq = ts_first;
+    Piece pq;
+    if (next_piece(p, t0, t1, jq, tq, pq)) {
+      const int r = 16 * (warp & 3) + (lane & 15), qtr = 2 * ((warp - 4) >> 2) + (lane >> 4);
+      if (r < pq.R) {
+        const uint16_t* src = p.q + (int64_t)(pq.q0 + r / p.group) * p.q_s0 + (int64_t)(r % p.group) * p.q_s1;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128 * qtr));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128 * qtr + 64));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + kMlaNope + 16 * qtr));
+      }
+    }
+  }
+
 
   if (warp == 0 || warp == 2 || warp == 3) {
     // ======================= TMA producers ======================================
@@ -673,8 +683,18 @@ cudaError_t prepare_mla_tc() {
 }
 
 cudaError_t launch_mla_tc(const Params& p, const CUtensorMap& tm_kv, cudaStream_t stream) {
-  va_mla_tc_kernel<<<dim3(p.num_splits), kThreads, kSmemBytes, stream>>>(p, tm_kv);
-  return cudaGetLastError();
+  // a programmatic dependent of the stream's previous kernel (see the kernel)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, va_mla_tc_kernel, p, tm_kv);
 }
 
 }  // namespace va
