@@ -818,12 +818,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<uint4*>(dst)[v4] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         } else {
+          // 32-byte stores: a warp's store then writes 32 whole sectors of
+          // 32 rows instead of 32 half sectors, half the write requests of
+          // 16-byte stores (the workspace is 256-byte aligned, col % 32 == 0)
           float* dst = p.ws_acc + (piece * p.max_rows + r) * kHeadDim + col;
 #pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4)
-            reinterpret_cast<float4*>(dst)[v4] =
-                make_float4(__uint_as_float(o[4 * v4]), __uint_as_float(o[4 * v4 + 1]),
-                            __uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3]));
+          for (int v8 = 0; v8 < 4; ++v8) st_global_v8(dst + 8 * v8, o + 8 * v8);
         }
       };
       if constexpr (FP8) {
