@@ -280,6 +280,8 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
   p.out = static_cast<uint16_t*>(out->data);
   p.o_s0 = out->stride[0];
   p.o_s1 = out->stride[1];
+  p.out_v8 = (reinterpret_cast<uintptr_t>(out->data) & 31u) == 0 && (p.o_s0 * 2) % 32 == 0 &&
+             (p.o_s1 * 2) % 32 == 0;
   p.num_seqs = (int32_t)sh.num_seqs;
   p.hq = (int32_t)sh.hq;
   p.hkv = (int32_t)sh.hkv;

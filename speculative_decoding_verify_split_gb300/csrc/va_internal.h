@@ -46,6 +46,7 @@ struct Params {
   const float* v_descale;  // nullable
   uint16_t* out;           // bf16 bits
   int64_t o_s0, o_s1;
+  int32_t out_v8;          // out and its row strides are 32-byte aligned (32-byte stores)
   int32_t num_seqs, hq, hkv, group, num_blocks, total_q, max_seqlen_q, max_seqlen_k;
   int32_t kv_fp8;
   float scale_log2;  // softmax_scale * log2(e)

@@ -808,14 +808,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!row_ok) return;
         if (pc.direct) {
           uint16_t* dst = p.out + (int64_t)(pc.q0 + tq) * p.o_s0 + (int64_t)(pc.kvh * G + gq) * p.o_s1 + col;
+          uint32_t w[16];
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint32_t w[4];
+          for (int e2 = 0; e2 < 16; ++e2)
+            w[e2] = pack_bf16x2(__uint_as_float(o[2 * e2]) * inv, __uint_as_float(o[2 * e2 + 1]) * inv);
+          if (p.out_v8) {  // whole sectors, as for the partials
+            st_global_v8(dst, w);
+            st_global_v8(dst + 16, w + 8);
+          } else {
 #pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2)
-              w[e2] = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2 * e2]) * inv,
-                                  __uint_as_float(o[v4 * 8 + 2 * e2 + 1]) * inv);
-            reinterpret_cast<uint4*>(dst)[v4] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int v4 = 0; v4 < 4; ++v4)
+              reinterpret_cast<uint4*>(dst)[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
           }
         } else {
           // 32-byte stores: a warp's store then writes 32 whole sectors of

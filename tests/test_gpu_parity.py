@@ -162,6 +162,21 @@ def test_strided_q_and_out():
     assert torch.isnan(out_big[..., :256].float()).all()
 
 
+@pytest.mark.parametrize("splits", [0, 1])
+def test_out_rows_16_byte_aligned(splits):
+    """Output rows 16- but not 32-byte aligned (row stride 528 B, base 16 B into
+    a row): rows written directly (one split: every item) take 16-byte stores."""
+    w = make_workload([4, 2, 3], [300, 200, 1000], 16, 1, "fp8_e4m3", seed=16)
+    ref = oracle_from_torch(w)
+    wg = to_gpu(w)
+    out_big = torch.full((wg.q.shape[0], 16, 264), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = out_big[..., 8:264]
+    va.run_workload_ex(wg, out=out, num_splits=splits)
+    torch.cuda.synchronize()
+    compare(out, ref)
+    assert torch.isnan(out_big[..., :8].float()).all()
+
+
 def test_side_stream():
     w = make_workload([4, 2], [800, 600], 16, 1, "fp8_e4m3", seed=15)
     s = torch.cuda.Stream()
