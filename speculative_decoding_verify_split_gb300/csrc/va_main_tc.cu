@@ -47,6 +47,8 @@
 // window, logit soft cap, sinks). Waits are bounded in time and warp-uniform:
 // on a timeout the kernel sets the workspace status word, stops issuing
 // work, drains and frees its TMEM.
+#include <type_traits>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -790,10 +792,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(kBarPFull + pb));
       }
 
-      // -- epilogue: this thread writes O[r][128 kh + 64 sub, +64)
+      // -- epilogue: the row sum first (it does not depend on O, so the
+      // exchange with the quadrant's other warp overlaps the last P V), then O
+      float lrow = exchange(l, false);
       wait_or_fail(kBarOFull, piece_idx & 1, 4096);
       tc_fence_after();
-      float lrow = exchange(l, false);
       ++piece_idx;
       if (!ok) continue;
       // an attention sink joins the normaliser once per row: here for rows
@@ -804,44 +807,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float inv = lrow > 0.f ? vd / lrow : 0.f;
       const int64_t piece = (int64_t)pc.j + c;
-      auto emit = [&](const uint32_t (&o)[32], int col) {
+      // this row's n (16 or 32) values of O from column col (col % 16 == 0)
+      auto emit = [&](const uint32_t* o, int col, auto n_c) {
+        constexpr int n = decltype(n_c)::value;
         if (!row_ok) return;
         if (pc.direct) {
           uint16_t* dst = p.out + (int64_t)(pc.q0 + tq) * p.o_s0 + (int64_t)(pc.kvh * G + gq) * p.o_s1 + col;
-          uint32_t w[16];
+          uint32_t w[n / 2];
 #pragma unroll
-          for (int e2 = 0; e2 < 16; ++e2)
+          for (int e2 = 0; e2 < n / 2; ++e2)
             w[e2] = pack_bf16x2(__uint_as_float(o[2 * e2]) * inv, __uint_as_float(o[2 * e2 + 1]) * inv);
           if (p.out_v8) {  // whole sectors, as for the partials
-            st_global_v8(dst, w);
-            st_global_v8(dst + 16, w + 8);
+#pragma unroll
+            for (int v = 0; v < n / 16; ++v) st_global_v8(dst + 16 * v, w + 8 * v);
           } else {
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
+            for (int v4 = 0; v4 < n / 8; ++v4)
               reinterpret_cast<uint4*>(dst)[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
           }
         } else {
-          // 32-byte stores: a warp's store then writes 32 whole sectors of
-          // 32 rows instead of 32 half sectors, half the write requests of
-          // 16-byte stores (the workspace is 256-byte aligned, col % 32 == 0)
+          // 32-byte stores: a warp's store writes whole sectors, half the
+          // write requests of 16-byte stores (the workspace is 256-byte
+          // aligned and col % 16 == 0)
           float* dst = p.ws_acc + (piece * p.max_rows + r) * kHeadDim + col;
 #pragma unroll
-          for (int v8 = 0; v8 < 4; ++v8) st_global_v8(dst + 8 * v8, o + 8 * v8);
+          for (int v8 = 0; v8 < n / 8; ++v8) st_global_v8(dst + 8 * v8, o + 8 * v8);
         }
       };
       if constexpr (FP8) {
         // own lane holds the hi (sub 0) or lo (sub 1) part of all 128 columns
-        // of the half; add the partner's and keep chunks 2 sub, 2 sub + 1
+        // of the half. Per 32-column chunk the pair splits the work: lane
+        // i + 16 sub sums and writes columns [16 sub, 16 sub + 16), sending
+        // the partner the other 16 (one shuffle per summed value)
 #pragma unroll 1
         for (int k = 0; k < 4; ++k) {
           uint32_t o[32];
           tmem_ld_32x32b_x32(tmem + lane_base + kColO + 128 * kh + 32 * k, o);
           tmem_wait_ld();
+          uint32_t sum[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            o[i] = __float_as_uint(__uint_as_float(o[i]) +
-                                   __shfl_xor_sync(0xffffffffu, __uint_as_float(o[i]), 16));
-          if ((k >> 1) == sub) emit(o, 128 * kh + 32 * k);
+          for (int i = 0; i < 16; ++i) {
+            const float mine = __uint_as_float(sub ? o[16 + i] : o[i]);
+            const float give = __uint_as_float(sub ? o[i] : o[16 + i]);
+            sum[i] = __float_as_uint(mine + __shfl_xor_sync(0xffffffffu, give, 16));
+          }
+          emit(sum, 128 * kh + 32 * k + 16 * sub, std::integral_constant<int, 16>{});
         }
       } else {
 #pragma unroll 1
@@ -849,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t o[32];
           tmem_ld_16x32bx2_x32<64>(tmem + lane_base + kColO + 128 * kh + 32 * k, o);
           tmem_wait_ld();
-          emit(o, 128 * kh + 64 * sub + 32 * k);
+          emit(o, 128 * kh + 64 * sub + 32 * k, std::integral_constant<int, 32>{});
         }
       }
       if (row_ok && !pc.direct && kh == 0 && sub == 0) {
