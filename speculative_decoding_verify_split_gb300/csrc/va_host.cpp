@@ -124,6 +124,26 @@ va_status validate(const va_tensor* q, const va_tensor* k, const va_tensor* v,
   return VA_OK;
 }
 
+// Upper bound on the key tiles of a batch (B sequences x hkv KV heads of at
+// most max_k keys, or of a window of max_q + window_left keys).
+static int64_t tiles_upper_bound(int64_t B, int64_t hkv, int32_t max_q, int32_t max_k, int tile,
+                                 int32_t window_left) {
+  int64_t item_tiles = (max_k + tile - 1) / tile;
+  if (window_left >= 0) {  // a window of max_q + window_left keys spans at most this many tiles
+    const int64_t w_tiles = ((int64_t)max_q + window_left + tile - 1) / tile + 1;
+    if (w_tiles < item_tiles) item_tiles = w_tiles;
+  }
+  return B * hkv * item_tiles;
+}
+
+// The split cost of starting an item (see kPieceCostTiles) for a plan: the
+// full cost when CTAs hold many tiles, 1 when the tile bound per CTA is
+// small (every CTA then pays a start-up anyway).
+static int32_t piece_cost_for(const va_plan& plan, int64_t tiles_bound) {
+  return tiles_bound < kSmallSplitTiles * (int64_t)plan.num_splits ? kPieceCostTilesSmall
+                                                                    : kPieceCostTiles;
+}
+
 va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t max_k, int32_t kv_dtype,
                     int32_t num_sms, int32_t force, va_plan* plan, int32_t window_left) {
   if (!plan) return VA_ERR_NULL;
@@ -134,12 +154,7 @@ va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t m
   if (G * max_q > kMaxRows) return VA_ERR_UNSUPPORTED;
   const int tile = kv_dtype == VA_FP8_E4M3 ? kTcTileKeysFp8 : kTcTileKeysBf16;
   const int64_t J = B * hkv;
-  int64_t item_tiles = (max_k + tile - 1) / tile;
-  if (window_left >= 0) {  // a window of max_q + window_left keys spans at most this many tiles
-    const int64_t w_tiles = ((int64_t)max_q + window_left + tile - 1) / tile + 1;
-    if (w_tiles < item_tiles) item_tiles = w_tiles;
-  }
-  const int64_t tiles_bound = J * item_tiles;
+  const int64_t tiles_bound = tiles_upper_bound(B, hkv, max_q, max_k, tile, window_left);
   if (tiles_bound + J * kPieceCostTiles > INT32_MAX / 2) return VA_ERR_UNSUPPORTED;
   // Heuristic: one CTA per SM (the main kernel keeps one CTA per SM), fewer
   // only when the upper-bound workload has fewer tiles than SMs. A CTA's
@@ -299,7 +314,8 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
   p.num_splits = plan.num_splits;
   p.max_rows = plan.max_rows;
   p.num_work = plan.num_work;
-  p.piece_cost = kPieceCostTiles;
+  p.piece_cost = piece_cost_for(
+      plan, tiles_upper_bound(sh.num_seqs, sh.hkv, max_q, max_k, plan.tile_keys, p.window_left));
   p.dv = kHeadDim;
   if (part) {
     p.partial = 1;

@@ -106,9 +106,15 @@ constexpr int kTcTileKeysFp8 = 128;  // keys per tile, FP8 KV
 constexpr int kTcTileKeysBf16 = 64;  // keys per tile, BF16 KV
 // Split cost of starting a work item, in tiles: a CTA's boundary between two
 // items (epilogue of one, Q staging and pipeline refill of the next). Swept
-// over 3/4/6/8 on the mid- and long-context FP8 workloads: 4 is best on the
-// first and within noise on the second.
+// over 2/3/4/6/8 on the mid- and long-context FP8 workloads: 4 is best on both.
+// When the tile bound per CTA is under kSmallSplitTiles, every CTA pays a
+// start-up of its own and charging it to the CTAs that start an item only
+// unbalances the split: swept over 1-4 there, 1 is best (main kernel,
+// gqa_32q2kv 22.5 -> 21.2 us on one box and 22.9 -> 22.7 on another,
+// tiny_verify 18.7 -> 18.4).
 constexpr int kPieceCostTiles = 4;
+constexpr int kPieceCostTilesSmall = 1;
+constexpr int64_t kSmallSplitTiles = 16;
 
 cudaError_t launch_merge(const Params& p, cudaStream_t stream);
 
