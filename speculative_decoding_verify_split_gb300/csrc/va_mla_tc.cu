@@ -636,9 +636,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // rows, partial[piece][row / 4][column][row % 4] (mla_acc_index): a
       // lane's four rows are one 16-byte store and a warp's stores of a group
       // are 512 contiguous bytes. The merge kernel writes the output rows.
+      // The row sum does not depend on O: its exchange overlaps the last P V.
+      const float lrow = exchange(l, false);
       wait_or_fail(kBarOFull, piece_idx & 1, 4096);
       tc_fence_after();
-      const float lrow = exchange(l, false);
       ++piece_idx;
       if (!ok) continue;
       const int64_t piece = (int64_t)pc.j + c;
