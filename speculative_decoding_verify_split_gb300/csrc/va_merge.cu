@@ -43,6 +43,10 @@ __global__ void __launch_bounds__(kMergeThreads, 4) va_merge_kernel(const Params
   const int col4 = (int)(threadIdx.x % kThreadsPerRow);
   const int b = j / p.hkv;
   const int kvh = j - b * p.hkv;
+  // the split metadata (written for every item) is read with the lengths,
+  // not after them: one round trip instead of two before the partials
+  const long long N = p.ws_meta[p.num_work];
+  const long long ts = p.ws_meta[j];
   const int L = seq_q_len(p, b);
   const int G = p.group;
   if (r >= G * L) return;
@@ -63,8 +67,6 @@ __global__ void __launch_bounds__(kMergeThreads, 4) va_merge_kernel(const Params
       *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
     return;
   }
-  const long long N = p.ws_meta[p.num_work];
-  const long long ts = p.ws_meta[j];
   const int c0 = split_of(ts, N, p.num_splits);
   const int c1 = split_of(ts + nt - 1, N, p.num_splits);
   if (!PARTIAL && c0 == c1) return;  // one CTA held the whole item and wrote it
