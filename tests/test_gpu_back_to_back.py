@@ -31,6 +31,7 @@ def _batches(make):
     b = make(seed=42).to("cuda")
     su = torch.tensor([max(k - d, q) for k, d, q in zip(KV_LENS, SHORTER, Q_LENS)], dtype=torch.int32)
     b.seqused_k = su.to("cuda")
+    b.kv_lens = su.tolist()
     assert a.block_table.shape == b.block_table.shape and a.q.shape == b.q.shape
     return a, b
 
@@ -93,6 +94,64 @@ def test_back_to_back_gqa(dt):
     assert not torch.equal(refs[0], refs[1])
     for i, o in enumerate(outs):
         assert torch.equal(o.view(torch.int16), refs[i % 2].view(torch.int16)), f"call {i}"
+
+
+class _Variants(_Gqa):
+    """verify_attn_opt with a window, a soft cap and sinks (the VAR main
+    kernel and the SINKS merge)."""
+
+    def __init__(self, hq):
+        self.sinks = torch.linspace(-1.5, 1.5, hq, device="cuda")
+
+    def __call__(self, w, out, ws):
+        return va.verify_attn_opt(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q,
+                                  w.seqused_k, w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale,
+                                  w.k_descale, w.v_descale, out=out, workspace=ws, window_left=700,
+                                  softcap=20.0, sinks=self.sinks)
+
+
+def test_back_to_back_variants():
+    a, b = _batches(lambda seed: make_workload(Q_LENS, KV_LENS, 16, 2, "fp8_e4m3", seed=seed,
+                                               k_descale=1.1, v_descale=0.8))
+    outs, refs = _run_alternating(a, b, ["q", "k_cache", "v_cache", "block_table", "seqused_k"],
+                                  _Variants(a.q.shape[1]))
+    assert not torch.equal(refs[0], refs[1])
+    for i, o in enumerate(outs):
+        assert torch.equal(o.view(torch.int16), refs[i % 2].view(torch.int16)), f"call {i}"
+
+
+def test_back_to_back_shards():
+    """Two shards and their merge per call (verify_attn_partial twice, then
+    verify_attn_merge_partials), calls unsynchronised, each shard with its
+    own workspace reused across calls."""
+    from speculative_decoding_verify_split_gb300.workloads import split_kv_shards
+    a, b = _batches(lambda seed: make_workload(Q_LENS, KV_LENS, 16, 1, "fp8_e4m3", seed=seed))
+    width = a.block_table.shape[1]
+    plans = {id(x): split_kv_shards(x, 2, seed=3) for x in (a, b)}
+    wss = []
+    for bt, su, ext in plans[id(a)]:
+        n = va.workspace_size(a.q, a.k_cache, su, a.max_seqlen_q, width * 16)
+        wss.append(torch.zeros(n + 256, dtype=torch.uint8, device="cuda"))
+
+    def call(w):
+        parts = []
+        for (bt, su, ext), ws in zip(plans[id(w)], wss):
+            parts.append(va.verify_attn_partial(w.q, w.k_cache, w.v_cache, bt, w.cu_seqlens_q, su,
+                                                w.max_seqlen_q, width * 16, w.softmax_scale,
+                                                w.k_descale, w.v_descale, kv_extent=ext, workspace=ws))
+        return va.merge_partials(parts)
+
+    refs = []
+    for w in (a, b):
+        refs.append(call(w).clone())
+        torch.cuda.synchronize()
+    outs = [call(a if i % 2 == 0 else b) for i in range(6)]
+    torch.cuda.synchronize()
+    assert not torch.equal(refs[0], refs[1])
+    for i, o in enumerate(outs):
+        assert torch.equal(o.view(torch.int16), refs[i % 2].view(torch.int16)), f"call {i}"
+    for ws in wss:
+        assert va.workspace_status(ws) == 0
 
 
 def test_back_to_back_latent():
