@@ -142,30 +142,32 @@ __global__ void __launch_bounds__(kMergeThreads, 4) va_merge_kernel(const Params
 // The latent-cache path's merge. Its partials come in groups of four rows,
 // partial[piece][row / 4][column][row % 4] (mla_acc_index), and every piece
 // has one, also when a single CTA held the whole item. One thread per output
-// column (512), one group of four packed rows per CTA: a thread reads one
-// 16-byte group per segment, a warp's loads are 512 contiguous bytes, and two
-// CTAs fit on an SM. Segments go eight at a time: every thread issues all its partial loads at once (one L2 round trip
-// per group), while warp 0, one lane per (segment, row), reads the group's
-// (m, l), moves each row's running max and publishes the group's weights
-// 2^(m_s - M) and the rescale of the earlier sum in shared memory. Each output row is written as
-// one coalesced 1 KB line.
-constexpr int kMlaMergeRows = 4;  // one 16-byte row group per thread and segment
-constexpr int kMlaSegChunk = 8;
-
+// column (512), GROUPS groups of four packed rows per CTA: a thread reads one
+// 16-byte group per segment and group, a warp's loads are 512 contiguous
+// bytes, and two CTAs fit on an SM. Segments go SEGS at a time: every thread
+// issues all its partial loads at once (one L2 round trip per chunk), while
+// warp 0, one lane per (segment, row), reads the chunk's (m, l), moves each
+// row's running max and publishes the chunk's weights 2^(m_s - M) and the
+// rescale of the earlier sum in shared memory. Each output row is written as
+// one coalesced 1 KB line. (GROUPS, SEGS) is (1, 8) while the four-row CTAs
+// fit in one wave, else (2, 4): half the CTAs, two row groups of four
+// segments per thread.
+template <int GROUPS, int SEGS>
 __global__ void __launch_bounds__(kMlaNope, 2) va_merge_mla_kernel(const Params p) {
-  __shared__ float s_w[kMlaSegChunk][kMlaMergeRows];
-  __shared__ float s_sc[kMlaMergeRows];
+  constexpr int kRows = 4 * GROUPS;  // rows per CTA
+  static_assert(SEGS * kRows == 32, "warp 0: one lane per (segment, row)");
+  __shared__ float s_w[SEGS][kRows];
+  __shared__ float s_sc[kRows];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int j = blockIdx.x;  // one KV head: item j is sequence j
-  const int r0 = blockIdx.y * kMlaMergeRows;
-  static_assert(kMlaMergeRows == 4 && kMlaSegChunk * kMlaMergeRows == 32, "one row group per thread; warp 0 holds a group's (m, l)");
+  const int r0 = blockIdx.y * kRows;
   const int d = threadIdx.x;
   const int L = seq_q_len(p, j);
   const int G = p.group;
   const int R = G * L;
   if (r0 >= R) return;  // CTA-uniform
-  const int nrow = R - r0 < kMlaMergeRows ? R - r0 : kMlaMergeRows;
+  const int nrow = R - r0 < kRows ? R - r0 : kRows;
   const int q0 = p.cu_q[j];
   auto dst = [&](int rr) {
     const int t = (r0 + rr) / G, g = (r0 + rr) - t * G;
@@ -190,36 +192,37 @@ __global__ void __launch_bounds__(kMlaNope, 2) va_merge_mla_kernel(const Params 
     return k < ns && (!may_be_empty || split_begin(N, c, p.num_splits) != split_begin(N, c + 1, p.num_splits));
   };
 
-  float acc[kMlaMergeRows];
+  float acc[kRows];
 #pragma unroll
-  for (int i = 0; i < kMlaMergeRows; ++i) acc[i] = 0.f;
-  float M = -INFINITY, den = 0.f;  // row (d & 3)'s, in warp 0
-  for (int base = 0; base < ns; base += kMlaSegChunk) {
-    float4 a[kMlaSegChunk];
+  for (int i = 0; i < kRows; ++i) acc[i] = 0.f;
+  float M = -INFINITY, den = 0.f;  // row (d % kRows)'s, in warp 0
+  for (int base = 0; base < ns; base += SEGS) {
+    float4 a[SEGS][GROUPS];
 #pragma unroll
-    for (int k = 0; k < kMlaSegChunk; ++k) {
+    for (int k = 0; k < SEGS; ++k) {
       const int64_t piece = (int64_t)j + c0 + base + k;
-      a[k] = exists(base + k) ? __ldcg(reinterpret_cast<const float4*>(p.ws_acc + mla_acc_index(piece, r0, d, ldr)))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int gg = 0; gg < GROUPS; ++gg)  // groups past the piece's rows do not exist
+        a[k][gg] = (exists(base + k) && r0 + 4 * gg < ldr)
+                       ? __ldcg(reinterpret_cast<const float4*>(p.ws_acc + mla_acc_index(piece, r0 + 4 * gg, d, ldr)))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (d < 32) {
-      // warp 0: lane 4k + i holds segment base + k, row r0 + i; rows reduce
-      // over the lanes with the same i (xor 4, 8, 16)
-      const int k = d >> 2, i = d & 3;
+      // warp 0: lane kRows k + i holds segment base + k, row r0 + i; rows
+      // reduce over the lanes with the same i
+      const int k = d / kRows, i = d % kRows;
       float2 ml = make_float2(-INFINITY, 0.f);
       if (i < nrow && exists(base + k))
         ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (((int64_t)j + c0 + base + k) * p.max_rows + r0 + i) * 2));
       float mc = ml.x;
-      mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 4));
-      mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 8));
-      mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 16));
+#pragma unroll
+      for (int o = kRows; o < 32; o <<= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
       mc = fmaxf(mc, M);
       const float sc = (M == -INFINITY || mc == -INFINITY) ? 0.f : exp2f(M - mc);
       const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mc);
       float wl = w * ml.y;
-      wl += __shfl_xor_sync(0xffffffffu, wl, 4);
-      wl += __shfl_xor_sync(0xffffffffu, wl, 8);
-      wl += __shfl_xor_sync(0xffffffffu, wl, 16);
+#pragma unroll
+      for (int o = kRows; o < 32; o <<= 1) wl += __shfl_xor_sync(0xffffffffu, wl, o);
       den = den * sc + wl;  // each lane keeps its row's (M, den)
       if (mc != -INFINITY) M = mc;
       s_w[k][i] = w;
@@ -227,22 +230,23 @@ __global__ void __launch_bounds__(kMlaNope, 2) va_merge_mla_kernel(const Params 
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < kMlaMergeRows; ++i) {
+    for (int i = 0; i < kRows; ++i) {
       float x = acc[i] * s_sc[i];
 #pragma unroll
-      for (int k = 0; k < kMlaSegChunk; ++k) {
-        const float4 v = a[k];
-        x = fmaf(s_w[k][i], i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w)), x);
+      for (int k = 0; k < SEGS; ++k) {
+        const float4 v = a[k][i / 4];
+        const int e = i % 4;
+        x = fmaf(s_w[k][i], e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w)), x);
       }
       acc[i] = x;
     }
     __syncthreads();  // s_w and s_sc are rewritten by the next group
   }
   const float vd = p.v_descale ? *p.v_descale : 1.0f;
-  if (d < kMlaMergeRows) s_sc[d] = (M == -INFINITY || !(den > 0.f)) ? 0.f : vd / den;  // lanes 0-3
+  if (d < kRows) s_sc[d] = (M == -INFINITY || !(den > 0.f)) ? 0.f : vd / den;  // lanes 0..kRows-1
   __syncthreads();
 #pragma unroll
-  for (int i = 0; i < kMlaMergeRows; ++i)
+  for (int i = 0; i < kRows; ++i)
     if (i < nrow) *dst(i) = float_to_bf16_bits(acc[i] * s_sc[i]);
 }
 
@@ -294,8 +298,13 @@ cudaError_t launch_merge(const Params& p, cudaStream_t stream) {
   if (p.num_work == 0 || p.max_rows == 0) return cudaSuccess;
   if (p.dv != kHeadDim && p.dv != kMlaNope) return cudaErrorInvalidValue;
   if (p.dv == kMlaNope) {
+    // four-row CTAs while they fit in one wave (two per SM, one split per
+    // SM), else eight-row CTAs: mla_mid_context_fp8 (768 four-row CTAs)
+    const int64_t ctas4 = (int64_t)p.num_work * ((p.max_rows + 3) / 4);
+    const bool wide = ctas4 > 2 * (int64_t)p.num_splits;
+    const int rows = wide ? 8 : 4;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.num_work, (unsigned)((p.max_rows + kMlaMergeRows - 1) / kMlaMergeRows));
+    cfg.gridDim = dim3((unsigned)p.num_work, (unsigned)((p.max_rows + rows - 1) / rows));
     cfg.blockDim = dim3(kMlaNope);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -303,7 +312,8 @@ cudaError_t launch_merge(const Params& p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, va_merge_mla_kernel, p);
+    return wide ? cudaLaunchKernelEx(&cfg, va_merge_mla_kernel<2, 4>, p)
+                : cudaLaunchKernelEx(&cfg, va_merge_mla_kernel<1, 8>, p);
   }
   const int rows_per_cta = kMergeThreads / (p.dv / 4);
   cudaLaunchConfig_t cfg = {};

@@ -107,6 +107,15 @@ def test_long_context_sampled():
     compare(got[torch.as_tensor(r, device="cuda")], ref[r])
 
 
+def test_many_sequences_eight_row_merge():
+    """64 short sequences of 3 draft tokens x 16 heads: 768 four-row merge
+    CTAs, more than one wave, so the merge takes eight rows per CTA."""
+    g = np.random.default_rng(5)
+    kv = [int(x) for x in g.integers(64, 600, size=64)]
+    w = make_mla_workload([3] * 64, kv, 16, seed=23, k_descale=1.2, v_descale=0.9)
+    compare(run(w.to("cuda")), mla_oracle_from_torch(w))
+
+
 def test_errors():
     w = make_mla_workload([2], [100], 16, seed=41).to("cuda")
     with pytest.raises(va.VerifyAttnError) as e:   # 16 heads x 5 tokens > 64 rows
