@@ -266,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const void* tmap = is_k ? (const void*)&tm_k : (const void*)&tm_v;
     constexpr int kBoxes = kPagesPerTile * C::kChunks;  // boxes per tile
     static_assert(kBoxes <= 32, "one box per lane");
+    const uint64_t kv_policy = l2_evict_first_policy();  // K and V are read once
     int it = 0;
     int j = j_first;
     long long ts = ts_first;
@@ -319,8 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 1; u < kPagesPerTile; ++u)
             if (i == u) id = ids[u];
           if (id >= 0)
-            tma_load_4d(dst + ch * C::kRegion + i * 2048, tmap, ch * (128 / C::kEsize), pc.kvh, 0, id,
-                        bar(bar_full + s));
+            tma_load_4d_hint(dst + ch * C::kRegion + i * 2048, tmap, ch * (128 / C::kEsize), pc.kvh, 0, id,
+                             bar(bar_full + s), kv_policy);
         }
         __syncwarp();
       }

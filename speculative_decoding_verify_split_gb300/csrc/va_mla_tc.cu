@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 || warp == 2 || warp == 3) {
     // ======================= TMA producers ======================================
     const int prod = warp == 0 ? 0 : warp - 1;
+    const uint64_t kv_policy = l2_evict_first_policy();  // the cache rows are read once
     int it = 0;
     int j = j_first;
     long long ts = ts_first;
@@ -273,7 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 1; u < kPagesPerTile; ++u)
             if (i == u) id = ids[u];
-          if (id >= 0) tma_load_4d(dst + ch * kRegion + i * 2048, &tm_kv, ch * 128, 0, 0, id, bar(kBarFull + s));
+          if (id >= 0)
+            tma_load_4d_hint(dst + ch * kRegion + i * 2048, &tm_kv, ch * 128, 0, 0, id, bar(kBarFull + s),
+                             kv_policy);
         }
         __syncwarp();
       }

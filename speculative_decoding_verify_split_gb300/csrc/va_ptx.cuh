@@ -98,6 +98,25 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
 }
 
 // 4-D tiled load into shared memory, completing on `bar` (complete_tx bytes).
+// An L2 cache policy that marks the lines it tags to be evicted first: for
+// data read exactly once (the KV stream), so that it does not push out what
+// is read again (Q, the block table, the split partials).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// tma_load_4d with an L2 cache policy (a hint: it changes no value).
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void* tmap, int c0, int c1, int c2,
+                                                 int c3, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int c0, int c1, int c2,
                                             int c3, uint32_t bar) {
   asm volatile(
