@@ -69,13 +69,41 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def strip_c_comments(text: str) -> str:
+    """C/C++ source without its comments and whitespace runs (string and
+    character literals kept as they are), so that a change of wording alone
+    does not count as a change of the kernels."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_sha():
+    """A hash of the CUDA/C++ sources' code (comments and whitespace removed):
+    DRAM traffic recorded by ncu is reported only for the code it was taken
+    on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verify_split_gb300", "csrc")
     for f in sorted(glob.glob(os.path.join(csrc, "*"))):
-        with open(f, "rb") as fh:
+        with open(f, encoding="utf-8") as fh:
             h.update(os.path.basename(f).encode())
-            h.update(fh.read())
+            h.update(strip_c_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -10,7 +10,15 @@
 //
 // KV pages are TMA-loaded as 128-byte-swizzled boxes (16 tokens x 128 bytes
 // of one KV head) into separate K and V rings of 32 KB tiles and fed to the
-// tensor cores as they are.
+// tensor cores as they are. The loads carry an L2 evict_first policy: the
+// cache is read once per call, and its stream should not push Q, the block
+// table or the split partials out of L2.
+//
+// Launch order: the kernel is a programmatic dependent of the stream's
+// previous kernel. It sets up (barriers, TMEM, descriptor prefetch) before
+// griddepcontrol.wait and touches global memory only after it; its merge
+// kernel is its own programmatic dependent and lets the next call launch, so
+// back-to-back calls overlap a merge with the next call's launch and setup.
 //  * FP8 E4M3 cache, kind::f8f6f4. Q (bf16) is scaled per row by an exact
 //    power of two 2^e and split into two e4m3 terms, Qh = e4m3(Q 2^e) and
 //    Ql = e4m3(Q 2^e - Qh); P is split the same way. The two terms are
@@ -46,7 +54,9 @@
 // m_ref sits 4 above its first tile's max, so rescales are rare. The VAR instantiation adds the generic attention's variants (sliding
 // window, logit soft cap, sinks). Waits are bounded in time and warp-uniform:
 // on a timeout the kernel sets the workspace status word, stops issuing
-// work, drains and frees its TMEM.
+// work, drains and frees its TMEM. The epilogue writes split partials as
+// fp32 with 32-byte stores (whole L2 sectors), each lane of a hi/lo pair
+// summing and writing half of every 32-column chunk.
 #include <type_traits>
 
 #include <cuda_bf16.h>

@@ -27,7 +27,10 @@
 // bytes (four latent chunks and the rope chunk, whose box reaches past the
 // row end and is zero-filled), so a tile fills five 8 KB 128-byte-swizzled
 // regions; five ring slots (200 KB) are in flight. A slot is freed after
-// P V, since the same bytes are K and V.
+// P V, since the same bytes are K and V. The cache loads carry an L2
+// evict_first policy, and the kernel is launched as a programmatic dependent
+// of the stream's previous kernel (setup before griddepcontrol.wait), as in
+// the GQA kernel.
 // O^T columns are rows, so a rescale of some rows touches every lane: the
 // softmax warps decide together, per tile, with one barrier reduction.
 // FP8 cache only; plain attention (no window, soft cap or sinks).
