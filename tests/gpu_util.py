@@ -7,6 +7,7 @@ import torch
 
 import speculative_decoding_verify_split_gb300 as va
 from oracle.attention_fp64 import oracle_from_torch
+from parity_gate import check_gates
 
 # Tolerance on the bf16 output, from the pages' parity test (sglang PR 36330
 # digest, unit test: assert_close(actual, expected, atol=1e-2, rtol=1e-2)).
@@ -37,7 +38,10 @@ def rows_of(w, seqs):
 
 
 def compare(got_bf16: torch.Tensor, ref: np.ndarray, rows=None) -> dict:
-    """Elementwise |got - ref| <= ATOL + RTOL * |ref| on the given q rows."""
+    """The pages' elementwise bound |got - ref| <= ATOL + RTOL * |ref| on the
+    given q rows, and beside it the gates that scale with the output
+    (parity_gate.check_gates: relative L2 error of the whole output and of
+    every (token, head) row)."""
     got = got_bf16.to(torch.float64).cpu().numpy()
     if rows is not None:
         got, ref = got[rows], ref[rows]
@@ -46,9 +50,8 @@ def compare(got_bf16: torch.Tensor, ref: np.ndarray, rows=None) -> dict:
     err = np.abs(got - ref)
     bound = ATOL + RTOL * np.abs(ref)
     bad = err > bound
-    stats = dict(max_abs=float(err.max()) if err.size else 0.0,
-                 rel_l2=float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)),
-                 n=int(err.size))
+    stats = dict(max_abs=float(err.max()) if err.size else 0.0, n=int(err.size))
+    stats.update(check_gates(got, ref))
     assert not bad.any(), f"{int(bad.sum())} of {err.size} elements out of tolerance; {stats}"
     return stats
 

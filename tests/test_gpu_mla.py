@@ -8,8 +8,8 @@ tolerance (atol = rtol = 1e-2 on the bf16 output):
   draft tokens, 1 to 64 heads, descales, forced splits;
 * bit-identical results run to run, under a relabelling of the physical
   pages, and between CUDA-graph replays and eager calls;
-* the long-context workload (16 sequences of 64K-128K keys), its shortest
-  and longest sequences, in the launch configuration the benchmark times."""
+* the long-context workload (16 sequences of 64K-128K keys), every
+  sequence, in the launch configuration the benchmark times."""
 import numpy as np
 import pytest
 import torch
@@ -17,7 +17,7 @@ import torch
 import speculative_decoding_verify_split_gb300 as va
 from speculative_decoding_verify_split_gb300.workloads import make_mla_workload, named_mla_workload
 from oracle.mla_fp64 import mla_oracle_from_torch
-from gpu_util import compare, rows_of
+from gpu_util import compare
 
 pytestmark = pytest.mark.gpu
 
@@ -96,15 +96,10 @@ def test_peaked_softmax_and_rescales():
         compare(run(w.to("cuda"), splits), mla_oracle_from_torch(w))
 
 
-def test_long_context_sampled():
+def test_long_context_every_sequence():
     w = named_mla_workload("mla_long_context_fp8", value_device="cuda")
-    wg = w.to("cuda")
-    got = run(wg)
-    kv = w.kv_lens
-    seqs = [int(np.argmin(kv)), int(np.argmax(kv))]
-    ref = mla_oracle_from_torch(w.to("cpu"), seqs)
-    r = rows_of(w.to("cpu"), seqs)
-    compare(got[torch.as_tensor(r, device="cuda")], ref[r])
+    got = run(w.to("cuda"))
+    print("mla_long_context_fp8", compare(got, mla_oracle_from_torch(w.to("cpu"))))
 
 
 def test_many_sequences_eight_row_merge():

@@ -6,7 +6,7 @@ log-sum-exp merge (verify_attn_merge_partials), through the C-ABI:
   row sees no key of the shard);
 * the merged output of 1-4 shards (page-aligned cuts, some empty) against
   the full verify-attention oracle, on both KV types and at forced splits;
-* the long-context workload cut in two, merged, on sampled sequences;
+* the long-context workload cut in two, merged, every sequence;
 * argument errors."""
 import numpy as np
 import pytest
@@ -17,7 +17,7 @@ from speculative_decoding_verify_split_gb300.workloads import (make_workload, na
                                                                split_kv_shards)
 from oracle.attention_fp64 import oracle_from_torch
 from oracle.partial_fp64 import partial_oracle_from_torch
-from gpu_util import compare, rows_of
+from gpu_util import compare
 
 pytestmark = pytest.mark.gpu
 
@@ -63,8 +63,7 @@ def test_each_shard_against_its_oracle(ci):
         assert np.array_equal(np.isinf(got_l), np.isinf(rl)), "rows without visible keys differ"
         fin = np.isfinite(rl)
         assert np.abs(got_l[fin] - rl[fin]).max(initial=0.0) < 2e-2
-        got_o = o.cpu().numpy().astype(np.float64)
-        assert np.all(np.abs(got_o - ro) <= 1e-2 + 1e-2 * np.abs(ro))
+        compare(o, ro)
 
 
 @pytest.mark.parametrize("ci", range(len(CASES)))
@@ -93,17 +92,12 @@ def test_one_shard_is_verify_attn():
     compare(out, oracle_from_torch(w))
 
 
-def test_long_context_in_two_shards_sampled():
+def test_long_context_in_two_shards_every_sequence():
     w = named_workload("long_context_fp8", value_device="cuda").to("cuda")
     parts = [run_shard(w, bt, su, ext) for bt, su, ext in split_kv_shards(w, 2, seed=9)]
     out = va.merge_partials(parts)
     torch.cuda.synchronize()
-    kv = w.kv_lens
-    seqs = [int(np.argmin(kv)), int(np.argmax(kv))]
-    wc = w.to("cpu")
-    ref = oracle_from_torch(wc, seqs)
-    r = rows_of(wc, seqs)
-    compare(out[torch.as_tensor(r, device="cuda")], ref[r])
+    print("two shards", compare(out, oracle_from_torch(w.to("cpu"))))
 
 
 def test_errors():

@@ -9,7 +9,7 @@ import torch
 import speculative_decoding_verify_split_gb300 as va
 from speculative_decoding_verify_split_gb300.workloads import make_workload, named_workload
 from oracle.attention_fp64 import oracle_from_torch
-from gpu_util import compare, rows_of
+from gpu_util import compare
 
 pytestmark = pytest.mark.gpu
 
@@ -108,14 +108,10 @@ def test_all_variants_with_forced_splits(ci):
         compare(got, ref)
 
 
-def test_long_context_window_sampled():
+def test_long_context_window_every_sequence():
     w = named_workload("long_context_fp8", value_device="cuda").to("cuda")
     got = run_opt(w, window_left=4096)
-    kv = w.kv_lens
-    seqs = [int(np.argmin(kv)), int(np.argmax(kv))]
-    ref = oracle(w, seqs, window_left=4096)
-    r = rows_of(w.to("cpu"), seqs)
-    compare(got[torch.as_tensor(r, device="cuda")], ref[r])
+    print("window 4096", compare(got, oracle(w, window_left=4096)))
 
 
 def test_options_are_validated():
