@@ -117,6 +117,8 @@ typedef struct va_plan {
  * first call with the largest shape before capturing a CUDA graph, or use
  * verify_attn_ex with a caller workspace. Calls that share the library
  * workspace must be ordered on one stream (concurrent streams race on it).
+ * verify_attn_last_device_error(NULL, ...) reports a bounded wait that ran
+ * out in a call made with it.
  */
 va_status verify_attn(const va_tensor* q, const va_tensor* k_cache, const va_tensor* v_cache,
                       const va_tensor* block_table, const va_tensor* cu_seqlens_q,
@@ -139,7 +141,9 @@ va_status verify_attn(const va_tensor* q, const va_tensor* k_cache, const va_ten
  * event_after_main NULL, or a cudaEvent_t recorded on `stream` between the
  *                  main and the merge kernel (lets a caller time the main
  *                  kernel alone with CUDA events on the launching stream).
- * The workspace holds no state between calls.
+ * The workspace holds no state between calls, except its status word (the
+ * first 4 bytes; zero it before first use), which a bounded wait that runs out
+ * sets and verify_attn_last_device_error reads and clears.
  */
 va_status verify_attn_ex(const va_tensor* q, const va_tensor* k_cache, const va_tensor* v_cache,
                          const va_tensor* block_table, const va_tensor* cu_seqlens_q,
@@ -256,6 +260,10 @@ va_status verify_attn_opt(const va_tensor* q, const va_tensor* k_cache, const va
  *    behind. Nothing in it needs to start at zero, but calls that overlap on
  *    the GPU (different streams, or different host threads) race on it:
  *    order them on one stream.
+ *  - The array's first word is the status word of the kernels' bounded
+ *    waits, shared by every call on the device. This call never clears it;
+ *    verify_attn_last_device_error(NULL, ...) reads and clears it (and
+ *    synchronises the stream it is given, so call it between batches).
  */
 #define VERIFY_ATTN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
@@ -411,6 +419,49 @@ va_status verify_attn_partial(const va_tensor* q, const va_tensor* k_cache, cons
  */
 va_status verify_attn_merge_partials(int32_t n, const va_tensor* o_parts, const va_tensor* lse_parts,
                                      va_tensor* out, void* stream);
+
+/*
+ * verify_attn_last_device_error - reads and clears the device status word of
+ * a workspace. This turns the pages' gates and asserts (sglang PR 36330 digest,
+ * "Key code excerpts") into something a caller can check after launch: a
+ * condition found on the device, when no host check could see it.
+ *
+ * Every wait of the main kernels (a ring slot, a TMA copy landing, an MMA
+ * finishing) is bounded in time (2 s unless verify_attn_set_wait_limit says
+ * otherwise). A wait that runs out makes the kernel stop issuing work, let
+ * its copies and MMAs in flight finish, free its tensor memory and return;
+ * it ORs a nonzero code into the status word of the call's workspace. The
+ * outputs of that call are then unspecified. The status word is sticky:
+ * kernels only ever set bits in it.
+ *
+ *  workspace  the 256-byte-aligned workspace pointer that was passed to
+ *             verify_attn_ex, verify_attn_opt, verify_attn_mla or
+ *             verify_attn_partial; or NULL for the library's own scratch on
+ *             the current device: the workspace of calls made without one
+ *             (verify_attn, and the others with a NULL workspace) and the
+ *             built-in array of verify_attn_noalloc. The library's workspace
+ *             is replaced when it grows; its word then starts at 0 again.
+ *  bits       host int32, written: the OR of the words read (0 = no bounded
+ *             wait ran out since the last read and clear). Nonzero bits name
+ *             the wait that gave up; they are diagnostic, not an API.
+ *  stream     the words are read after the work queued on `stream` (this
+ *             call synchronises it), then cleared on it. Calls on other
+ *             streams that use the same scratch must be ordered by the caller.
+ * Returns VA_ERR_NULL for a NULL bits, VA_ERR_WORKSPACE for a misaligned
+ * workspace, VA_ERR_CUDA if a copy or the synchronisation fails.
+ */
+va_status verify_attn_last_device_error(const void* workspace, int32_t* bits, void* stream);
+
+/*
+ * verify_attn_set_wait_limit - the time limit, in nanoseconds, of the main
+ * kernels' bounded waits for launches made after this call, process-wide; 0
+ * restores the default of 2 s. A hook for tests of the timeout path: a limit
+ * of a few nanoseconds makes waits run out on any input, so that a test can
+ * check that the call still returns, the status word is set and the next
+ * call is correct. Not for production use (any limit shorter than the
+ * kernels' normal waits makes every call fail). Always returns VA_OK.
+ */
+va_status verify_attn_set_wait_limit(uint64_t limit_ns);
 
 /* Static, NUL-terminated name of a status code. */
 const char* verify_attn_status_string(int32_t status);

@@ -30,7 +30,8 @@ _DTYPES = {torch.bfloat16: VA_BF16, torch.float8_e4m3fn: VA_FP8_E4M3,
 EXPORTS = ("verify_attn", "verify_attn_ex", "verify_attn_check", "verify_attn_plan",
            "verify_attn_workspace_size", "verify_attn_status_string", "verify_attn_noalloc",
            "verify_attn_block_table_from_indptr", "verify_attn_opt", "verify_attn_mla",
-           "verify_attn_mla_workspace_size", "verify_attn_partial", "verify_attn_merge_partials")
+           "verify_attn_mla_workspace_size", "verify_attn_partial", "verify_attn_merge_partials",
+           "verify_attn_last_device_error", "verify_attn_set_wait_limit")
 
 # Absorbed-MLA latent cache: row = [latent (MLA_NOPE) | rope key (MLA_PE)].
 MLA_NOPE, MLA_PE = 512, 64
@@ -111,6 +112,11 @@ def _lib():
         lib.verify_attn_partial.restype = ctypes.c_int32
         lib.verify_attn_merge_partials.argtypes = [ctypes.c_int32, P, P, P, ctypes.c_void_p]
         lib.verify_attn_merge_partials.restype = ctypes.c_int32
+        lib.verify_attn_last_device_error.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32),
+                                                      ctypes.c_void_p]
+        lib.verify_attn_last_device_error.restype = ctypes.c_int32
+        lib.verify_attn_set_wait_limit.argtypes = [ctypes.c_uint64]
+        lib.verify_attn_set_wait_limit.restype = ctypes.c_int32
         lib.verify_attn_status_string.argtypes = [ctypes.c_int32]
         lib.verify_attn_status_string.restype = ctypes.c_char_p
         _LIB = lib
@@ -228,6 +234,39 @@ def verify_attn_noalloc(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_
     if s != VA_OK:
         raise VerifyAttnError(s, "verify_attn_noalloc")
     return out
+
+
+def _workspace_addr(workspace: Optional[torch.Tensor]) -> int:
+    """The 256-byte-aligned address the wrappers pass for a workspace tensor."""
+    if workspace is None:
+        return 0
+    a = workspace.data_ptr()
+    return a + (-a) % 256
+
+
+def last_device_error(workspace: Optional[torch.Tensor] = None, stream=None, device=None) -> int:
+    """Reads and clears the status word of bounded waits that ran out (0 =
+    none): of ``workspace`` as the wrappers passed it, or with None, of the
+    library's own scratch on the device (its workspace and the no-alloc
+    array). Synchronises ``stream`` (see include/verify_attn.h)."""
+    if workspace is not None:
+        dev = workspace.device
+    else:
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    bits = ctypes.c_int32(0)
+    with torch.cuda.device(dev):
+        s = _lib().verify_attn_last_device_error(ctypes.c_void_p(_workspace_addr(workspace)),
+                                                 ctypes.byref(bits),
+                                                 ctypes.c_void_p(_stream_handle(stream, dev)))
+    if s != VA_OK:
+        raise VerifyAttnError(s, "verify_attn_last_device_error")
+    return int(bits.value)
+
+
+def set_wait_limit(limit_ns: int) -> None:
+    """Time limit of the kernels' bounded waits for later launches (0 = the
+    default 2 s). A test hook for the timeout path."""
+    _lib().verify_attn_set_wait_limit(int(limit_ns))
 
 
 def workspace_status(workspace: torch.Tensor) -> int:

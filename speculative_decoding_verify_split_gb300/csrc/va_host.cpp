@@ -1,5 +1,6 @@
 // Host side of the C ABI (include/verify_attn.h): argument validation, the
 // split heuristic, the library-owned workspace and the kernel launches.
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstring>
@@ -221,6 +222,15 @@ static bool make_kv_map(CUtensorMap* m, const va_tensor* t, int64_t nb, int64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Limit of the main kernels' bounded waits for the next launches; 0 means
+// kDefaultWaitLimitNs (see verify_attn_set_wait_limit).
+static std::atomic<uint64_t> g_wait_limit_ns{0};
+
+uint64_t wait_limit_ns() {
+  const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return v ? v : kDefaultWaitLimitNs;
+}
+
 struct DeviceState {
   bool ready = false;
   int sms = 0;
@@ -317,6 +327,7 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
   p.piece_cost = piece_cost_for(
       plan, tiles_upper_bound(sh.num_seqs, sh.hkv, max_q, max_k, plan.tile_keys, p.window_left));
   p.dv = kHeadDim;
+  p.wait_limit_ns = wait_limit_ns();
   if (part) {
     p.partial = 1;
     p.kv_extent = part->kv_extent ? static_cast<const int32_t*>(part->kv_extent->data) : nullptr;
@@ -485,6 +496,7 @@ va_status launch_mla(const va_tensor* q, const va_tensor* kv, const va_tensor* b
   p.num_work = plan.num_work;
   p.piece_cost = kMlaPieceCostTiles;
   p.dv = kMlaNope;
+  p.wait_limit_ns = wait_limit_ns();
   const WorkspaceLayout lay =
       workspace_layout(plan.num_work, plan.num_splits, mla_row_stride(plan.max_rows), kMlaNope);
   char* base = static_cast<char*>(ws);
@@ -498,6 +510,24 @@ va_status launch_mla(const va_tensor* q, const va_tensor* kv, const va_tensor* b
   if (launch_mla_tc(p, tm, stream) != cudaSuccess) return VA_ERR_CUDA;
   if (ev_mid && cudaEventRecord(ev_mid, stream) != cudaSuccess) return VA_ERR_CUDA;
   if (launch_merge(p, stream) != cudaSuccess) return VA_ERR_CUDA;
+  return VA_OK;
+}
+
+// The library's per-device workspace, grown to `bytes` if smaller. Grow only:
+// cudaFree waits for work already queued on the old buffer. A new buffer's
+// status word is zeroed on the caller's stream (the rest needs no clearing).
+// Caller holds g_mu.
+static va_status library_workspace(DeviceState* st, size_t bytes, cudaStream_t stream) {
+  if (bytes <= st->ws_bytes) return VA_OK;
+  if (st->ws) cudaFree(st->ws);
+  st->ws = nullptr;
+  st->ws_bytes = 0;
+  if (cudaMalloc(&st->ws, bytes) != cudaSuccess) {
+    st->ws = nullptr;
+    return VA_ERR_CUDA;
+  }
+  if (cudaMemsetAsync(st->ws, 0, 256, stream) != cudaSuccess) return VA_ERR_CUDA;
+  st->ws_bytes = bytes;
   return VA_OK;
 }
 
@@ -571,18 +601,8 @@ static va_status run_call(const va_tensor* q, const va_tensor* k_cache, const va
   if (s != VA_OK) return s;
   if (own_ws) {
     if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;
-    if ((size_t)plan.workspace_bytes > st->ws_bytes) {
-      // Grow only. cudaFree waits for work already queued on the old buffer.
-      if (st->ws) cudaFree(st->ws);
-      st->ws = nullptr;
-      st->ws_bytes = 0;
-      if (cudaMalloc(&st->ws, (size_t)plan.workspace_bytes) != cudaSuccess) {
-        st->ws = nullptr;
-        return VA_ERR_CUDA;
-      }
-      if (cudaMemset(st->ws, 0, (size_t)plan.workspace_bytes) != cudaSuccess) return VA_ERR_CUDA;
-      st->ws_bytes = (size_t)plan.workspace_bytes;
-    }
+    s = library_workspace(st, (size_t)plan.workspace_bytes, stream);
+    if (s != VA_OK) return s;
     workspace = st->ws;
     workspace_bytes = st->ws_bytes;
   } else {
@@ -688,17 +708,8 @@ VA_EXPORT va_status verify_attn_mla(const va_tensor* q, const va_tensor* kv_cach
   if (s != VA_OK) return s;
   if (!workspace) {
     if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;
-    if ((size_t)plan.workspace_bytes > st->ws_bytes) {
-      if (st->ws) cudaFree(st->ws);
-      st->ws = nullptr;
-      st->ws_bytes = 0;
-      if (cudaMalloc(&st->ws, (size_t)plan.workspace_bytes) != cudaSuccess) {
-        st->ws = nullptr;
-        return VA_ERR_CUDA;
-      }
-      if (cudaMemset(st->ws, 0, (size_t)plan.workspace_bytes) != cudaSuccess) return VA_ERR_CUDA;
-      st->ws_bytes = (size_t)plan.workspace_bytes;
-    }
+    s = library_workspace(st, (size_t)plan.workspace_bytes, static_cast<cudaStream_t>(stream));
+    if (s != VA_OK) return s;
     workspace = st->ws;
     workspace_bytes = st->ws_bytes;
   } else {
@@ -771,17 +782,8 @@ VA_EXPORT va_status verify_attn_partial(const va_tensor* q, const va_tensor* k_c
   if (s != VA_OK) return s;
   if (!workspace) {
     if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;
-    if ((size_t)plan.workspace_bytes > st->ws_bytes) {
-      if (st->ws) cudaFree(st->ws);
-      st->ws = nullptr;
-      st->ws_bytes = 0;
-      if (cudaMalloc(&st->ws, (size_t)plan.workspace_bytes) != cudaSuccess) {
-        st->ws = nullptr;
-        return VA_ERR_CUDA;
-      }
-      if (cudaMemset(st->ws, 0, (size_t)plan.workspace_bytes) != cudaSuccess) return VA_ERR_CUDA;
-      st->ws_bytes = (size_t)plan.workspace_bytes;
-    }
+    s = library_workspace(st, (size_t)plan.workspace_bytes, static_cast<cudaStream_t>(stream));
+    if (s != VA_OK) return s;
     workspace = st->ws;
     workspace_bytes = st->ws_bytes;
   } else {
@@ -832,6 +834,50 @@ VA_EXPORT va_status verify_attn_merge_partials(int32_t n, const va_tensor* o_par
     m.lse_s1[i] = l->stride[1];
   }
   return launch_merge_shards(m, static_cast<cudaStream_t>(stream)) == cudaSuccess ? VA_OK : VA_ERR_CUDA;
+}
+
+VA_EXPORT va_status verify_attn_set_wait_limit(uint64_t limit_ns) {
+  g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+  return VA_OK;
+}
+
+// Reads the status word at `word` after the work queued on `stream`, ORs it
+// into *bits and queues its clearing.
+static va_status take_status(void* word, int32_t* bits, cudaStream_t stream) {
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, word, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return VA_ERR_CUDA;
+  *bits |= v;
+  if (v != 0 && cudaMemsetAsync(word, 0, sizeof(v), stream) != cudaSuccess) return VA_ERR_CUDA;
+  return VA_OK;
+}
+
+VA_EXPORT va_status verify_attn_last_device_error(const void* workspace, int32_t* bits, void* stream) {
+  if (!bits) return VA_ERR_NULL;
+  *bits = 0;
+  cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+  if (workspace) {
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return VA_ERR_WORKSPACE;
+    return take_status(const_cast<void*>(workspace), bits, st_);
+  }
+  void* lib_ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* st = nullptr;
+    const va_status s = device_state(&st);
+    if (s != VA_OK) return s;
+    lib_ws = st->ws;
+  }
+  if (lib_ws) {
+    const va_status s = take_status(lib_ws, bits, st_);
+    if (s != VA_OK) return s;
+  }
+  void* scratch = nullptr;
+  va_status s = noalloc_scratch(&scratch, false);
+  if (s != VA_OK) return s;
+  if (scratch) s = take_status(scratch, bits, st_);
+  return s;
 }
 
 VA_EXPORT const char* verify_attn_status_string(int32_t status) {

@@ -50,4 +50,12 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
 // SM count of the current device (initialises the per-device state once).
 va_status current_device_sms(int* sms);
 
+// Limit of the main kernels' bounded waits for launches made now, in ns.
+uint64_t wait_limit_ns();
+
+// Device address of verify_attn_noalloc's built-in scratch on the current
+// device. With lookup, looks it up on first use; without, *out is NULL until
+// a verify_attn_noalloc call on this device has looked it up.
+va_status noalloc_scratch(void** out, bool lookup);
+
 }  // namespace va_host_impl

@@ -73,11 +73,20 @@ struct Params {
   // tiles.
   int32_t tile_keys, num_splits, max_rows, num_work, piece_cost;
   int32_t dv;          // output (value) columns: kHeadDim, or kMlaNope over a latent cache
+  // Limit of every bounded wait of the main kernels, in ns (kDefaultWaitLimitNs
+  // unless a test shortened it to make waits run out).
+  uint64_t wait_limit_ns;
   int32_t* ws_status;  // sticky error bits (a bounded wait timed out); never cleared by kernels
   int32_t* ws_meta;  // [num_work + 1]: first tile of each work item (split units), then the total
   float* ws_ml;      // [pieces][max_rows][2]: running max (log2 units), row sum
   float* ws_acc;     // [pieces][max_rows][dv]: unnormalised output rows
 };
+
+// A bounded wait of the main kernels gives up after this long (by
+// %globaltimer), sets the workspace status word and lets the kernel wind down.
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+// The drains on the way out (copies and MMAs in flight) wait this long at most.
+constexpr uint64_t kDrainLimitNs = 100000000ull;  // 100 ms
 
 // Workspace layout. pieces = num_work + num_splits: a work item split over
 // CTAs c0..c1 stores the partial of CTA c at piece j + c, which is unique

@@ -142,7 +142,6 @@ constexpr float kHeadroom = 1.f;    // m_ref = tile max + kHeadroom when it move
 constexpr float kHeadroomFirst = 4.f;  // ... and + kHeadroomFirst for a row's first reference
 constexpr float kOvershoot = 2.8f;  // move only if the tile max > m_ref + kOvershoot (P <= 2^8.8 < 448)
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 constexpr int kMaxSlots = 5;
 // Barrier slots (8 bytes each) after kOffBar.
@@ -162,7 +161,7 @@ enum : int {
   kBarDrain,
   kNumBars
 };
-static_assert(8 * kNumBars + 16 + 34 * 8 <= 1024, "barrier area");
+static_assert(8 * kNumBars + 16 + 34 * 8 + 4 * 2 * kMaxSlots <= 1024, "barrier area");
 
 template <bool FP8>
 __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -193,6 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   long long* scratch = reinterpret_cast<long long*>(sm + C::kOffBar + 8 * kNumBars + 16);  // 32 slots
   long long* s_ts = scratch + 32;
   int* s_j = reinterpret_cast<int*>(scratch + 33);
+  // last tile issued into each ring slot: [K slots | V slots], for the drain
+  volatile int* slot_tile = reinterpret_cast<volatile int*>(scratch + 34);
   float* xch = reinterpret_cast<float*>(sm + C::kOffX);
 
   const int tid = threadIdx.x;
@@ -231,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarOFree), kSwWarps);
     mbar_init(bar(kBarDrain), 2);
     *abort_flag = 0;
+    for (int s = 0; s < 2 * kMaxSlots; ++s) slot_tile[s] = -1;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -274,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bar_empty = is_k ? kBarEmptyK : kBarEmptyV;
     const uint32_t ring = sbase + (is_k ? 0u : (uint32_t)(C::kKSlots * C::kTensorBytes));
     const void* tmap = is_k ? (const void*)&tm_k : (const void*)&tm_v;
+    volatile int* ring_tile = slot_tile + (is_k ? 0 : kMaxSlots);
     constexpr int kBoxes = kPagesPerTile * C::kChunks;  // boxes per tile
     static_assert(kBoxes <= 32, "one box per lane");
     const uint64_t kv_policy = l2_evict_first_policy();  // K and V are read once
@@ -314,14 +317,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           nvalid += v ? 1u : 0u;
         }
         const bool got = __all_sync(
-            0xffffffffu, mbar_wait(bar(bar_empty + s), ((it / nslots) & 1) ^ 1, abort_flag, kWaitLimitNs));
+            0xffffffffu, mbar_wait(bar(bar_empty + s), ((it / nslots) & 1) ^ 1, abort_flag, p.wait_limit_ns));
         if (!got) {  // warp-uniform
           if (lane == 0) fail(p, abort_flag, 1);
           ok = false;
           break;
         }
         const uint32_t dst = ring + s * C::kTensorBytes;
-        if (lane == 0) mbar_arrive_expect_tx(bar(bar_full + s), nvalid * (uint32_t)C::kPageBytes);
+        if (lane == 0) {
+          ring_tile[s] = it;
+          mbar_arrive_expect_tx(bar(bar_full + s), nvalid * (uint32_t)C::kPageBytes);
+        }
         __syncwarp();
         if (lane < kBoxes) {  // lane -> (page, 128-byte d chunk)
           const int i = lane / C::kChunks, ch = lane % C::kChunks;
@@ -336,13 +342,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
     }
-    if (!ok) {
-      // let copies already in flight land before the CTA goes away
-      for (int k = (it > nslots ? it - nslots : 0); k < it; ++k) {
+    // Copies still in flight land before the CTA goes away, also when another
+    // role gave up (then nobody consumes them). This producer's tiles that may
+    // be in flight are among the last nslots + nprod - 1 tiles it walked: its
+    // last issued tile z is at most nprod tiles back, and a tile is issued
+    // only once the tile nslots before it in the ring was consumed.
+    if (lane == 0) {
+      for (int k = (it > nslots + nprod - 1 ? it - nslots - nprod + 1 : 0); k < it; ++k) {
         if (k % nprod != prod) continue;
-        mbar_wait(bar(bar_full + k % nslots), (k / nslots) & 1, abort_flag, 10000000ull);
+        drain_ring_tile(bar(bar_full + k % nslots), k, nslots, ring_tile + k % nslots, kDrainLimitNs);
       }
     }
+    __syncwarp();
   } else if (warp == 1 || warp == 12) {
     // ======================= MMA issuers ==========================================
     // Warp 1 issues Q K^T into the S buffers, warp 12 issues P V into O: the
@@ -358,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       auto wait_or_fail = [&](int b, uint32_t par, int code) {
         if (!ok) return false;
-        if (!mbar_wait(bar(b), par, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait(bar(b), par, abort_flag, p.wait_limit_ns)) {
           fail(p, abort_flag, code);
           ok = false;
         }
@@ -428,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every tensor-core operation of both issuers has finished before TMEM is freed
       mma_commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, abort_flag, 100000000ull);
+      mbar_wait_drain(bar(kBarDrain), 0, kDrainLimitNs);
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
@@ -457,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // meet at every exchange barrier.
     auto wait_or_fail = [&](int b, uint32_t par, int code) {
       if (!ok) return false;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(bar(b), par, abort_flag, kWaitLimitNs));
+      const bool got = __all_sync(0xffffffffu, mbar_wait(bar(b), par, abort_flag, p.wait_limit_ns));
       if (!got) {
         if (lane == 0) fail(p, abort_flag, code);
         ok = false;

@@ -97,7 +97,6 @@ constexpr float kPShift = 6.f;
 constexpr float kHeadroom = 1.f;
 constexpr float kHeadroomFirst = 4.f;
 constexpr float kOvershoot = 2.8f;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 enum : int {
   kBarFull = 0,
@@ -114,11 +113,13 @@ enum : int {
   kNumBars
 };
 // barrier area: mbarriers | TMEM address, abort flag | scan scratch (34 x 8) |
-// per-row factors [2 rounds][64] floats at +512
+// last tile issued into each ring slot | per-row factors [2 rounds][64] floats
+// at +512
 constexpr int kOffTmemSlot = 8 * kNumBars;
 constexpr int kOffScratch = 192;
+constexpr int kOffSlotTile = kOffScratch + 34 * 8;  // last tile issued into each slot
 constexpr int kOffRowVals = 512;
-static_assert(kOffTmemSlot + 8 <= kOffScratch && kOffScratch + 34 * 8 <= kOffRowVals, "barrier area");
+static_assert(kOffTmemSlot + 8 <= kOffScratch && kOffSlotTile + 4 * kSlots <= kOffRowVals, "barrier area");
 
 // Four bf16 values (two words) times 2^e -> e4m3 hi and lo bytes, in order.
 __device__ __forceinline__ void split_q4(uint32_t wa, uint32_t wb, float up, uint32_t& hi, uint32_t& lo) {
@@ -154,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_j = reinterpret_cast<int*>(scratch + 33);
   float* xch = reinterpret_cast<float*>(sm + kOffX);
   float* row_vals = reinterpret_cast<float*>(sm + kOffBar + kOffRowVals);  // [2][64]
+  volatile int* slot_tile = reinterpret_cast<volatile int*>(sm + kOffBar + kOffSlotTile);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -186,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarOFree), kSwWarps);
     mbar_init(bar(kBarDrain), 2);
     *abort_flag = 0;
+    for (int s = 0; s < kSlots; ++s) slot_tile[s] = -1;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -262,14 +265,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           nvalid += v ? 1u : 0u;
         }
         const bool got = __all_sync(
-            0xffffffffu, mbar_wait(bar(kBarEmpty + s), ((it / kSlots) & 1) ^ 1, abort_flag, kWaitLimitNs));
+            0xffffffffu, mbar_wait(bar(kBarEmpty + s), ((it / kSlots) & 1) ^ 1, abort_flag, p.wait_limit_ns));
         if (!got) {
           if (lane == 0) fail(p, abort_flag, 1);
           ok = false;
           break;
         }
         const uint32_t dst = sbase + s * kTileBytes;
-        if (lane == 0) mbar_arrive_expect_tx(bar(kBarFull + s), nvalid * (uint32_t)(kRegions * 2048));
+        if (lane == 0) {
+          slot_tile[s] = it;
+          mbar_arrive_expect_tx(bar(kBarFull + s), nvalid * (uint32_t)(kRegions * 2048));
+        }
         __syncwarp();
         if (lane < kBoxes) {  // lane -> (page, 128-byte column chunk)
           const int i = lane / kRegions, ch = lane % kRegions;
@@ -284,12 +290,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
     }
-    if (!ok) {  // let copies in flight land before the CTA goes away
-      for (int k = (it > kSlots ? it - kSlots : 0); k < it; ++k) {
+    // Copies still in flight land before the CTA goes away, also when another
+    // role gave up (the window: see the GQA kernel's producers).
+    if (lane == 0) {
+      for (int k = (it > kSlots + kProducers - 1 ? it - kSlots - kProducers + 1 : 0); k < it; ++k) {
         if (k % kProducers != prod) continue;
-        mbar_wait(bar(kBarFull + k % kSlots), (k / kSlots) & 1, abort_flag, 10000000ull);
+        drain_ring_tile(bar(kBarFull + k % kSlots), k, kSlots, slot_tile + k % kSlots, kDrainLimitNs);
       }
     }
+    __syncwarp();
   } else if (warp == 1 || warp == 12) {
     // ======================= MMA issuers ==========================================
     if (lane == 0) {
@@ -302,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       auto wait_or_fail = [&](int b, uint32_t par, int code) {
         if (!ok) return false;
-        if (!mbar_wait(bar(b), par, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait(bar(b), par, abort_flag, p.wait_limit_ns)) {
           fail(p, abort_flag, code);
           ok = false;
         }
@@ -370,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++piece_idx;
       }
       mma_commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, abort_flag, 100000000ull);
+      mbar_wait_drain(bar(kBarDrain), 0, kDrainLimitNs);
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
@@ -395,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // and tiles "dry" so that every named barrier still sees all its threads.
     auto wait_or_fail = [&](int b, uint32_t par, int code) {
       if (!ok) return false;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(bar(b), par, abort_flag, kWaitLimitNs));
+      const bool got = __all_sync(0xffffffffu, mbar_wait(bar(b), par, abort_flag, p.wait_limit_ns));
       if (!got) {
         if (lane == 0) fail(p, abort_flag, code);
         ok = false;

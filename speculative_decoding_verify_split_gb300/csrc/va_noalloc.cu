@@ -29,13 +29,19 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up once).
-va_status scratch_address(void** out) {
+}  // namespace
+
+namespace va_host_impl {
+
+// Device address of the scratch array on the current device (looked up once,
+// with that device current).
+va_status noalloc_scratch(void** out, bool lookup) {
+  *out = nullptr;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return VA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return VA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (!g_scratch_ptr[dev] && lookup) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return VA_ERR_CUDA;
     g_scratch_ptr[dev] = ptr;
@@ -44,7 +50,7 @@ va_status scratch_address(void** out) {
   return VA_OK;
 }
 
-}  // namespace
+}  // namespace va_host_impl
 
 using namespace va_host_impl;
 
@@ -67,10 +73,12 @@ VA_EXPORT va_status verify_attn_noalloc(const va_tensor* q, const va_tensor* k_c
   if ((size_t)plan.workspace_bytes > kNoAllocScratchBytes) return VA_ERR_WORKSPACE;
   if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;
   void* scratch = nullptr;
-  s = scratch_address(&scratch);
+  s = noalloc_scratch(&scratch, true);
   if (s != VA_OK) return s;
   // Nothing in the scratch has to start at zero: every byte the merge kernel
-  // reads is written earlier in the same call by the main kernel.
+  // reads is written earlier in the same call by the main kernel. Its first
+  // word is the status word of bounded waits that ran out (sticky, as in a
+  // workspace); verify_attn_last_device_error(NULL, ...) reads and clears it.
   return launch(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, max_seqlen_q,
                 max_seqlen_k, softmax_scale, k_descale, v_descale, out, sh, plan, scratch,
                 kNoAllocScratchBytes, nullptr, static_cast<cudaStream_t>(stream));

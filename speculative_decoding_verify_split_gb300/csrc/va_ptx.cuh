@@ -68,6 +68,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// The same wait without the abort flag, for the drains on the way out (copies
+// and MMAs in flight must land before the CTA ends or frees TMEM, also after
+// another role gave up). Still gives up after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Waits, on the way out, for the TMA copy of ring tile k (ring slot s, its full
+// barrier `bar`) to land, unless the slot has been refilled since (*slot_tile,
+// the last tile issued into slot s, is no longer k: then tile k was consumed,
+// so it landed). Needed because the full barrier's parity names tile k only
+// while the slot holds it. Gives up after `limit_ns`.
+__device__ __forceinline__ bool drain_ring_tile(uint32_t bar, int k, int nslots,
+                                                const volatile int* slot_tile, uint64_t limit_ns) {
+  const uint32_t parity = (uint32_t)((k / nslots) & 1);
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (*slot_tile != k) return true;
+    if (mbar_test_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // ---- fences -------------------------------------------------------------------
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
