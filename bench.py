@@ -467,7 +467,7 @@ def run_ours(args):
         inputs = ("q", "k_cache", "v_cache", "block_table", "cu_seqlens_q", "seqused_k")
         kernel = MAIN_KERNEL[w.kv_dtype]
     alg = w.algorithmic_bytes()
-    ws = torch.empty(n_ws + 256, dtype=torch.uint8, device=dev)
+    ws = torch.zeros(n_ws + 256, dtype=torch.uint8, device=dev)
 
     def step(ev_mid=None):
         if mla:

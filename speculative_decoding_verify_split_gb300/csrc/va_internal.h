@@ -153,9 +153,10 @@ cudaError_t prepare_main_tc();  // once per device: opt in to its shared memory
 constexpr int kMlaTileKeys = 64;
 // Split cost of starting an item on the latent path, in 64-key tiles: Q
 // staging (576 columns) and the 128 KB partial of the previous piece, both
-// through a memory system saturated by the ring. Swept over 6/12/18/24/32 on
-// the mid- and long-context latent workloads: 18.
-constexpr int kMlaPieceCostTiles = 18;
+// through a memory system saturated by the ring. Swept over 12/18/24 on the
+// mid- and long-context latent workloads (same box, back to back): 12 is
+// best by ~1.5 us on both.
+constexpr int kMlaPieceCostTiles = 12;
 cudaError_t prepare_mla_tc();
 cudaError_t launch_mla_tc(const Params& p, const CUtensorMap& tm_kv, cudaStream_t stream);
 cudaError_t launch_main_tc(const Params& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,

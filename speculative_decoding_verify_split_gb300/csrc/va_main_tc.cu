@@ -617,6 +617,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         float x[kKpt];  // logits of keys [kKpt qtr, +kKpt) of this tile, this row
 #pragma unroll
         for (int i = 0; i < kKpt; ++i) x[i] = -INFINITY;
+        // x[] holds logits in log2 units, or with a soft cap c (log2 units)
+        // tanh(logit / c): the logit is then xs * x (xs = c), applied inside
+        // the ex2 of P as one FMA, so the cap costs one SFU op per key
+        float rx = rs;
+        float xs = 1.f;
+        if constexpr (VAR) {
+          if (p.softcap_log2 > 0.f) {
+            xs = p.softcap_log2;
+            rx = rs / xs;
+          }
+        }
         if (wait_or_fail(kBarSFull + b, (cur / kSBufs) & 1, 256)) {
           tc_fence_after();
           if constexpr (FP8) {
@@ -633,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) {
               const float mine = __uint_as_float(sub ? vb[i] : va[i]);
               const float give = __uint_as_float(sub ? va[i] : vb[i]);
-              x[i] = (mine + __shfl_xor_sync(0xffffffffu, give, 16)) * rs;
+              x[i] = (mine + __shfl_xor_sync(0xffffffffu, give, 16)) * rx;
             }
           } else {
             uint32_t v[16];
@@ -643,19 +654,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarSFree + b));
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(v[i]) * rs;
+            for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(v[i]) * rx;
           }
           if constexpr (VAR) {
             if (p.softcap_log2 > 0.f) {
-              // soft cap in log2 units, c tanh(x / c), before masking, with
-              // tanh(y) = 1 - 2 / (1 + e^(2y)) (ends at -1 and 1 without
-              // overflow). A Taylor polynomial for small |y| measured no
-              // faster: the extra instructions per key, not the special-
-              // function unit, bound this path.
-              const float c = p.softcap_log2;
-              const float k2 = 2.f * kLog2e / c;
+              // soft cap c tanh(logit / c), before masking, kept as the tanh
+              // (see xs). tanh.approx's relative error of ~2^-11 moves a
+              // logit l by at most |l| 2^-11 log2 units (0.5 % of a key's
+              // weight at l = 10).
 #pragma unroll
-              for (int i = 0; i < kKpt; ++i) x[i] = c - __fdividef(2.f * c, 1.f + ex2(x[i] * k2));
+              for (int i = 0; i < kKpt; ++i) x[i] = tanh_approx(x[i]);
             }
           }
           const int key0 = lt * kT + kKpt * qtr;
@@ -675,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float tmax = -INFINITY;
 #pragma unroll
         for (int i = 0; i < kKpt; i += 2) tmax = fmaxf(tmax, fmaxf(x[i], x[i + 1]));
-        tmax = exchange(tmax, true);
+        tmax = exchange(tmax * xs, true);  // log2 units (xs > 0 keeps the order)
         if (!ok) continue;
 
         // P buffer pb was last read by PV(cur - kPBufs). (A TMEM P goes over
@@ -729,8 +737,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t ph[8], pl[8];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float a = live ? ex2(x[2 * i] - mref_s) : 0.f;
-            const float bb = live ? ex2(x[2 * i + 1] - mref_s) : 0.f;
+            const float a = live ? ex2(fmaf(x[2 * i], xs, -mref_s)) : 0.f;
+            const float bb = live ? ex2(fmaf(x[2 * i + 1], xs, -mref_s)) : 0.f;
             ls0 += a;
             ls1 += bb;
             uint32_t h2, l2;
@@ -763,8 +771,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pw[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float a = live ? ex2(x[2 * i] - mref_s) : 0.f;
-            const float bb = live ? ex2(x[2 * i + 1] - mref_s) : 0.f;
+            const float a = live ? ex2(fmaf(x[2 * i], xs, -mref_s)) : 0.f;
+            const float bb = live ? ex2(fmaf(x[2 * i + 1], xs, -mref_s)) : 0.f;
             ls0 += a;
             ls1 += bb;
             pw[i] = pack_bf16x2(a, bb);

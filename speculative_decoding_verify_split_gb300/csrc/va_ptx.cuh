@@ -313,6 +313,14 @@ __device__ __forceinline__ void tmem_ld_16x32bx2_x8(uint32_t taddr, uint32_t (&r
       : "r"(taddr), "n"(SPLIT));
 }
 
+// tanh(x) on the SFU: one tanh.approx.f32 (relative error about 2^-11 over
+// the whole range, exact limits -1 and 1).
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // 2^x on the SFU (ex2.approx.ftz: flushes subnormal results to zero).
 __device__ __forceinline__ float ex2(float x) {
   float y;
