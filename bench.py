@@ -34,7 +34,7 @@ UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 MAIN_KERNEL = {"fp8_e4m3": "va_main_tc_kernel<true, false>", "bf16": "va_main_tc_kernel<false, false>",
-               "mla": "va_mla_tc_kernel"}
+               "mla": "va_mla_tc_kernel", "mla_bf16": "va_mla_bf16_tc_kernel"}
 
 
 def is_mla(name):
@@ -459,7 +459,7 @@ def run_ours(args):
         out = torch.empty(w.q.shape[0], w.q.shape[1], va.MLA_NOPE, dtype=torch.bfloat16, device=dev)
         n_ws = va.mla_workspace_size(w.q, w.seqused_k, w.max_seqlen_q, w.max_seqlen_k)
         inputs = ("q", "kv_cache", "block_table", "cu_seqlens_q", "seqused_k")
-        kernel = MAIN_KERNEL["mla"]
+        kernel = MAIN_KERNEL["mla" if w.kv_dtype == "fp8_e4m3" else "mla_bf16"]
     else:
         w = named_workload(args.workload, seed=0, value_device=str(dev)).to(dev)
         out = torch.empty_like(w.q)
@@ -627,7 +627,8 @@ def run_reference(args):
     mla = is_mla(args.workload)
     if mla:
         from oracle.mla_fp64 import mla_oracle_from_torch as oracle_from_torch
-        st = dict(mla_workload_structure(args.workload, 0), Hkv=1, kv_dtype="fp8_e4m3")
+        st = dict(mla_workload_structure(args.workload, 0), Hkv=1)
+        st.setdefault("kv_dtype", "fp8_e4m3")
     else:
         from oracle.attention_fp64 import oracle_from_torch
         st = workload_structure(args.workload, 0)
@@ -638,7 +639,7 @@ def run_reference(args):
     def sample(b, cap, seed):
         S = min(kv_lens[b], cap)
         if mla:
-            w = make_mla_workload([q_lens[b]], [S], st["Hq"], seed=seed)
+            w = make_mla_workload([q_lens[b]], [S], st["Hq"], st["kv_dtype"], seed=seed)
         else:
             w = make_workload([q_lens[b]], [S], st["Hq"], st["Hkv"], st["kv_dtype"], seed=seed)
         return w, seq_bytes(w, 0, mla)

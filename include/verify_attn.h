@@ -327,7 +327,7 @@ va_status verify_attn_block_table_from_indptr(const va_tensor* kv_indptr,
  * the latent columns of the same cache rows. The latent width is not on the
  * pages; this library takes NOPE_DIM = 512 (the DeepSeek-V3 / Kimi-K2 MLA
  * family). For sequence b (L draft tokens, S = seqused_k[b]) and query head h
- * of draft token t, with cache row j = [c_j | r_j] (decoded e4m3):
+ * of draft token t, with cache row j = [c_j | r_j] (decoded e4m3 or bf16):
  *
  *   out[cu[b]+t, h, :] = sum_j softmax_j(softmax_scale * k_descale *
  *                          (q[.., :512] . c_j + q[.., 512:] . r_j)) * v_descale * c_j
@@ -336,7 +336,9 @@ va_status verify_attn_block_table_from_indptr(const va_tensor* kv_indptr,
  *
  * Arguments (device memory unless stated):
  *  q            [total_q, Hq, 576] bf16: [q_nope (absorbed, 512) | q_pe (64)].
- *  kv_cache     [num_blocks, 16, 1, 576] FP8 E4M3 (OCP FN): [latent | rope key].
+ *  kv_cache     [num_blocks, 16, 1, 576] FP8 E4M3 (OCP FN) or BF16: [latent |
+ *               rope key] (the digest's tests cover both cache types, same
+ *               digest, "Implementation breakdown" item 4).
  *  block_table, cu_seqlens_q, seqused_k, max_seqlen_q, max_seqlen_k,
  *  softmax_scale, k_descale, v_descale: as for verify_attn (Hkv = 1, so the
  *               group is Hq and Hq * max_seqlen_q <= 64). A cache with one
@@ -354,8 +356,9 @@ va_status verify_attn_block_table_from_indptr(const va_tensor* kv_indptr,
  * Layout: innermost strides 1 and every other stride a multiple of 16 bytes;
  * q, out, kv_cache 16-byte aligned.
  * Errors (before any launch): VA_ERR_NULL, VA_ERR_SHAPE, VA_ERR_DTYPE,
- * VA_ERR_LAYOUT as for verify_attn; VA_ERR_UNSUPPORTED for a BF16 cache,
- * more than one KV head, other row widths or Hq * max_seqlen_q > 64;
+ * VA_ERR_LAYOUT as for verify_attn (VA_ERR_DTYPE for a cache that is neither
+ * FP8 E4M3 nor BF16); VA_ERR_UNSUPPORTED for more than one KV head, other row
+ * widths or Hq * max_seqlen_q > 64;
  * VA_ERR_WORKSPACE for a short or misaligned workspace; VA_ERR_CUDA for a
  * failed launch or allocation. Device-side timeouts set the workspace
  * status word as for verify_attn_ex.
@@ -368,7 +371,7 @@ va_status verify_attn_mla(const va_tensor* q, const va_tensor* kv_cache, const v
                           void* event_after_main, void* stream);
 
 /* Workspace bytes verify_attn_mla needs for these shapes on the current
- * device (0 if they are unsupported). */
+ * device, for either cache type (0 if they are unsupported). */
 size_t verify_attn_mla_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_seqlen_q,
                                       int32_t max_seqlen_k, int32_t num_splits);
 

@@ -22,7 +22,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libverify_attn.so")
 
-SOURCES = ["va_host.cpp", "va_main_tc.cu", "va_mla_tc.cu", "va_merge.cu", "va_noalloc.cu",
+SOURCES = ["va_host.cpp", "va_main_tc.cu", "va_mla_tc.cu", "va_mla_bf16_tc.cu", "va_merge.cu", "va_noalloc.cu",
            "va_pagetable.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -251,7 +251,9 @@ static va_status device_state(DeviceState** out) {
   if (!st.ready) {
     if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return VA_ERR_CUDA;
-    if (prepare_main_tc() != cudaSuccess || prepare_mla_tc() != cudaSuccess) return VA_ERR_CUDA;
+    if (prepare_main_tc() != cudaSuccess || prepare_mla_tc() != cudaSuccess ||
+        prepare_mla_bf16_tc() != cudaSuccess)
+      return VA_ERR_CUDA;
     st.ready = true;
   }
   *out = &st;
@@ -371,8 +373,7 @@ va_status validate_mla(const va_tensor* q, const va_tensor* kv, const va_tensor*
   if (kv->dtype != VA_FP8_E4M3 && kv->dtype != VA_BF16) return VA_ERR_DTYPE;
   if (bt->dtype != VA_INT32 || cu->dtype != VA_INT32 || su->dtype != VA_INT32) return VA_ERR_DTYPE;
   // one latent KV head (the digest's k_extend.shape[1] != 1 rejection), rows
-  // [latent | rope], an FP8 cache (the only one this kernel reads)
-  if (kv->dtype != VA_FP8_E4M3) return VA_ERR_UNSUPPORTED;
+  // [latent | rope]; FP8 E4M3 or BF16
   if (kv->shape[1] != kPageSize || kv->shape[2] != 1 || kv->shape[3] != kMlaRow) return VA_ERR_UNSUPPORTED;
   if (q->shape[2] != kMlaRow || out->shape[2] != kMlaNope) return VA_ERR_UNSUPPORTED;
   if (out->shape[0] != q->shape[0] || out->shape[1] != q->shape[1]) return VA_ERR_SHAPE;
@@ -410,20 +411,24 @@ va_status validate_mla(const va_tensor* q, const va_tensor* kv, const va_tensor*
   return VA_OK;
 }
 
-// The split heuristic of make_plan on 64-key latent tiles, value width 512.
+// The split heuristic of make_plan on latent tiles (64 keys for an FP8 cache,
+// 32 for BF16), value width 512.
 va_status make_mla_plan(int64_t B, int64_t hq, int32_t max_q, int32_t max_k, int32_t num_sms,
-                        int32_t force, va_plan* plan) {
+                        int32_t force, va_plan* plan, int32_t kv_dtype) {
   if (!plan) return VA_ERR_NULL;
   if (B < 0 || hq < 1 || max_q < 1 || max_k < 0 || num_sms < 1) return VA_ERR_UNSUPPORTED;
+  if (kv_dtype != VA_FP8_E4M3 && kv_dtype != VA_BF16) return VA_ERR_UNSUPPORTED;
   if (hq * max_q > kMaxRows) return VA_ERR_UNSUPPORTED;
-  const int64_t item_tiles = ((int64_t)max_k + kMlaTileKeys - 1) / kMlaTileKeys;
+  const int tile = kv_dtype == VA_FP8_E4M3 ? kMlaTileKeys : kMlaTileKeysBf16;
+  const int cost = kv_dtype == VA_FP8_E4M3 ? kMlaPieceCostTiles : kMlaPieceCostTilesBf16;
+  const int64_t item_tiles = ((int64_t)max_k + tile - 1) / tile;
   const int64_t tiles_bound = B * item_tiles;
-  if (tiles_bound + B * kMlaPieceCostTiles > INT32_MAX / 2) return VA_ERR_UNSUPPORTED;
+  if (tiles_bound + B * cost > INT32_MAX / 2) return VA_ERR_UNSUPPORTED;
   int64_t splits = force > 0 ? force : num_sms;
   if (splits > tiles_bound) splits = tiles_bound;
   if (splits < 1) splits = 1;
   std::memset(plan, 0, sizeof(*plan));
-  plan->tile_keys = kMlaTileKeys;
+  plan->tile_keys = tile;
   plan->num_splits = (int32_t)splits;
   plan->max_rows = (int32_t)(hq * max_q);
   plan->num_work = (int32_t)B;
@@ -435,20 +440,24 @@ va_status make_mla_plan(int64_t B, int64_t hq, int32_t max_q, int32_t max_k, int
   return VA_OK;
 }
 
-// 4-D map over a latent cache [num_blocks, 16, 1, 576] (e4m3): box = one page,
-// 128 bytes of the row, 128-byte swizzle. The box at column 512 holds the
-// 64 rope bytes; its other 64 lie past the row end and are zero-filled.
+// 4-D map over a latent cache [num_blocks, 16, 1, 576]: box = one page, 128
+// bytes of the row, 128-byte swizzle. For e4m3 the box at column 512 holds the
+// 64 rope bytes, its other 64 lie past the row end and are zero-filled; a
+// bf16 row is nine whole boxes of 64 elements.
 static bool make_mla_map(CUtensorMap* m, const va_tensor* t, int64_t nb) {
   EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
+  const cuuint64_t es_bytes = (cuuint64_t)elem_size(t->dtype);
   cuuint64_t dims[4] = {(cuuint64_t)kMlaRow, 1, (cuuint64_t)kPageSize, (cuuint64_t)nb};
-  cuuint64_t strides[3] = {(cuuint64_t)t->stride[2], (cuuint64_t)t->stride[1], (cuuint64_t)t->stride[0]};
-  if (strides[0] == 0 || strides[0] % 16 != 0) strides[0] = (cuuint64_t)kMlaRow;  // one head: unused
-  cuuint32_t box[4] = {128, 1, (cuuint32_t)kPageSize, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)t->stride[2] * es_bytes, (cuuint64_t)t->stride[1] * es_bytes,
+                           (cuuint64_t)t->stride[0] * es_bytes};
+  if (strides[0] == 0 || strides[0] % 16 != 0) strides[0] = (cuuint64_t)kMlaRow * es_bytes;  // one head: unused
+  cuuint32_t box[4] = {(cuuint32_t)(128 / es_bytes), 1, (cuuint32_t)kPageSize, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, t->data, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUtensorMapDataType dt = es_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  return fn(m, dt, 4, t->data, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 va_status launch_mla(const va_tensor* q, const va_tensor* kv, const va_tensor* bt, const va_tensor* cu,
@@ -487,14 +496,14 @@ va_status launch_mla(const va_tensor* q, const va_tensor* kv, const va_tensor* b
   p.total_q = (int32_t)sh.total_q;
   p.max_seqlen_q = max_q;
   p.max_seqlen_k = max_k;
-  p.kv_fp8 = 1;
+  p.kv_fp8 = sh.kv_dtype == VA_FP8_E4M3 ? 1 : 0;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.window_left = -1;
   p.tile_keys = plan.tile_keys;
   p.num_splits = plan.num_splits;
   p.max_rows = plan.max_rows;
   p.num_work = plan.num_work;
-  p.piece_cost = kMlaPieceCostTiles;
+  p.piece_cost = p.kv_fp8 ? kMlaPieceCostTiles : kMlaPieceCostTilesBf16;
   p.dv = kMlaNope;
   p.wait_limit_ns = wait_limit_ns();
   const WorkspaceLayout lay =
@@ -507,7 +516,8 @@ va_status launch_mla(const va_tensor* q, const va_tensor* kv, const va_tensor* b
   CUtensorMap tm;
   std::memset(&tm, 0, sizeof(tm));
   if (sh.num_blocks > 0 && !make_mla_map(&tm, kv, sh.num_blocks)) return VA_ERR_LAYOUT;
-  if (launch_mla_tc(p, tm, stream) != cudaSuccess) return VA_ERR_CUDA;
+  if ((p.kv_fp8 ? launch_mla_tc(p, tm, stream) : launch_mla_bf16_tc(p, tm, stream)) != cudaSuccess)
+    return VA_ERR_CUDA;
   if (ev_mid && cudaEventRecord(ev_mid, stream) != cudaSuccess) return VA_ERR_CUDA;
   if (launch_merge(p, stream) != cudaSuccess) return VA_ERR_CUDA;
   return VA_OK;
@@ -704,7 +714,7 @@ VA_EXPORT va_status verify_attn_mla(const va_tensor* q, const va_tensor* kv_cach
   s = device_state(&st);
   if (s != VA_OK) return s;
   va_plan plan;
-  s = make_mla_plan(sh.num_seqs, sh.hq, max_seqlen_q, max_seqlen_k, st->sms, num_splits, &plan);
+  s = make_mla_plan(sh.num_seqs, sh.hq, max_seqlen_q, max_seqlen_k, st->sms, num_splits, &plan, sh.kv_dtype);
   if (s != VA_OK) return s;
   if (!workspace) {
     if (sh.total_q == 0 || sh.num_seqs == 0) return VA_OK;
@@ -726,11 +736,16 @@ VA_EXPORT size_t verify_attn_mla_workspace_size(int32_t num_seqs, int32_t num_q_
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState* st = nullptr;
   if (device_state(&st) != VA_OK) return 0;
-  va_plan plan;
-  if (make_mla_plan(num_seqs, num_q_heads, max_seqlen_q, max_seqlen_k, st->sms, num_splits, &plan) !=
-      VA_OK)
-    return 0;
-  return (size_t)plan.workspace_bytes;
+  // enough for either cache dtype (their tiles, and so their splits, differ)
+  size_t bytes = 0;
+  for (int32_t dt : {(int32_t)VA_FP8_E4M3, (int32_t)VA_BF16}) {
+    va_plan plan;
+    if (make_mla_plan(num_seqs, num_q_heads, max_seqlen_q, max_seqlen_k, st->sms, num_splits, &plan, dt) !=
+        VA_OK)
+      return 0;
+    if ((size_t)plan.workspace_bytes > bytes) bytes = (size_t)plan.workspace_bytes;
+  }
+  return bytes;
 }
 
 // ---- one shard of each sequence's keys, and the merge of shards ---------------

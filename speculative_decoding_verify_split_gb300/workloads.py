@@ -458,6 +458,9 @@ MLA_WORKLOADS = (
     "mla_tiny",                # 2 seqs, q [4,2], kv [1024,769], 16 heads, fp8 latent
     "mla_mid_context_fp8",     # 64 seqs, q 3, kv U[8192,32768], 16 heads, descale U[0.5,2]
     "mla_long_context_fp8",    # 16 seqs, q 4, kv U[65536,131072], 16 heads, fp8 latent
+    "mla_tiny_bf16",           # the same shapes on a bf16 latent cache
+    "mla_mid_context_bf16",
+    "mla_long_context_bf16",
 )
 
 
@@ -465,6 +468,10 @@ def mla_workload_structure(name: str, seed: int = 0) -> dict:
     """q_lens, kv_lens, heads and descales of a named latent-cache workload
     (the shapes of the GQA workloads of the same names, on a latent cache)."""
     g = torch.Generator().manual_seed(seed)
+    if name.endswith("_bf16"):  # the FP8 workload's structure on a bf16 cache
+        st = mla_workload_structure(name[:-len("_bf16")] + ("" if name == "mla_tiny_bf16" else "_fp8"), seed)
+        st["kv_dtype"] = BF16
+        return st
     if name == "mla_tiny":
         return dict(q_lens=[4, 2], kv_lens=[1024, 769], Hq=16, gen=g, descale=None)
     if name == "mla_mid_context_fp8":
@@ -478,7 +485,7 @@ def mla_workload_structure(name: str, seed: int = 0) -> dict:
 
 def named_mla_workload(name: str, seed: int = 0, value_device: str = "cpu") -> MlaWorkload:
     st = mla_workload_structure(name, seed)
-    return make_mla_workload(st["q_lens"], st["kv_lens"], st["Hq"], FP8, seed=seed,
+    return make_mla_workload(st["q_lens"], st["kv_lens"], st["Hq"], st.get("kv_dtype", FP8), seed=seed,
                              k_descale=st["descale"], value_device=value_device, name=name,
                              _gen=st["gen"])
 

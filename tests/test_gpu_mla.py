@@ -117,10 +117,62 @@ def test_errors():
         va.verify_attn_mla(w.q, w.kv_cache, w.block_table, w.cu_seqlens_q, w.seqused_k, 5,
                            w.max_seqlen_k, w.softmax_scale)
     assert e.value.status == 4
-    with pytest.raises(va.VerifyAttnError) as e:   # a BF16 latent cache is not read by this kernel
-        va.verify_attn_mla(w.q, w.kv_cache.to(torch.bfloat16), w.block_table, w.cu_seqlens_q,
+    with pytest.raises(va.VerifyAttnError) as e:   # an fp32 latent cache
+        va.verify_attn_mla(w.q, w.kv_cache.to(torch.float32), w.block_table, w.cu_seqlens_q,
                            w.seqused_k, w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale)
-    assert e.value.status == 4
+    assert e.value.status == 3
+
+
+# --- a BF16 latent cache (the BF16 kernel: 32-key tiles, Q in shared memory) ---
+
+@pytest.mark.parametrize("splits", [0, 1, 2, 7, 64, 1000])
+def test_bf16_tiny_whole(splits):
+    w = named_mla_workload("mla_tiny_bf16")
+    compare(run(w.to("cuda"), splits), mla_oracle_from_torch(w))
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_bf16_random_shapes(seed):
+    """Ragged lengths (0, 1, page and tile edges), 1-4 draft tokens, 1 to 64
+    heads, descales, forced splits, on a BF16 latent cache."""
+    g = torch.Generator().manual_seed(900 + seed)
+    B = int(torch.randint(1, 7, (1,), generator=g))
+    hq = [1, 2, 4, 8, 16, 32, 64][int(torch.randint(0, 7, (1,), generator=g))]
+    qmax = min(4, 64 // hq)
+    q_lens = torch.randint(1, qmax + 1, (B,), generator=g).tolist()
+    choices = [0, 1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 500, 1000, 2500]
+    kv_lens = [choices[int(i)] for i in torch.randint(0, len(choices), (B,), generator=g)]
+    kd = float(torch.rand(1, generator=g) * 1.5 + 0.5)
+    vd = float(torch.rand(1, generator=g) * 1.5 + 0.5)
+    w = make_mla_workload(q_lens, kv_lens, hq, "bf16", seed=950 + seed, k_descale=kd, v_descale=vd)
+    splits = [0, 1, 3, 200][seed % 4]
+    compare(run(w.to("cuda"), splits), mla_oracle_from_torch(w))
+
+
+def test_bf16_peaked_softmax_and_bit_identity():
+    """Queries scaled up so that row maxima jump across tiles (O^T rescales);
+    results bit-identical run to run and under a relabelling of the pages."""
+    w = make_mla_workload([4, 2, 3], [2000, 4100, 600], 16, "bf16", seed=931)
+    w.q = (w.q.to(torch.float32) * 6).to(torch.bfloat16)
+    ref = mla_oracle_from_torch(w)
+    wg = w.to("cuda")
+    a = run(wg, 11)
+    compare(a, ref)
+    assert torch.equal(run(wg, 11).view(torch.int16), a.view(torch.int16))
+    nb = wg.kv_cache.shape[0]
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(5)).to("cuda")
+    kv2 = torch.empty_like(wg.kv_cache)
+    kv2[perm] = wg.kv_cache
+    w2 = w.to("cuda")
+    w2.kv_cache = kv2
+    w2.block_table = perm.to(torch.int32)[wg.block_table.long()]
+    assert torch.equal(run(w2, 11).view(torch.int16), a.view(torch.int16))
+
+
+def test_bf16_long_context_every_sequence():
+    w = named_mla_workload("mla_long_context_bf16", value_device="cuda")
+    got = run(w.to("cuda"))
+    print("mla_long_context_bf16", compare(got, mla_oracle_from_torch(w.to("cpu"))))
 
 
 @pytest.mark.parametrize("hq,q_lens", [(64, [1, 1, 1]), (32, [2, 1]), (1, [4, 3, 1]), (2, [1, 4])])

@@ -12,8 +12,8 @@ test checks that:
   on a fresh one matches the CPU oracle.
 
 Covered: the GQA kernel on both KV types (many CTAs and one), the variant
-kernel, a shard call, the latent-cache kernel, the library's own workspace
-and the no-alloc array."""
+kernel, a shard call, the latent-cache kernels (FP8 and BF16 caches), the
+library's own workspace and the no-alloc array."""
 import numpy as np
 import pytest
 import torch
@@ -93,8 +93,9 @@ def test_variant_kernel_and_shard_timeout():
     assert va.last_device_error(ws) == 0
 
 
-def test_latent_kernel_timeout():
-    m_cpu = make_mla_workload([4, 2, 3], [2500, 700, 130], 16, seed=303, k_descale=1.1, v_descale=0.8)
+@pytest.mark.parametrize("dt", ["fp8_e4m3", "bf16"])
+def test_latent_kernel_timeout(dt):
+    m_cpu = make_mla_workload([4, 2, 3], [2500, 700, 130], 16, dt, seed=303, k_descale=1.1, v_descale=0.8)
     m = m_cpu.to("cuda")
     n = va.mla_workspace_size(m.q, m.seqused_k, m.max_seqlen_q, m.max_seqlen_k)
     ws = torch.zeros(n + 256, dtype=torch.uint8, device="cuda")

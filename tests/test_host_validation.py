@@ -171,7 +171,10 @@ def wm():
 def test_mla_validation(wm):
     assert _mla_status(wm, q=None) == NULL
     assert _mla_status(wm, out=None) == NULL
-    assert _mla_status(wm, kv=wm.kv_cache.to(torch.bfloat16)) == UNSUP    # FP8 latent only
+    # a BF16 latent cache passes the cache checks (then the mismatched out is reported)
+    assert _mla_status(wm, kv=wm.kv_cache.to(torch.bfloat16),
+                       out=torch.empty(6, 8, 512, dtype=torch.bfloat16)) == SHAPE
+    assert _mla_status(wm, kv=wm.kv_cache.to(torch.float32)) == DTYPE
     assert _mla_status(wm, kv=wm.kv_cache.view(torch.uint8).to(torch.int32)) == DTYPE
     two = torch.cat([wm.kv_cache, wm.kv_cache], dim=2)
     assert _mla_status(wm, kv=two) == UNSUP                                # one latent head

@@ -125,7 +125,20 @@ def pin_constant_rows_and_rope_spike(orc):
             assert np.abs(out[t, h] - s64).max() < 1e-12, "the rope spike must dominate"
 
 
-PINS = [pin_sdpa, pin_gqa_oracle_on_padded_values, pin_constant_rows_and_rope_spike]
+def pin_sdpa_bf16(orc):
+    """The same SDPA pin on a BF16 latent cache (the oracle's bf16 decode of
+    the cache rows; torch converts the rows for SDPA by itself)."""
+    for seed, (q_lens, kv_lens, hq) in enumerate([((4, 2, 3), (40, 17, 1), 16), ((1, 4), (33, 64), 8)]):
+        w = make_mla_workload(list(q_lens), list(kv_lens), hq, "bf16", seed=40 + seed, k_descale=1.3,
+                              v_descale=0.6)
+        out = run(orc, w)
+        for b in range(len(q_lens)):
+            q0 = int(w.cu_seqlens_q[b])
+            ref = sdpa_mla(w, b)
+            assert np.abs(out[q0:q0 + q_lens[b]] - ref).max() < 1e-10
+
+
+PINS = [pin_sdpa, pin_gqa_oracle_on_padded_values, pin_constant_rows_and_rope_spike, pin_sdpa_bf16]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)

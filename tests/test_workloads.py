@@ -64,7 +64,9 @@ def test_sizes_count_kv_once_per_kv_head():
 def test_latent_structures_mirror_the_gqa_shapes(name):
     st = mla_workload_structure(name)
     base = {"mla_tiny": "tiny_verify", "mla_mid_context_fp8": "mid_context_fp8",
-            "mla_long_context_fp8": "long_context_fp8"}[name]
+            "mla_long_context_fp8": "long_context_fp8", "mla_tiny_bf16": "tiny_verify",
+            "mla_mid_context_bf16": "mid_context_fp8", "mla_long_context_bf16": "long_context_fp8"}[name]
+    assert st.get("kv_dtype", FP8) == (BF16 if name.endswith("_bf16") else FP8)
     B, qs, kv, hq, _, _ = CONFIGS[base]
     assert len(st["q_lens"]) == B and st["Hq"] == hq
     if qs is not None:
