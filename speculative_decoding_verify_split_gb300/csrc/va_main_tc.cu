@@ -631,21 +631,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (wait_or_fail(kBarSFull + b, (cur / kSBufs) & 1, 256)) {
           tc_fence_after();
           if constexpr (FP8) {
-            // lane t reads its TMEM lane: hi (t < 16) or lo (t >= 16) partial of
-            // row 16q + rl for keys [64 kh, +64); sub 0 keeps the first 32
-            // keys, sub 1 the second, each adding the partner lane's part
+            // the hi and lo partials of row 16q + rl, keys [64 kh + 32 sub,
+            // +32): two 16-lane loads (hi rows in lanes 32q.., lo rows in
+            // lanes 32q + 16..) whose second halves go to threads 16-31, so
+            // every thread gets both terms of its own keys
             // (S buffer b is then overwritten by P(cur); P V's commit frees it)
-            uint32_t va[32], vb[32];
-            tmem_ld_32x32b_x32(tmem + lane_base + kColS + b * kT + 64 * kh, va);
-            tmem_ld_32x32b_x32(tmem + lane_base + kColS + b * kT + 64 * kh + 32, vb);
+            uint32_t vh[32], vl[32];
+            tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kColS + b * kT + 64 * kh, vh);
+            tmem_ld_16x32bx2_x32<32>(tmem + lane_base + (16u << 16) + kColS + b * kT + 64 * kh, vl);
             tmem_wait_ld();
             tc_fence_before();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float mine = __uint_as_float(sub ? vb[i] : va[i]);
-              const float give = __uint_as_float(sub ? va[i] : vb[i]);
-              x[i] = (mine + __shfl_xor_sync(0xffffffffu, give, 16)) * rx;
-            }
+            for (int i = 0; i < 32; ++i) x[i] = (__uint_as_float(vh[i]) + __uint_as_float(vl[i])) * rx;
           } else {
             uint32_t v[16];
             tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kColS + b * kT + 32 * kh, v);
@@ -754,18 +751,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // A operand of P V in TMEM, over S(cur): lane 32q + rl (hi row) and
           // lane 32q + 16 + rl (lo row) take the e4m3 bytes of keys
           // [64 kh, +64) at columns [16 kh, +16). This thread holds keys
-          // [32 qtr, +32) of both; it trades the part its lane does not take
-          // with the partner lane (t ^ 16).
-          uint32_t pw[16];
-#pragma unroll
-          for (int w = 0; w < 8; ++w) {
-            const uint32_t recv = __shfl_xor_sync(0xffffffffu, sub ? ph[w] : pl[w], 16);
-            pw[w] = sub ? recv : ph[w];
-            pw[8 + w] = sub ? pl[w] : recv;
-          }
-          // the quadrant's other warp read its S columns before the exchange
+          // [32 qtr, +32) of both: two 16-lane stores, its hi bytes into the
+          // hi row and its lo bytes into the lo row, threads 16-31 at +8.
+          // The quadrant's other warp read its S columns before the exchange.
           tc_fence_after();
-          tmem_st_32x32b_x16(tmem + lane_base + kColS + b * kT + 16 * kh, pw);
+          tmem_st_16x32bx2_x8<8>(tmem + lane_base + kColS + b * kT + 16 * kh, ph);
+          tmem_st_16x32bx2_x8<8>(tmem + lane_base + (16u << 16) + kColS + b * kT + 16 * kh, pl);
           tmem_wait_st();
         } else {
           uint32_t pw[8];

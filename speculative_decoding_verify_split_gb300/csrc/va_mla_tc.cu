@@ -540,21 +540,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i) x[i] = -INFINITY;
         if (wait_or_fail(kBarSFull + b, (cur / kSBufs) & 1, 256)) {
           tc_fence_after();
-          // own lane: the hi (sub 0) or lo (sub 1) part of row r, keys
-          // [32 kh, +32); sub 0 keeps the first 16 keys, sub 1 the second,
-          // each adding the partner lane's part
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + kColS + b * kT + 32 * kh, v);
+          // the hi and lo partials of row r, keys [32 kh + 16 sub, +16): two
+          // 16-lane loads (hi rows in lanes 32q.., lo rows in lanes
+          // 32q + 16..) whose second halves go to threads 16-31
+          uint32_t vh[16], vl[16];
+          tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kColS + b * kT + 32 * kh, vh);
+          tmem_ld_16x32bx2_x16<16>(tmem + lane_base + (16u << 16) + kColS + b * kT + 32 * kh, vl);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarSFree + b));
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float mine = __uint_as_float(sub ? v[16 + i] : v[i]);
-            const float give = __uint_as_float(sub ? v[i] : v[16 + i]);
-            x[i] = (mine + __shfl_xor_sync(0xffffffffu, give, 16)) * rs;
-          }
+          for (int i = 0; i < 16; ++i) x[i] = (__uint_as_float(vh[i]) + __uint_as_float(vl[i])) * rs;
           const int key0 = lt * kT + 16 * qtr;
           if (lt * kT + kT - 1 > pc.S - pc.L) {  // tail tile: causal mask
 #pragma unroll
@@ -565,19 +562,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         float tmax = -INFINITY;
 #pragma unroll
         for (int i = 0; i < 16; i += 2) tmax = fmaxf(tmax, fmaxf(x[i], x[i + 1]));
-        tmax = exchange(tmax, true);
-
-        const bool need = ok && tmax > m_ref + kOvershoot;
-        const float m_new = need ? tmax + (m_ref == -INFINITY ? kHeadroomFirst : kHeadroom) : m_ref;
-        const bool rescale = need && (m_ref != -INFINITY) && (cur > first);
-        const float alpha = rescale ? ex2(m_ref - m_new) : 1.f;
-        // O^T keeps a row in a column across all 128 lanes: every softmax
-        // warp scales its lanes' part of the rows that moved, so the decision
-        // is taken by all of them at once
+        // A row's reference moves only when one of its four threads sees a
+        // key above m_ref + kOvershoot. One vote over all softmax threads
+        // finds out; only then is the row max exchanged (the reference stays
+        // put on most tiles, and the exchange costs a barrier of its own).
+        // The decisions are those of an exchange on every tile.
+        float m_new = m_ref, alpha = 1.f;
+        bool any = false;
         float* al = row_vals + (round & 1) * 64;
         ++round;
-        if (kh == 0 && sub == 0) al[r] = alpha;
-        const bool any = named_bar_or(kBarAllSoftmax, kSoftmaxThreads, rescale);
+        if (named_bar_or(kBarAllSoftmax, kSoftmaxThreads, ok && tmax > m_ref + kOvershoot)) {
+          tmax = exchange(tmax, true);
+          const bool need = ok && tmax > m_ref + kOvershoot;
+          m_new = need ? tmax + (m_ref == -INFINITY ? kHeadroomFirst : kHeadroom) : m_ref;
+          const bool rescale = need && (m_ref != -INFINITY) && (cur > first);
+          alpha = rescale ? ex2(m_ref - m_new) : 1.f;
+          // O^T keeps a row in a column across all 128 lanes: every softmax
+          // warp scales its lanes' part of the rows that moved, so the
+          // decision is taken by all of them at once
+          if (kh == 0 && sub == 0) al[r] = alpha;
+          any = named_bar_or(kBarAllSoftmax, kSoftmaxThreads, rescale);
+        }
         if (!ok) continue;
 
         // P buffer pb was last read by P V(cur - kPBufs)

@@ -359,6 +359,17 @@ __device__ __forceinline__ void tmem_st_16x32bx2_x32(uint32_t taddr, const uint3
       : "memory");
 }
 
+// 16 lanes x 8 columns, two halves: threads 0-15 write lanes base..base+15 at
+// columns [col, col+8); threads 16-31 the same lanes at [col+SPLIT, ...).
+template <int SPLIT>
+__device__ __forceinline__ void tmem_st_16x32bx2_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9};" ::"r"(taddr),
+      "n"(SPLIT), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+      "r"(r[7])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
