@@ -453,7 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const float kd = p.k_descale ? *p.k_descale : 1.0f;
     const float vd = p.v_descale ? *p.v_descale : 1.0f;
-    const float cscale = p.scale_log2 * kd;
+    // The logit scale is kept positive (the softmax takes the max of the raw
+    // dot products and applies the scale after): a negative scale negates Q
+    // as it is staged, and a zero one becomes a tiny positive one (logits
+    // ~1e-30 s instead of 0).
+    const float cscale_signed = p.scale_log2 * kd;
+    const float cscale = fmaxf(fabsf(cscale_signed), 1e-30f);
+    const bool q_neg = cscale_signed < 0.f;
     const int G = p.group;
     unsigned char* qs = sm + C::kOffQ;
     int it = 0, piece_idx = 0;
@@ -523,9 +529,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             e = 7 - E;
             e = e < -120 ? -120 : (e > 120 ? 120 : e);
           }
-          const float up = __uint_as_float((uint32_t)(e + 127) << 23);
+          const float up = __uint_as_float((uint32_t)(e + 127) << 23) * (q_neg ? -1.f : 1.f);
           const float down = __uint_as_float((uint32_t)(127 - e) << 23);
-          rs = row_ok ? cscale * down : 0.f;
+          rs = cscale * down;  // rows past R stage zeros: their logits are 0
           // d [64 qtr, +64) = region kh, 16-byte pieces 4 sub .. 4 sub + 3;
           // hi to A row 32q + rl, lo to A row 32q + 16 + rl
           if (ok) {
@@ -553,13 +559,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          rs = row_ok ? cscale : 0.f;
+          rs = cscale;  // rows past R stage zeros: their logits are 0
           // d [64 qtr, +64) = one whole 128-byte region (qtr), eight 16-byte pieces
           if (ok) {
+            const uint32_t flip = q_neg ? 0x80008000u : 0u;  // bf16 sign bits
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const int off = qtr * C::kQRegion + r * 128 + ((i ^ (r & 7)) << 4);
-              *reinterpret_cast<uint4*>(qs + off) = raw[i];
+              *reinterpret_cast<uint4*>(qs + off) =
+                  make_uint4(raw[i].x ^ flip, raw[i].y ^ flip, raw[i].z ^ flip, raw[i].w ^ flip);
             }
           }
         }
@@ -617,11 +625,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float x[kKpt];  // logits of keys [kKpt qtr, +kKpt) of this tile, this row
 #pragma unroll
         for (int i = 0; i < kKpt; ++i) x[i] = -INFINITY;
-        // x[] holds logits in log2 units, or with a soft cap c (log2 units)
-        // tanh(logit / c): the logit is then xs * x (xs = c), applied inside
-        // the ex2 of P as one FMA, so the cap costs one SFU op per key
-        float rx = rs;
-        float xs = 1.f;
+        // x[] holds the raw dot products s (the logit in log2 units is
+        // xs * x, xs = the row's scale rs), or with a soft cap c (log2 units)
+        // tanh(rs s / c) (then xs = c). xs is applied in the ex2 of P as one
+        // FMA, and once to the tile's max (xs > 0 keeps the order), so the
+        // scale costs nothing per key and the cap one SFU op per key.
+        float rx = 0.f;
+        float xs = rs;
         if constexpr (VAR) {
           if (p.softcap_log2 > 0.f) {
             xs = p.softcap_log2;
@@ -642,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
             tc_fence_before();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = (__uint_as_float(vh[i]) + __uint_as_float(vl[i])) * rx;
+            for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(vh[i]) + __uint_as_float(vl[i]);
           } else {
             uint32_t v[16];
             tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kColS + b * kT + 32 * kh, v);
@@ -651,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarSFree + b));
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(v[i]) * rx;
+            for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(v[i]);
           }
           if constexpr (VAR) {
             if (p.softcap_log2 > 0.f) {
@@ -660,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // logit l by at most |l| 2^-11 log2 units (0.5 % of a key's
               // weight at l = 10).
 #pragma unroll
-              for (int i = 0; i < kKpt; ++i) x[i] = tanh_approx(x[i]);
+              for (int i = 0; i < kKpt; ++i) x[i] = tanh_approx(x[i] * rx);
             }
           }
           const int key0 = lt * kT + kKpt * qtr;
@@ -679,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float tmax = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < kKpt; i += 2) tmax = fmaxf(tmax, fmaxf(x[i], x[i + 1]));
+        for (int i = 0; i < kKpt; i += 2) tmax = fmax3(tmax, x[i], x[i + 1]);
         tmax = exchange(tmax * xs, true);  // log2 units (xs > 0 keeps the order)
         if (!ok) continue;
 
@@ -726,16 +736,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = m_new;
 
         // P = 2^(x - m_ref + kPShift) into the K-major no-swizzle A operand
-        const float mref_s = m_ref - kPShift;
-        const bool live = m_ref != -INFINITY;
+        // a row with no visible key yet (m_ref = -inf) gets P = ex2(-inf) = 0
+        const float mref_s = m_ref != -INFINITY ? m_ref - kPShift : INFINITY;
         float ls0 = 0.f, ls1 = 0.f;
         unsigned char* pbuf = sm + C::kOffP + pb * C::kPBuf;
         if constexpr (FP8) {
           uint32_t ph[8], pl[8];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float a = live ? ex2(fmaf(x[2 * i], xs, -mref_s)) : 0.f;
-            const float bb = live ? ex2(fmaf(x[2 * i + 1], xs, -mref_s)) : 0.f;
+            const float a = ex2(fmaf(x[2 * i], xs, -mref_s));
+            const float bb = ex2(fmaf(x[2 * i + 1], xs, -mref_s));
             ls0 += a;
             ls1 += bb;
             uint32_t h2, l2;
@@ -762,8 +772,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pw[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float a = live ? ex2(fmaf(x[2 * i], xs, -mref_s)) : 0.f;
-            const float bb = live ? ex2(fmaf(x[2 * i + 1], xs, -mref_s)) : 0.f;
+            const float a = ex2(fmaf(x[2 * i], xs, -mref_s));
+            const float bb = ex2(fmaf(x[2 * i + 1], xs, -mref_s));
             ls0 += a;
             ls1 += bb;
             pw[i] = pack_bf16x2(a, bb);

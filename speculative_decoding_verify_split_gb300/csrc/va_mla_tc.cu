@@ -392,7 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qtr = 2 * kh + sub;        // key quarter (16 keys) of a tile
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const float kd = p.k_descale ? *p.k_descale : 1.0f;
-    const float cscale = p.scale_log2 * kd;
+    // The logit scale is kept positive (the softmax takes the max of the raw
+    // dot products and applies the scale after): a negative scale negates Q
+    // as it is staged, and a zero one becomes a tiny positive one.
+    const float cscale_signed = p.scale_log2 * kd;
+    const float cscale = fmaxf(fabsf(cscale_signed), 1e-30f);
+    const bool q_neg = cscale_signed < 0.f;
     const int G = p.group;
     unsigned char* qpe_s = sm + kOffQpe;
     int it = 0, piece_idx = 0, round = 0;
@@ -455,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         e = 7 - E;
         e = e < -120 ? -120 : (e > 120 ? 120 : e);
       }
-      const float up = __uint_as_float((uint32_t)(e + 127) << 23);
+      const float up = __uint_as_float((uint32_t)(e + 127) << 23) * (q_neg ? -1.f : 1.f);
       const float down = __uint_as_float((uint32_t)(127 - e) << 23);
       if (ok) {
 #pragma unroll
@@ -496,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarQFull));
       }
-      return row_ok ? cscale * down : 0.f;
+      return cscale * down;  // rows past R stage zeros: their logits are 0
     };
     // The next piece's Q segments of this thread (three 128-byte lines) into
     // L2, a piece ahead: under full HBM load a round trip to DRAM takes
@@ -551,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarSFree + b));
 #pragma unroll
-          for (int i = 0; i < 16; ++i) x[i] = (__uint_as_float(vh[i]) + __uint_as_float(vl[i])) * rs;
+          for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(vh[i]) + __uint_as_float(vl[i]);
           const int key0 = lt * kT + 16 * qtr;
           if (lt * kT + kT - 1 > pc.S - pc.L) {  // tail tile: causal mask
 #pragma unroll
@@ -561,7 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float tmax = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) tmax = fmaxf(tmax, fmaxf(x[i], x[i + 1]));
+        for (int i = 0; i < 16; i += 2) tmax = fmax3(tmax, x[i], x[i + 1]);
+        tmax *= rs;  // x holds the raw dot products; rs > 0 keeps the order
         // A row's reference moves only when one of its four threads sees a
         // key above m_ref + kOvershoot. One vote over all softmax threads
         // finds out; only then is the row max exchanged (the reference stays
@@ -587,14 +593,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // P buffer pb was last read by P V(cur - kPBufs)
         if (cur >= kPBufs && !wait_or_fail(kBarPFree + pb, ((cur - kPBufs) / kPBufs) & 1, 512)) continue;
-        const float mref_s = m_new - kPShift;
-        const bool live = m_new != -INFINITY;
+        // a row with no visible key yet (m_new = -inf) gets P = ex2(-inf) = 0
+        const float mref_s = m_new != -INFINITY ? m_new - kPShift : INFINITY;
         uint32_t ph[4], pl[4];
         float ls = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float a = live ? ex2(x[2 * i] - mref_s) : 0.f;
-          const float bb = live ? ex2(x[2 * i + 1] - mref_s) : 0.f;
+          const float a = ex2(fmaf(x[2 * i], rs, -mref_s));
+          const float bb = ex2(fmaf(x[2 * i + 1], rs, -mref_s));
           ls += a + bb;
           uint32_t h2, l2;
           split_p(a, bb, h2, l2);

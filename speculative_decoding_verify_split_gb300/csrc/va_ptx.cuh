@@ -321,6 +321,14 @@ __device__ __forceinline__ float tanh_approx(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (sm_100 family); a NaN input is ignored
+// unless all are NaN, as with fmaxf.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // 2^x on the SFU (ex2.approx.ftz: flushes subnormal results to zero).
 __device__ __forceinline__ float ex2(float x) {
   float y;
