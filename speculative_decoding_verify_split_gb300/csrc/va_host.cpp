@@ -444,7 +444,9 @@ va_status make_mla_plan(int64_t B, int64_t hq, int32_t max_q, int32_t max_k, int
 // bytes of the row, 128-byte swizzle. For e4m3 the box at column 512 holds the
 // 64 rope bytes, its other 64 lie past the row end and are zero-filled; a
 // bf16 row is nine whole boxes of 64 elements.
-static bool make_mla_map(CUtensorMap* m, const va_tensor* t, int64_t nb) {
+// Box: 128 bytes of one row (a latent chunk, 128-byte swizzle), or with
+// `rope` the row's 64 rope bytes (64-byte swizzle), x 16 page rows.
+static bool make_mla_map(CUtensorMap* m, const va_tensor* t, int64_t nb, bool rope = false) {
   EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
   const cuuint64_t es_bytes = (cuuint64_t)elem_size(t->dtype);
@@ -452,11 +454,11 @@ static bool make_mla_map(CUtensorMap* m, const va_tensor* t, int64_t nb) {
   cuuint64_t strides[3] = {(cuuint64_t)t->stride[2] * es_bytes, (cuuint64_t)t->stride[1] * es_bytes,
                            (cuuint64_t)t->stride[0] * es_bytes};
   if (strides[0] == 0 || strides[0] % 16 != 0) strides[0] = (cuuint64_t)kMlaRow * es_bytes;  // one head: unused
-  cuuint32_t box[4] = {(cuuint32_t)(128 / es_bytes), 1, (cuuint32_t)kPageSize, 1};
+  cuuint32_t box[4] = {(cuuint32_t)((rope ? 64 : 128) / es_bytes), 1, (cuuint32_t)kPageSize, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   const CUtensorMapDataType dt = es_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
   return fn(m, dt, 4, t->data, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            rope ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -513,10 +515,12 @@ va_status launch_mla(const va_tensor* q, const va_tensor* kv, const va_tensor* b
   p.ws_meta = reinterpret_cast<int32_t*>(base + lay.meta_off);
   p.ws_ml = reinterpret_cast<float*>(base + lay.ml_off);
   p.ws_acc = reinterpret_cast<float*>(base + lay.acc_off);
-  CUtensorMap tm;
+  CUtensorMap tm, tm_pe;
   std::memset(&tm, 0, sizeof(tm));
+  std::memset(&tm_pe, 0, sizeof(tm_pe));
   if (sh.num_blocks > 0 && !make_mla_map(&tm, kv, sh.num_blocks)) return VA_ERR_LAYOUT;
-  if ((p.kv_fp8 ? launch_mla_tc(p, tm, stream) : launch_mla_bf16_tc(p, tm, stream)) != cudaSuccess)
+  if (sh.num_blocks > 0 && p.kv_fp8 && !make_mla_map(&tm_pe, kv, sh.num_blocks, true)) return VA_ERR_LAYOUT;
+  if ((p.kv_fp8 ? launch_mla_tc(p, tm, tm_pe, stream) : launch_mla_bf16_tc(p, tm, stream)) != cudaSuccess)
     return VA_ERR_CUDA;
   if (ev_mid && cudaEventRecord(ev_mid, stream) != cudaSuccess) return VA_ERR_CUDA;
   if (launch_merge(p, stream) != cudaSuccess) return VA_ERR_CUDA;

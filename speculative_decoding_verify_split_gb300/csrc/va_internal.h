@@ -158,7 +158,8 @@ constexpr int kMlaTileKeys = 64;
 // best by ~1.5 us on both.
 constexpr int kMlaPieceCostTiles = 12;
 cudaError_t prepare_mla_tc();
-cudaError_t launch_mla_tc(const Params& p, const CUtensorMap& tm_kv, cudaStream_t stream);
+cudaError_t launch_mla_tc(const Params& p, const CUtensorMap& tm_kv, const CUtensorMap& tm_pe,
+                          cudaStream_t stream);
 // Latent-cache main kernel over a BF16 cache (va_mla_bf16_tc.cu): 32-key
 // tiles (36 KB, the bytes of a 64-key FP8 tile), Q in shared memory. Its
 // piece cost is the FP8 kernel's in keys.

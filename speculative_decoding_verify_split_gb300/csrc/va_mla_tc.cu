@@ -23,14 +23,16 @@
 //    columns = 256 TMEM columns. V^T is the cache tile's latent part read as
 //    an MN-major A operand; P^T is a K-major B operand in smem.
 //  TMEM: O^T 0-255, two 64-column S tiles 256-383, Q latent 384-511.
-// A cache tile is 64 keys = 4 pages; a page is 5 TMA boxes of 16 rows x 128
-// bytes (four latent chunks and the rope chunk, whose box reaches past the
-// row end and is zero-filled), so a tile fills five 8 KB 128-byte-swizzled
-// regions; five ring slots (200 KB) are in flight. A slot is freed after
-// P V, since the same bytes are K and V. The cache loads carry an L2
-// evict_first policy, and the kernel is launched as a programmatic dependent
-// of the stream's previous kernel (setup before griddepcontrol.wait), as in
-// the GQA kernel.
+// A cache tile is 64 keys = 4 pages; a page is 5 TMA boxes of 16 rows: four
+// 128-byte latent chunks (128-byte swizzle) and the 64-byte rope part (64-byte
+// swizzle, its own tensor map), so a tile fills four 8 KB regions and one of
+// 4 KB; five ring slots (180 KB) are in flight, beside four P^T buffers (the
+// tensor pipe runs Q K^T up to two tiles ahead of P V, so the softmax's wait
+// for the P buffer of tile t - 4 never blocks). A slot is freed after P V,
+// since the same bytes are K and V. The cache loads carry an L2 evict_first
+// policy, and the kernel is launched as a programmatic dependent of the
+// stream's previous kernel (setup before griddepcontrol.wait), as in the GQA
+// kernel.
 // O^T columns are rows, so a rescale of some rows touches every lane: the
 // softmax warps decide together, per tile, with one barrier reduction.
 // FP8 cache only; plain attention (no window, soft cap or sinks).
@@ -47,16 +49,18 @@ constexpr int kT = kMlaTileKeys;               // 64 keys per tile
 constexpr int kPagesPerTile = kT / kPageSize;  // 4
 constexpr int kRegions = 5;                    // latent chunks 0-3, rope chunk 4
 constexpr int kRegion = kT * 128;              // 8 KB: 64 rows x 128 bytes, 128-byte swizzle
-constexpr int kTileBytes = kRegions * kRegion;  // 40 KB
+constexpr int kPeRegion = kT * kMlaPe;         // 4 KB: 64 rows x 64 bytes, 64-byte swizzle
+constexpr int kTileBytes = 4 * kRegion + kPeRegion;  // 36 KB
 constexpr int kSlots = 5;
 constexpr int kProducers = 3;                  // warps 0, 2, 3 take every third tile
 // A producer's wait for a slot relies on its own previous wait (kProducers
 // tiles back) to keep that slot's empty barrier within one phase.
 static_assert(kProducers <= kSlots, "producers exceed the ring");
-constexpr int kBoxes = kPagesPerTile * kRegions;  // 20 boxes of 2 KB per tile
+constexpr int kBoxes = kPagesPerTile * kRegions;  // 20 boxes per tile (16 of 2 KB, 4 of 1 KB)
+constexpr uint32_t kPageBytes = 4 * 2048 + 1024;   // one page's boxes
 static_assert(kBoxes <= 32, "one box per lane");
 constexpr int kSBufs = 2;
-constexpr int kPBufs = 2;
+constexpr int kPBufs = 4;                      // P^T buffers: the wait for P V(t - 4) never blocks
 constexpr int kPHalf = 64 * kT;                // one e4m3 term of P: 64 rows x 64 keys
 constexpr int kPBuf = 2 * kPHalf;              // hi then lo
 constexpr int kQpeBytes = 128 * kMlaPe;        // 128 stacked rows x 64 bytes
@@ -69,9 +73,10 @@ constexpr int kOffQpe = kSlots * kTileBytes;
 constexpr int kOffP = kOffQpe + kQpeBytes;
 constexpr int kOffX = kOffP + kPBufs * kPBuf;  // [2 parity][2 kh][64 rows] floats
 constexpr int kOffBar = kOffX + 1024;
-constexpr int kSmemBytes = kOffBar + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory");
+constexpr int kSmemBytes = kOffBar + 2048;
+static_assert(kSmemBytes + 1024 <= 232448, "shared memory (with the 1 KB alignment slack)");
 static_assert(kTileBytes % 1024 == 0 && kOffQpe % 1024 == 0, "swizzle atoms");
+static_assert((kPBufs & (kPBufs - 1)) == 0, "P buffers: a power of two");
 
 constexpr int kThreads = 416;  // 13 warps
 constexpr int kSoftmaxThreads = 256;
@@ -114,11 +119,11 @@ enum : int {
 };
 // barrier area: mbarriers | TMEM address, abort flag | scan scratch (34 x 8) |
 // last tile issued into each ring slot | per-row factors [2 rounds][64] floats
-// at +512
+// at +1024 (2 KB in all)
 constexpr int kOffTmemSlot = 8 * kNumBars;
-constexpr int kOffScratch = 192;
+constexpr int kOffScratch = 256;
 constexpr int kOffSlotTile = kOffScratch + 34 * 8;  // last tile issued into each slot
-constexpr int kOffRowVals = 512;
+constexpr int kOffRowVals = 1024;
 static_assert(kOffTmemSlot + 8 <= kOffScratch && kOffSlotTile + 4 * kSlots <= kOffRowVals, "barrier area");
 
 // Four bf16 values (two words) times 2^e -> e4m3 hi and lo bytes, in order.
@@ -143,7 +148,8 @@ __device__ __forceinline__ int core_off(int m, int k, int row_bytes) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    va_mla_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_kv) {
+    va_mla_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_kv,
+                     const __grid_constant__ CUtensorMap tm_pe) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -195,7 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 2 && lane == 0 && p.num_blocks > 0) tma_prefetch_desc(&tm_kv);
+  if (warp == 2 && lane == 0 && p.num_blocks > 0) {
+    tma_prefetch_desc(&tm_kv);
+    tma_prefetch_desc(&tm_pe);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -274,18 +283,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dst = sbase + s * kTileBytes;
         if (lane == 0) {
           slot_tile[s] = it;
-          mbar_arrive_expect_tx(bar(kBarFull + s), nvalid * (uint32_t)(kRegions * 2048));
+          mbar_arrive_expect_tx(bar(kBarFull + s), nvalid * kPageBytes);
         }
         __syncwarp();
-        if (lane < kBoxes) {  // lane -> (page, 128-byte column chunk)
+        if (lane < kBoxes) {  // lane -> (page, 128-byte latent chunk or the 64-byte rope)
           const int i = lane / kRegions, ch = lane % kRegions;
           int id = ids[0];
 #pragma unroll
           for (int u = 1; u < kPagesPerTile; ++u)
             if (i == u) id = ids[u];
-          if (id >= 0)
-            tma_load_4d_hint(dst + ch * kRegion + i * 2048, &tm_kv, ch * 128, 0, 0, id, bar(kBarFull + s),
-                             kv_policy);
+          if (id >= 0) {
+            if (ch < 4)
+              tma_load_4d_hint(dst + ch * kRegion + i * 2048, &tm_kv, ch * 128, 0, 0, id, bar(kBarFull + s),
+                               kv_policy);
+            else
+              tma_load_4d_hint(dst + 4 * kRegion + i * 1024, &tm_pe, kMlaNope, 0, 0, id, bar(kBarFull + s),
+                               kv_policy);
+          }
         }
         __syncwarp();
       }
@@ -340,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < kQkPeSteps; ++k) {
               const uint64_t adesc = smem_desc(qpe + k * 256, 128, 8 * kMlaPe, kLayoutNone);
-              const uint64_t bdesc = smem_desc(kst + 4 * kRegion + k * 32, 16, 1024, kLayoutSw128);
+              const uint64_t bdesc = smem_desc(kst + 4 * kRegion + k * 32, 16, 512, kLayoutSw64);
               mma_f8f6f4(d, adesc, bdesc, kIdQK, 1u);
             }
             mma_commit(bar(kBarSFull + b));
@@ -706,22 +720,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t prepare_mla_tc() {
-  return cudaFuncSetAttribute(va_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  return cudaFuncSetAttribute(va_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes + 1024);
 }
 
-cudaError_t launch_mla_tc(const Params& p, const CUtensorMap& tm_kv, cudaStream_t stream) {
+cudaError_t launch_mla_tc(const Params& p, const CUtensorMap& tm_kv, const CUtensorMap& tm_pe,
+                          cudaStream_t stream) {
   // a programmatic dependent of the stream's previous kernel (see the kernel)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_splits);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = kSmemBytes + 1024;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, va_mla_tc_kernel, p, tm_kv);
+  return cudaLaunchKernelEx(&cfg, va_mla_tc_kernel, p, tm_kv, tm_pe);
 }
 
 }  // namespace va

@@ -180,7 +180,7 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 
 // Shared-memory matrix descriptor (sm_100 family): start address, leading and
 // stride byte offsets (all >> 4), version 1, layout type in bits 61..63
-// (0 = no swizzle, 2 = 128-byte swizzle).
+// (0 = no swizzle, 2 = 128-byte swizzle, 4 = 64-byte swizzle).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
                                               uint32_t layout) {
   uint64_t d = 0;
@@ -194,6 +194,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 
 constexpr uint32_t kLayoutNone = 0;
 constexpr uint32_t kLayoutSw128 = 2;
+constexpr uint32_t kLayoutSw64 = 4;
 
 // Instruction descriptor for kind::f16 / kind::f8f6f4: f32 accumulate,
 // A/B formats, B transposed (MN-major) flag, N and M.
