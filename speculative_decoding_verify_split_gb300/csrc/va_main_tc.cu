@@ -118,7 +118,8 @@ struct Cfg {
   static constexpr int kOffP = kOffQ + 32768;
   static constexpr int kOffX = kOffP + (kPInTmem ? 0 : 32768);  // [2 parity][2 kh][64 rows] floats
   static constexpr int kOffBar = kOffX + 1024;
-  static constexpr int kSmemBytes = kOffBar + 1024;
+  static constexpr int kOffSeqs = kOffBar + 1024;  // the batch's lengths (SeqMeta, kSeqCache)
+  static constexpr int kSmemBytes = kOffSeqs + 16 * kSeqCache;
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(!kPInTmem || kSBufs == kPBufs, "a TMEM P shares its S buffer's index and barriers");
   static_assert(kChunks * kQRegion == 32768, "Q size");
@@ -257,7 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- work range (all threads) -------------------------------------------------
   long long t0, t1, ts_first = 0;
   int j_first = 0;
-  locate_work<kThreads>(p, c, scratch, s_j, s_ts, &t0, &t1, &j_first, &ts_first);
+  bool seqs_cached = false;
+  locate_work<kThreads>(p, c, scratch, s_j, s_ts, &t0, &t1, &j_first, &ts_first,
+                        reinterpret_cast<SeqMeta*>(sm + C::kOffSeqs), &seqs_cached);
+  const SeqMeta* seqs = seqs_cached ? reinterpret_cast<const SeqMeta*>(sm + C::kOffSeqs) : nullptr;
   if (t0 >= t1) {  // CTA-uniform
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
     return;
@@ -285,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long ts = ts_first;
     Piece pc;
     bool ok = true;
-    while (ok && next_piece(p, t0, t1, j, ts, pc)) {
+    while (ok && next_piece(p, t0, t1, j, ts, pc, seqs)) {
       const int npages = (pc.S + kPageSize - 1) / kPageSize;
       // pages wholly before the window are never loaded (a sliding-window
       // page table need not map them); the softmax zeroes their V rows
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return ok;
       };
-      while (ok && next_piece(p, t0, t1, j, ts, pc)) {
+      while (ok && next_piece(p, t0, t1, j, ts, pc, seqs)) {
         const int first = it;
         const int ntile = pc.lt1 - pc.lt0;
         if (is_qk) {
@@ -589,13 +593,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     float rs_next = 0.f;
     bool staged_next = false;
-    while (next_piece(p, t0, t1, j, ts, pc)) {
+    while (next_piece(p, t0, t1, j, ts, pc, seqs)) {
       // The next piece's Q is staged at the start of this piece's last tile,
       // so its first Q K^T overlaps that tile and this piece's epilogue.
       Piece pn;
       int jn = j;
       long long tsn = ts;
-      const bool has_next = next_piece(p, t0, t1, jn, tsn, pn);
+      const bool has_next = next_piece(p, t0, t1, jn, tsn, pn, seqs);
       const float rs = staged_next ? rs_next : stage_q(pc, piece_idx);
       staged_next = false;
       if (has_next) prefetch_q(pn);

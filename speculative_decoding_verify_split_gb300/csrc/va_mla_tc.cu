@@ -73,7 +73,8 @@ constexpr int kOffQpe = kSlots * kTileBytes;
 constexpr int kOffP = kOffQpe + kQpeBytes;
 constexpr int kOffX = kOffP + kPBufs * kPBuf;  // [2 parity][2 kh][64 rows] floats
 constexpr int kOffBar = kOffX + 1024;
-constexpr int kSmemBytes = kOffBar + 2048;
+constexpr int kOffSeqs = kOffBar + 2048;  // the batch's lengths (SeqMeta, kSeqCache)
+constexpr int kSmemBytes = kOffSeqs + 16 * kSeqCache;
 static_assert(kSmemBytes + 1024 <= 232448, "shared memory (with the 1 KB alignment slack)");
 static_assert(kTileBytes % 1024 == 0 && kOffQpe % 1024 == 0, "swizzle atoms");
 static_assert((kPBufs & (kPBufs - 1)) == 0, "P buffers: a power of two");
@@ -119,7 +120,7 @@ enum : int {
 };
 // barrier area: mbarriers | TMEM address, abort flag | scan scratch (34 x 8) |
 // last tile issued into each ring slot | per-row factors [2 rounds][64] floats
-// at +1024 (2 KB in all)
+// at +1024 (2 KB in all); then the batch's lengths (1 KB)
 constexpr int kOffTmemSlot = 8 * kNumBars;
 constexpr int kOffScratch = 256;
 constexpr int kOffSlotTile = kOffScratch + 34 * 8;  // last tile issued into each slot
@@ -217,7 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   long long t0, t1, ts_first = 0;
   int j_first = 0;
-  locate_work<kThreads>(p, c, scratch, s_j, s_ts, &t0, &t1, &j_first, &ts_first);
+  bool seqs_cached = false;
+  locate_work<kThreads>(p, c, scratch, s_j, s_ts, &t0, &t1, &j_first, &ts_first,
+                        reinterpret_cast<SeqMeta*>(sm + kOffSeqs), &seqs_cached);
+  const SeqMeta* seqs = seqs_cached ? reinterpret_cast<const SeqMeta*>(sm + kOffSeqs) : nullptr;
   if (t0 >= t1) {  // CTA-uniform
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
     return;
@@ -227,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int jq = j_first;
     long long tq = ts_first;
     Piece pq;
-    if (next_piece(p, t0, t1, jq, tq, pq)) {
+    if (next_piece(p, t0, t1, jq, tq, pq, seqs)) {
       const int r = 16 * (warp & 3) + (lane & 15), qtr = 2 * ((warp - 4) >> 2) + (lane >> 4);
       if (r < pq.R) {
         const uint16_t* src = p.q + (int64_t)(pq.q0 + r / p.group) * p.q_s0 + (int64_t)(r % p.group) * p.q_s1;
@@ -248,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long ts = ts_first;
     Piece pc;
     bool ok = true;
-    while (ok && next_piece(p, t0, t1, j, ts, pc)) {
+    while (ok && next_piece(p, t0, t1, j, ts, pc, seqs)) {
       const int npages = (pc.S + kPageSize - 1) / kPageSize;
       const int* bt_row = p.block_table + (int64_t)pc.b * p.bt_s0;
       int win = -1;
@@ -331,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return ok;
       };
-      while (ok && next_piece(p, t0, t1, j, ts, pc)) {
+      while (ok && next_piece(p, t0, t1, j, ts, pc, seqs)) {
         const int first = it;
         const int ntile = pc.lt1 - pc.lt0;
         if (is_qk) {
@@ -531,11 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     float rs_next = 0.f;
     bool staged_next = false;
-    while (next_piece(p, t0, t1, j, ts, pc)) {
+    while (next_piece(p, t0, t1, j, ts, pc, seqs)) {
       Piece pn;
       int jn = j;
       long long tsn = ts;
-      const bool has_next = next_piece(p, t0, t1, jn, tsn, pn);
+      const bool has_next = next_piece(p, t0, t1, jn, tsn, pn, seqs);
       const float rs = staged_next ? rs_next : stage_q(pc, piece_idx);
       staged_next = false;
       if (has_next) prefetch_q(pn);

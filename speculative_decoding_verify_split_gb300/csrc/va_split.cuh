@@ -55,6 +55,38 @@ __device__ __forceinline__ int work_tiles(const Params& p, int j) {
   return nt > 0 ? nt - first_tile(p, S, L) : 0;
 }
 
+// One sequence's clamped lengths as the split uses them: S cached keys, L
+// draft tokens, its first Q row q0 and causal extent E (S, or a shard's
+// kv_extent). A small batch's are kept in shared memory from the work scan
+// on (see locate_work), so that moving to the next piece reads no global
+// memory: under full HBM load each such read costs about a microsecond, and
+// every role makes it at every piece boundary.
+struct SeqMeta {
+  int S, L, q0, E;
+};
+constexpr int kSeqCache = 64;  // sequences a cache holds
+
+__device__ __forceinline__ SeqMeta seq_meta(const Params& p, const SeqMeta* cache, int b) {
+  if (cache) return cache[b];
+  SeqMeta m;
+  m.S = seq_kv_len(p, b);
+  m.L = seq_q_len(p, b);
+  m.q0 = p.cu_q[b];
+  m.E = m.S;
+  if (p.kv_extent) {
+    const int e = p.kv_extent[b];
+    m.E = e > m.S ? e : m.S;
+  }
+  return m;
+}
+
+// Key tiles of an item whose sequence has lengths m (as work_tiles).
+__device__ __forceinline__ int meta_tiles(const Params& p, const SeqMeta& m) {
+  if (m.L == 0) return 0;
+  const int nt = (m.S + p.tile_keys - 1) / p.tile_keys;
+  return nt > 0 ? nt - first_tile(p, m.S, m.L) : 0;
+}
+
 // Split cost of work item j with nt tiles: the tiles plus the item's start-up
 // cost, which comes first in split units.
 __device__ __forceinline__ long long work_cost(const Params& p, int nt) {
@@ -162,10 +194,16 @@ __device__ void find_work(const Params& p, long long x, long long* scratch, int*
 // item and the unit of that item's first tile. With at most one item per
 // thread the block scan's total is known in the same pass, so one scan does
 // both jobs; larger batches scan twice. Returns N.
+//
+// With a non-null `cache` (kSeqCache entries of shared memory) and a batch
+// small enough (at most NT items and kSeqCache sequences), the scan also
+// stores every sequence's lengths there; *cached then says so (for
+// next_piece's `cache` argument).
 template <int NT>
 __device__ long long locate_work(const Params& p, int c, long long* scratch, int* s_j,
                                  long long* s_ts, long long* t0, long long* t1, int* out_j,
-                                 long long* out_ts) {
+                                 long long* out_ts, SeqMeta* cache = nullptr, bool* cached = nullptr) {
+  if (cached) *cached = false;
   if (p.num_work > NT) {
     const long long N = scan_work<NT>(p, scratch, c == 0);
     *t0 = split_begin(N, c, p.num_splits);
@@ -174,10 +212,18 @@ __device__ long long locate_work(const Params& p, int c, long long* scratch, int
     return N;
   }
   const int j = (int)threadIdx.x;
-  const int nt = j < p.num_work ? work_tiles(p, j) : 0;
+  const bool fill = cache != nullptr && p.num_seqs <= kSeqCache;  // CTA-uniform
+  int nt = 0;
+  if (j < p.num_work) {
+    const int b = j / p.hkv;
+    const SeqMeta m = seq_meta(p, nullptr, b);
+    nt = meta_tiles(p, m);
+    if (fill && j - b * p.hkv == 0) cache[b] = m;
+  }
   const long long v = work_cost(p, nt);
   long long N;
-  const long long s = block_exclusive_scan<NT>(v, scratch, &N);
+  const long long s = block_exclusive_scan<NT>(v, scratch, &N);  // its barriers publish the cache
+  if (cached) *cached = fill;
   *t0 = split_begin(N, c, p.num_splits);
   *t1 = split_begin(N, c + 1, p.num_splits);
   if (c == 0 && j < p.num_work) p.ws_meta[j] = (int32_t)(s + (v - nt));
@@ -203,25 +249,24 @@ struct Piece {
 
 // Next (sequence, KV head) item with tiles in this CTA's split range [t0, t1);
 // ts is the split unit of item j's first tile.
+// `cache`: the sequences' lengths in shared memory (locate_work), or null.
 __device__ __forceinline__ bool next_piece(const Params& p, long long t0, long long t1, int& j,
-                                           long long& ts, Piece& pc) {
+                                           long long& ts, Piece& pc, const SeqMeta* cache = nullptr) {
   while (j < p.num_work && ts < t1) {
-    const int nt = work_tiles(p, j);
+    const int b = j / p.hkv;
+    const SeqMeta m = seq_meta(p, cache, b);
+    const int nt = meta_tiles(p, m);
     if (nt == 0) {
       ++j;
       continue;
     }
     pc.j = j;
-    pc.b = j / p.hkv;
+    pc.b = b;
     pc.kvh = j - pc.b * p.hkv;
-    pc.S = seq_kv_len(p, pc.b);
-    pc.L = seq_q_len(p, pc.b);
-    pc.E = pc.S;
-    if (p.kv_extent) {
-      const int e = p.kv_extent[pc.b];
-      pc.E = e > pc.S ? e : pc.S;
-    }
-    pc.q0 = p.cu_q[pc.b];
+    pc.S = m.S;
+    pc.L = m.L;
+    pc.E = m.E;
+    pc.q0 = m.q0;
     pc.R = p.group * pc.L;
     pc.tb = first_tile(p, pc.S, pc.L);
     pc.nt = pc.tb + nt;
