@@ -870,22 +870,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       if constexpr (FP8) {
-        // own lane holds the hi (sub 0) or lo (sub 1) part of all 128 columns
-        // of the half. Per 32-column chunk the pair splits the work: lane
-        // i + 16 sub sums and writes columns [16 sub, 16 sub + 16), sending
-        // the partner the other 16 (one shuffle per summed value)
+        // O's hi and lo rows sit 16 lanes apart, as S's do. Per 32-column
+        // chunk two 16-lane loads (hi lanes, lo lanes; second halves to
+        // threads 16-31) give thread i + 16 sub both terms of row 16q + i at
+        // columns [16 sub, 16 sub + 16), which it sums and writes.
 #pragma unroll 1
         for (int k = 0; k < 4; ++k) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + kColO + 128 * kh + 32 * k, o);
+          uint32_t oh[16], ol[16];
+          tmem_ld_16x32bx2_x16<16>(tmem + lane_base + kColO + 128 * kh + 32 * k, oh);
+          tmem_ld_16x32bx2_x16<16>(tmem + lane_base + (16u << 16) + kColO + 128 * kh + 32 * k, ol);
           tmem_wait_ld();
           uint32_t sum[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float mine = __uint_as_float(sub ? o[16 + i] : o[i]);
-            const float give = __uint_as_float(sub ? o[i] : o[16 + i]);
-            sum[i] = __float_as_uint(mine + __shfl_xor_sync(0xffffffffu, give, 16));
-          }
+          for (int i = 0; i < 16; ++i) sum[i] = __float_as_uint(__uint_as_float(oh[i]) + __uint_as_float(ol[i]));
           emit(sum, 128 * kh + 32 * k + 16 * sub, std::integral_constant<int, 16>{});
         }
       } else {
