@@ -24,7 +24,8 @@
 //    Ql = e4m3(Q 2^e - Qh); P is split the same way. The two terms are
 //    stacked in one M=128 MMA: packed row 16q + i uses A rows 32q + i (hi)
 //    and 32q + 16 + i (lo), so the hi and lo results land in lanes i and
-//    16 + i of the same TMEM lane quadrant and one lane shuffle adds them.
+//    16 + i of the same TMEM lane quadrant; two 16-lane TMEM loads hand each
+//    softmax thread both terms of its own keys, which it adds.
 //    P is written back into TMEM over its S tile, and P V reads its A operand
 //    there; the smem this saves buys a third K and V ring slot (3 + 3).
 //    K and V are never dequantised.
@@ -51,12 +52,16 @@
 // Online softmax in log2 units keeps a per-row reference m_ref and computes
 // P = 2^(s - m_ref + 6) <= 2^8.8; m_ref moves (and O, l are rescaled in
 // TMEM) only when a tile's max exceeds it by more than 2.8, and a row's first
-// m_ref sits 4 above its first tile's max, so rescales are rare. The VAR instantiation adds the generic attention's variants (sliding
+// m_ref sits 4 above its first tile's max, so rescales are rare. The tile
+// max is taken over the raw dot products and the (positive) row scale
+// applied inside the FMA of P's exponent. The VAR instantiation adds the
+// generic attention's variants (sliding
 // window, logit soft cap, sinks). Waits are bounded in time and warp-uniform:
 // on a timeout the kernel sets the workspace status word, stops issuing
 // work, drains and frees its TMEM. The epilogue writes split partials as
-// fp32 with 32-byte stores (whole L2 sectors), each lane of a hi/lo pair
-// summing and writing half of every 32-column chunk.
+// fp32 with 32-byte stores (whole L2 sectors), each thread of a hi/lo lane
+// pair summing and writing half of every 32-column chunk. A batch of at most
+// 64 sequences keeps its lengths in shared memory for the piece walk.
 #include <type_traits>
 
 #include <cuda_bf16.h>
