@@ -213,18 +213,49 @@ def throughput(alg_bytes: int, world: int, ms_per_step: float) -> float:
     return alg_bytes * world / (ms_per_step / 1e3) / 1e9
 
 
-def workload_config(w, name, world):
+def config_block(name, q_lens, kv_lens, hq, hkv, kv_dtype, alg_bytes, world):
+    """The JSON line's config: the workload by name, its seeded lengths and
+    sizes. Both arms print it (the reference arm from the same seeded
+    structure, without drawing the cache)."""
     layout = ({"layout": "absorbed-MLA latent cache, rows [latent 512 | rope 64], values = latent",
                "row_width": 576, "value_dim": 512} if is_mla(name) else {"head_dim": 256})
-    return {"workload": name, "num_seqs": w.num_seqs, "q_lens": sorted(set(w.q_lens)),
-            "kv_len_range": [min(w.kv_lens), max(w.kv_lens)], "kv_tokens": sum(w.kv_lens),
-            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, **layout,
-            "page_size": 16, "kv_dtype": w.kv_dtype, "algorithmic_bytes": w.algorithmic_bytes(),
+    return {"workload": name, "num_seqs": len(q_lens), "q_lens": sorted(set(q_lens)),
+            "kv_len_range": [min(kv_lens), max(kv_lens)], "kv_tokens": sum(kv_lens),
+            "num_q_heads": hq, "num_kv_heads": hkv, **layout,
+            "page_size": 16, "kv_dtype": kv_dtype, "algorithmic_bytes": alg_bytes,
             "l2": ("inputs under 2x the 129 MB L2: a 256 MB buffer is written before every step, "
-                   "outside the per-step CUDA events" if needs_flush(w) else
+                   "outside the per-step CUDA events" if alg_bytes < 2 * L2_BYTES else
                    "inputs exceed the 129 MB L2; steps back to back, no flush"),
             "accumulate": "f32",
             "parallelism": f"replicas x{world}", "seed": 0}
+
+
+def workload_config(w, name, world):
+    return config_block(name, w.q_lens, w.kv_lens, w.num_q_heads, w.num_kv_heads, w.kv_dtype,
+                        w.algorithmic_bytes(), world)
+
+
+def reference_structure(name):
+    """The seeded structure of a workload (lengths, heads, cache type) and its
+    algorithmic bytes as Workload / MlaWorkload count them, without drawing
+    any values."""
+    from speculative_decoding_verify_split_gb300.workloads import mla_workload_structure, workload_structure
+    mla = is_mla(name)
+    if mla:
+        st = dict(mla_workload_structure(name, 0), Hkv=1)
+        st.setdefault("kv_dtype", "fp8_e4m3")
+    else:
+        st = workload_structure(name, 0)
+    e = 1 if st["kv_dtype"] == "fp8_e4m3" else 2
+    key_bytes = 576 * e if mla else st["Hkv"] * 512 * e  # cache bytes per key
+    q_bytes = st["Hq"] * ((576 + 512) * 2 if mla else 2 * 256 * 2)  # per draft token: Q in, out
+    alg = sum(st["kv_lens"]) * key_bytes + sum(st["q_lens"]) * q_bytes
+    return st, key_bytes, alg
+
+
+def reference_config(name, world):
+    st, _, alg = reference_structure(name)
+    return config_block(name, st["q_lens"], st["kv_lens"], st["Hq"], st["Hkv"], st["kv_dtype"], alg, world)
 
 
 def seq_bytes(w, b, mla):
@@ -621,20 +652,14 @@ def run_reference(args):
     rank = env_int("RANK", 0)
     if rank != 0:
         return
-    from speculative_decoding_verify_split_gb300.workloads import (make_mla_workload, make_workload,
-                                                                   mla_workload_structure,
-                                                                   workload_structure)
+    from speculative_decoding_verify_split_gb300.workloads import make_mla_workload, make_workload
     mla = is_mla(args.workload)
     if mla:
         from oracle.mla_fp64 import mla_oracle_from_torch as oracle_from_torch
-        st = dict(mla_workload_structure(args.workload, 0), Hkv=1)
-        st.setdefault("kv_dtype", "fp8_e4m3")
     else:
         from oracle.attention_fp64 import oracle_from_torch
-        st = workload_structure(args.workload, 0)
+    st, key_bytes, _ = reference_structure(args.workload)
     q_lens, kv_lens = st["q_lens"], st["kv_lens"]
-    e = 1 if st["kv_dtype"] == "fp8_e4m3" else 2
-    key_bytes = 576 * e if mla else st["Hkv"] * 512 * e  # cache bytes per key
 
     def sample(b, cap, seed):
         S = min(kv_lens[b], cap)
@@ -669,10 +694,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "num_seqs": len(q_lens), "q_len": q_lens[0],
-                       "num_q_heads": st["Hq"], "num_kv_heads": st["Hkv"],
-                       **({"row_width": 576, "value_dim": 512} if mla else {"head_dim": 256}),
-                       "page_size": 16, "kv_dtype": st["kv_dtype"]},
+            "config": reference_config(args.workload, args.gpus),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"each step one sequence of the workload's shape with kv_len "
                                        f"capped at {cap}"},

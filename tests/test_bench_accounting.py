@@ -60,3 +60,30 @@ def test_throughput_is_whole_job():
     bench = _bench()
     assert bench.throughput(10**9, 1, 1.0) == pytest.approx(1000.0)
     assert bench.throughput(10**9, 4, 2.0) == pytest.approx(2000.0)
+
+
+@pytest.mark.parametrize("name", ["tiny_verify", "gqa_32q2kv", "mla_tiny", "mla_tiny_bf16"])
+@pytest.mark.parametrize("world", [1, 4])
+def test_reference_arm_reports_our_config(name, world):
+    """The reference arm (the oracle on the host cores) reports the same
+    config block as our arm, computed from the seeded structure alone."""
+    from speculative_decoding_verify_split_gb300.workloads import named_mla_workload, named_workload
+    b = _bench()
+    w = named_mla_workload(name) if name.startswith("mla_") else named_workload(name)
+    assert b.reference_config(name, world) == b.workload_config(w, name, world)
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS) + list(MLA_WORKLOADS))
+def test_reference_bytes_match_the_structure(name):
+    b = _bench()
+    _, _, alg = b.reference_structure(name)
+    if name in WORKLOADS:
+        assert alg == workload_sizes(name)["algorithmic_bytes"]
+    else:
+        st = mla_workload_structure(name)
+        w = make_mla_workload([1] * len(st["q_lens"]), [1] * len(st["kv_lens"]), st["Hq"],
+                              st.get("kv_dtype", "fp8_e4m3"), seed=0)
+        e = 1 if st.get("kv_dtype", "fp8_e4m3") == "fp8_e4m3" else 2
+        per_key, per_token = 576 * e, st["Hq"] * (576 + 512) * 2
+        assert w.algorithmic_bytes() == len(st["kv_lens"]) * per_key + len(st["q_lens"]) * per_token
+        assert alg == sum(st["kv_lens"]) * per_key + sum(st["q_lens"]) * per_token
