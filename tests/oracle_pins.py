@@ -197,6 +197,31 @@ def pin_constant_keys(orc):
                 _close(got[q0 + t, h], ref)
 
 
+def pin_zero_scale(orc):
+    """softmax_scale 0 => every visible logit 0 => out = mean of visible V,
+    whatever Q and K hold (the kernels turn 0 into a tiny positive scale)."""
+    ql, kl = [4, 2], [37, 20]
+    w = make_workload(ql, kl, 8, 2, "fp8_e4m3", seed=27, softmax_scale=0.0, k_descale=1.7)
+    got = run(orc, w)
+    for b in range(2):
+        _, v = dense_kv(w, b)
+        S, L, q0 = kl[b], ql[b], int(w.cu_seqlens_q[b])
+        for t in range(L):
+            n = S - L + t + 1
+            for h in range(8):
+                _close(got[q0 + t, h], v[:n, h // 4, :].mean(dim=0).numpy())
+
+
+def pin_negative_scale_sdpa(orc):
+    """A negative softmax scale (the softmax of the negated logits) against
+    torch's float64 SDPA with the same scale."""
+    w = make_workload([4, 3], [90, 41], 16, 1, "bf16", seed=29, softmax_scale=-1 / 16)
+    got = run(orc, w)
+    for b in range(2):
+        q0, L = int(w.cu_seqlens_q[b]), int(w.cu_seqlens_q[b + 1] - w.cu_seqlens_q[b])
+        _close(got[q0:q0 + L], sdpa_reference(w, b), tol=1e-10)
+
+
 def pin_spike_boundary(orc):
     """All-zero keys except one large key at position p = S - 2: with L = 4,
     tokens 0 and 1 do not see it (uniform mean over their keys), tokens 2 and 3
@@ -328,4 +353,5 @@ def pin_sink_closed_forms(orc):
 ALL_PINS = [pin_e4m3_exhaustive, pin_e4m3_spec_points, pin_bf16_exhaustive, pin_sdpa_bruteforce,
             pin_gqa_equals_mha, pin_page_permutation, pin_qlen1_decode, pin_constant_keys,
             pin_spike_boundary, pin_descale, pin_empty_rows, pin_window_sdpa,
-            pin_window_never_reads_pages_before_it, pin_softcap_closed_forms, pin_sink_closed_forms]
+            pin_window_never_reads_pages_before_it, pin_softcap_closed_forms, pin_sink_closed_forms,
+            pin_zero_scale, pin_negative_scale_sdpa]

@@ -44,6 +44,14 @@ def _attend_no_scale(q, K, V, n, scale, *rest):
     return _real_attend(q, K, V, n, 1.0, *rest)
 
 
+def _attend_abs_scale(q, K, V, n, scale, *rest):
+    return _real_attend(q, K, V, n, abs(scale), *rest)
+
+
+def _attend_zero_scale_as_one(q, K, V, n, scale, *rest):
+    return _real_attend(q, K, V, n, scale if scale != 0 else 1.0, *rest)
+
+
 def _attend_keys_as_values(q, K, V, n, scale, *rest):
     return _real_attend(q, K, K, n, scale, *rest)
 
@@ -87,6 +95,8 @@ MUTATIONS = {
     "ignores_block_table": ("gather_kv", _gather_logical_pages),
     "drops_descale": ("gather_kv", _gather_no_descale),
     "drops_softmax_scale": ("softmax_attend", _attend_no_scale),
+    "softmax_scale_sign_dropped": ("softmax_attend", _attend_abs_scale),
+    "zero_softmax_scale_as_one": ("softmax_attend", _attend_zero_scale_as_one),
     "keys_used_as_values": ("softmax_attend", _attend_keys_as_values),
     "rows_reversed": ("softmax_attend", _attend_reversed_rows),
     "window_off_by_one": ("first_visible_key", _window_off_by_one),
