@@ -138,7 +138,30 @@ def pin_sdpa_bf16(orc):
             assert np.abs(out[q0:q0 + q_lens[b]] - ref).max() < 1e-10
 
 
-PINS = [pin_sdpa, pin_gqa_oracle_on_padded_values, pin_constant_rows_and_rope_spike, pin_sdpa_bf16]
+def pin_scale_sign_and_zero(orc):
+    """A negative softmax scale against torch's float64 SDPA with that scale,
+    and a zero one against the mean of the visible latent rows times
+    v_descale (every logit 0)."""
+    w = make_mla_workload([4, 2], [70, 33], 8, seed=47, k_descale=1.2, v_descale=0.9, softmax_scale=-0.08)
+    out = run(orc, w)
+    for b, L in enumerate([4, 2]):
+        q0 = int(w.cu_seqlens_q[b])
+        ref = sdpa_mla(w, b)
+        assert np.abs(out[q0:q0 + L] - ref).max() <= 1e-11 * max(1.0, np.abs(ref).max())
+    w = make_mla_workload([3, 1], [40, 18], 4, seed=48, v_descale=0.9, softmax_scale=0.0)
+    out = run(orc, w)
+    for b, (L, S) in enumerate([(3, 40), (1, 18)]):
+        q0 = int(w.cu_seqlens_q[b])
+        n = (S + 15) // 16
+        pages = w.block_table[b, :n].long()
+        lat = w.kv_cache[pages].to(torch.float64).reshape(n * 16, -1)[:S, :w.nope_dim] * float(w.v_descale[0])
+        for t in range(L):
+            ref = lat[:S - L + t + 1].mean(dim=0).numpy()
+            assert np.abs(out[q0 + t] - ref[None, :]).max() <= 1e-11 * max(1.0, np.abs(ref).max())
+
+
+PINS = [pin_sdpa, pin_gqa_oracle_on_padded_values, pin_constant_rows_and_rope_spike, pin_sdpa_bf16,
+        pin_scale_sign_and_zero]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -178,8 +201,16 @@ def _visible_minus_one(S, L, t):
     return max(0, min(S, S - L + t))
 
 
+_real_attend = mla._attend
+
+
+def _attend_abs_scale(q_rows, K, V, n_vis, scale, nope_dim):
+    return _real_attend(q_rows, K, V, n_vis, abs(scale), nope_dim)
+
+
 MUTATIONS = [("mla_logit_rows", _rope_dropped), ("latent_and_rope", _values_from_the_tail),
-             ("query_parts", _query_parts_swapped), ("visible_keys", _visible_minus_one)]
+             ("query_parts", _query_parts_swapped), ("visible_keys", _visible_minus_one),
+             ("_attend", _attend_abs_scale)]
 
 
 @pytest.mark.parametrize("name,fake", MUTATIONS, ids=[m[0] for m in MUTATIONS])
