@@ -26,9 +26,11 @@
 //    and 32q + 16 + i (lo), so the hi and lo results land in lanes i and
 //    16 + i of the same TMEM lane quadrant; two 16-lane TMEM loads hand each
 //    softmax thread both terms of its own keys, which it adds.
-//    P is written back into TMEM over its S tile, and P V reads its A operand
-//    there; the smem this saves buys a third K and V ring slot (3 + 3).
-//    K and V are never dequantised.
+//    Q K^T and P V take their A operands (Q, P) from TMEM: Q is staged there
+//    by the softmax warps, P written there beside the one S tile, which is
+//    free again once the softmax has loaded it. The shared memory this
+//    leaves to the rings holds 4 K + 3 V slots. K and V are never
+//    dequantised.
 //  * BF16 cache, kind::f16, M=64 (packed row 16q + i in lane 32q + i); P goes
 //    through four smem buffers; rings 3 K + 2 V.
 // V is the MN-major B operand of O += P V. The k/v descales fold into the
@@ -40,7 +42,7 @@
 //              (V ring, freed after P V). Block-table walk with 32 page ids
 //              per lane load, read before waiting for the ring slot; one
 //              2 KB box per lane.
-//  warp 1      TMEM owner; one thread issues Q K^T into the S buffers.
+//  warp 1      TMEM owner; one thread issues Q K^T into the S buffer(s).
 //  warp 12     one thread issues P V into O.
 //  warps 4-11  softmax, two warps per TMEM lane quadrant q = w % 4 (both on
 //              the same SMSP). Warp half kh = (w - 4) / 4 takes half of each
@@ -82,8 +84,8 @@ struct Cfg {
   static constexpr int kT = FP8 ? kTcTileKeysFp8 : kTcTileKeysBf16;  // keys per tile: 128 / 64
   static constexpr int kPagesPerTile = kT / kPageSize;
   static constexpr int kKpt = kT / 4;                      // keys per softmax thread per tile
-  static constexpr int kSBufs = FP8 ? 2 : 4;               // S tiles in TMEM (256 columns)
-  static constexpr int kPBufs = FP8 ? 2 : 4;               // P buffers in smem (32 KB)
+  static constexpr int kSBufs = FP8 ? 1 : 4;               // S tiles in TMEM (128 / 256 columns)
+  static constexpr int kPBufs = FP8 ? 2 : 4;               // P buffers: TMEM (fp8) / smem (bf16)
   static constexpr int kEsize = FP8 ? 1 : 2;               // bytes per KV element
   static constexpr int kChunks = kHeadDim * kEsize / 128;  // 128-byte d chunks (2 or 4)
   static constexpr int kRegion = kT * 128;                 // one d chunk of a K or V tile
@@ -91,11 +93,15 @@ struct Cfg {
   // Separate K and V rings of 32 KB tiles (a K slot is free again once Q K^T
   // has read it, a V slot only after P V). A slot turns over in about DRAM
   // latency + hold + producer reaction (~3500 + 1500 + 500 cycles at full HBM
-  // load), so the tile rate is slots / that: FP8 keeps P in TMEM and spends
-  // the freed shared memory on three slots per ring (192 KB); BF16 keeps its
-  // smem P buffers and has room for 3 K + 2 V (160 KB).
+  // load), so the tile rate is slots / that. FP8 keeps Q, S and P in TMEM and
+  // spends the shared memory on 4 K + 3 V slots (224 KB): with one S tile,
+  // Q K^T of a tile waits for the softmax to load the previous S, which
+  // lengthens a K slot's hold (measured: 4 K + 3 V beats 3 K + 4 V by 1.8 us
+  // on a 128 us call). BF16 keeps Q and its P buffers in shared memory and
+  // has room for 3 K + 2 V (160 KB).
   static constexpr bool kPInTmem = FP8;
-  static constexpr int kKSlots = 3;
+  static constexpr bool kQInTmem = FP8;
+  static constexpr int kKSlots = FP8 ? 4 : 3;
   static constexpr int kVSlots = FP8 ? 3 : 2;
   static constexpr int kRingBytes = (kKSlots + kVSlots) * 32768;
   // Producer warps: one streams K, two alternate on V's tiles. A producer's
@@ -118,18 +124,19 @@ struct Cfg {
   static constexpr uint32_t kIdQK = instr_desc(kFmt, kFmt, false, kT, kM);
   static constexpr uint32_t kIdPV = instr_desc(kFmt, kFmt, true, kHeadDim, kM);
   static_assert(kTensorBytes == 32768, "ring slot size");
-  // shared memory: rings | Q | P buffers (smem P only) | row exchange | barriers
+  // shared memory: rings | Q (smem Q only) | P buffers (smem P only) | row
+  // exchange | barriers
   static constexpr int kOffQ = kRingBytes;
-  static constexpr int kOffP = kOffQ + 32768;
+  static constexpr int kOffP = kOffQ + (kQInTmem ? 0 : 32768);
   static constexpr int kOffX = kOffP + (kPInTmem ? 0 : 32768);  // [2 parity][2 kh][64 rows] floats
   static constexpr int kOffBar = kOffX + 1024;
   static constexpr int kOffSeqs = kOffBar + 1024;  // the batch's lengths (SeqMeta, kSeqCache)
   static constexpr int kSmemBytes = kOffSeqs + 16 * kSeqCache;
   static_assert(kSmemBytes <= 232448, "shared memory");
-  static_assert(!kPInTmem || kSBufs == kPBufs, "a TMEM P shares its S buffer's index and barriers");
   static_assert(kChunks * kQRegion == 32768, "Q size");
-  static_assert(kPBufs * kPBuf == 32768, "P buffers");
-  static_assert(kSBufs * kT == 256, "S buffers");
+  static_assert(kPInTmem || kPBufs * kPBuf == 32768, "P buffers");
+  static_assert(kSBufs * kT == (FP8 ? 128 : 256), "S buffers");
+  static_assert(kPInTmem == kQInTmem, "the TMEM layout below");
   static_assert(kPagesPerTile * kChunks <= 32, "one TMA box per lane");
 };
 
@@ -138,8 +145,14 @@ constexpr int kMaxPBufs = 4;
 constexpr int kThreads = 416;  // 13 warps
 constexpr int kSoftmaxThreads = 256;
 
+// TMEM columns. BF16: O [0, 256), four 64-column S tiles [256, 512). FP8: O,
+// one 128-column S tile, two P tiles of 32 columns (128 keys of e4m3, hi row
+// in lane 32q + i, lo row in lane 32q + 16 + i, as S) and the Q A operand
+// (64 columns: 256 e4m3 bytes of each hi and lo row).
 constexpr uint32_t kColO = 0;    // 256 fp32 columns
-constexpr uint32_t kColS = 256;  // four 64-column S tiles
+constexpr uint32_t kColS = 256;
+constexpr uint32_t kColP = 384;  // FP8
+constexpr uint32_t kColQ = 448;  // FP8
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -395,20 +408,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = cur % C::kKSlots;
             const int b = cur & (kSBufs - 1);
             if (!wait_or_fail(kBarFullK + s, (cur / C::kKSlots) & 1, 32)) break;
-            // S buffer b is free once the softmax has read S(cur - kSBufs) or,
-            // with P in TMEM over it, once P V(cur - kSBufs) has read that P
-            if (cur >= kSBufs &&
-                !wait_or_fail(C::kPInTmem ? kBarPFree + b : kBarSFree + b, ((cur - kSBufs) / kSBufs) & 1, 64))
-              break;
+            // S buffer b is free once the softmax has read S(cur - kSBufs)
+            if (cur >= kSBufs && !wait_or_fail(kBarSFree + b, ((cur - kSBufs) / kSBufs) & 1, 64)) break;
             tc_fence_after();
             const uint32_t kst = sbase + s * C::kTensorBytes;
 #pragma unroll
             for (int k = 0; k < C::kQkSteps; ++k) {
-              const uint32_t qoff = (uint32_t)((k >> 2) * C::kQRegion + (k & 3) * 32);
               const uint32_t koff = (uint32_t)((k >> 2) * C::kRegion + (k & 3) * 32);
-              const uint64_t a = smem_desc(qbase + qoff, 16, 1024, kLayoutSw128);
               const uint64_t bdesc = smem_desc(kst + koff, 16, 1024, kLayoutSw128);
-              mma<FP8>(tmem + kColS + b * kT, a, bdesc, C::kIdQK, k ? 1u : 0u);
+              if constexpr (C::kQInTmem) {
+                // Q's d bytes [32 k, +32) are columns [8 k, +8) of its TMEM rows
+                mma_f8f6f4_ta(tmem + kColS + b * kT, tmem + kColQ + 8 * k, bdesc, C::kIdQK, k ? 1u : 0u);
+              } else {
+                const uint32_t qoff = (uint32_t)((k >> 2) * C::kQRegion + (k & 3) * 32);
+                const uint64_t a = smem_desc(qbase + qoff, 16, 1024, kLayoutSw128);
+                mma<FP8>(tmem + kColS + b * kT, a, bdesc, C::kIdQK, k ? 1u : 0u);
+              }
             }
             mma_commit(bar(kBarSFull + b));
             mma_commit(bar(kBarEmptyK + s));
@@ -431,8 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                1024, kLayoutSw128);
               const uint32_t acc = (i == 0 && kk == 0) ? 0u : 1u;
               if constexpr (C::kPInTmem) {
-                // P(x) sits in the first kT/4 columns of S buffer pb, 8 per K-step
-                mma_f8f6f4_ta(tmem + kColO, tmem + kColS + pb * kT + 8 * kk, bdesc, C::kIdPV, acc);
+                // P(x) sits in P tile pb, 8 columns per K-step
+                mma_f8f6f4_ta(tmem + kColO, tmem + kColP + pb * (kT / 4) + 8 * kk, bdesc, C::kIdPV, acc);
               } else {
                 const uint64_t a = smem_desc(pbuf + kk * 256, 128, C::kPSbo, kLayoutNone);
                 mma<FP8>(tmem + kColO, a, bdesc, C::kIdPV, acc);
@@ -541,31 +556,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float up = __uint_as_float((uint32_t)(e + 127) << 23) * (q_neg ? -1.f : 1.f);
           const float down = __uint_as_float((uint32_t)(127 - e) << 23);
           rs = cscale * down;  // rows past R stage zeros: their logits are 0
-          // d [64 qtr, +64) = region kh, 16-byte pieces 4 sub .. 4 sub + 3;
-          // hi to A row 32q + rl, lo to A row 32q + 16 + rl
+          // d [64 qtr, +64): 16 words of each term, the TMEM A operand's
+          // columns [16 qtr, +16) of lane 32q + rl (hi) and lane 32q + 16 + rl
+          // (lo): per half of them two 16-lane stores, threads 16-31 (sub 1)
+          // at +16
           if (ok) {
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              uint32_t hw[4], lw[4];
+            for (int h = 0; h < 2; ++h) {
+              uint32_t hw[8], lw[8];
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint4 a = raw[2 * cc + (k >> 1)];
-                const uint32_t wa = (k & 1) ? a.z : a.x;
-                const uint32_t wb = (k & 1) ? a.w : a.y;
-                const float x0 = __uint_as_float(wa << 16) * up, x1 = __uint_as_float(wa & 0xFFFF0000u) * up;
-                const float x2 = __uint_as_float(wb << 16) * up, x3 = __uint_as_float(wb & 0xFFFF0000u) * up;
-                const uint32_t h01 = pack_fp8x2(x0, x1), h23 = pack_fp8x2(x2, x3);
-                const float2 f01 = unpack_fp8x2(h01), f23 = unpack_fp8x2(h23);
-                const uint32_t l01 = pack_fp8x2(x0 - f01.x, x1 - f01.y), l23 = pack_fp8x2(x2 - f23.x, x3 - f23.y);
-                hw[k] = h01 | (h23 << 16);
-                lw[k] = l01 | (l23 << 16);
+              for (int c2 = 0; c2 < 2; ++c2) {
+                const int cc = 2 * h + c2;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint4 a = raw[2 * cc + (k >> 1)];
+                  const uint32_t wa = (k & 1) ? a.z : a.x;
+                  const uint32_t wb = (k & 1) ? a.w : a.y;
+                  const float x0 = __uint_as_float(wa << 16) * up, x1 = __uint_as_float(wa & 0xFFFF0000u) * up;
+                  const float x2 = __uint_as_float(wb << 16) * up, x3 = __uint_as_float(wb & 0xFFFF0000u) * up;
+                  const uint32_t h01 = pack_fp8x2(x0, x1), h23 = pack_fp8x2(x2, x3);
+                  const float2 f01 = unpack_fp8x2(h01), f23 = unpack_fp8x2(h23);
+                  const uint32_t l01 = pack_fp8x2(x0 - f01.x, x1 - f01.y), l23 = pack_fp8x2(x2 - f23.x, x3 - f23.y);
+                  hw[4 * c2 + k] = h01 | (h23 << 16);
+                  lw[4 * c2 + k] = l01 | (l23 << 16);
+                }
               }
-              const int piece16 = 4 * sub + cc;
-              const int swz = (piece16 ^ (rl & 7)) << 4;
-              const int ahi = 32 * q + rl, alo = ahi + 16;
-              *reinterpret_cast<uint4*>(qs + kh * C::kQRegion + ahi * 128 + swz) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-              *reinterpret_cast<uint4*>(qs + kh * C::kQRegion + alo * 128 + swz) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+              tmem_st_16x32bx2_x8<16>(tmem + lane_base + kColQ + 32 * kh + 8 * h, hw);
+              tmem_st_16x32bx2_x8<16>(tmem + lane_base + (16u << 16) + kColQ + 32 * kh + 8 * h, lw);
             }
+            tmem_wait_st();
           }
         } else {
           rs = cscale;  // rows past R stage zeros: their logits are 0
@@ -582,7 +601,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (ok) {
-        fence_proxy_async_smem();
+        if constexpr (C::kQInTmem)
+          tc_fence_before();
+        else
+          fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarQFull));
       }
@@ -653,13 +675,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the hi and lo partials of row 16q + rl, keys [64 kh + 32 sub,
             // +32): two 16-lane loads (hi rows in lanes 32q.., lo rows in
             // lanes 32q + 16..) whose second halves go to threads 16-31, so
-            // every thread gets both terms of its own keys
-            // (S buffer b is then overwritten by P(cur); P V's commit frees it)
+            // every thread gets both terms of its own keys; S buffer b is then
+            // free for Q K^T of the next tile
             uint32_t vh[32], vl[32];
             tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kColS + b * kT + 64 * kh, vh);
             tmem_ld_16x32bx2_x32<32>(tmem + lane_base + (16u << 16) + kColS + b * kT + 64 * kh, vl);
             tmem_wait_ld();
             tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarSFree + b));
 #pragma unroll
             for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(vh[i]) + __uint_as_float(vl[i]);
           } else {
@@ -702,11 +726,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmax = exchange(tmax * xs, true);  // log2 units (xs > 0 keeps the order)
         if (!ok) continue;
 
-        // P buffer pb was last read by PV(cur - kPBufs). (A TMEM P goes over
-        // S(cur), whose Q K^T already waited for that.)
-        if (!C::kPInTmem && cur >= kPBufs &&
-            !wait_or_fail(kBarPFree + pb, ((cur - kPBufs) / kPBufs) & 1, 512))
-          continue;
+        // P buffer pb was last read by PV(cur - kPBufs)
+        if (cur >= kPBufs && !wait_or_fail(kBarPFree + pb, ((cur - kPBufs) / kPBufs) & 1, 512)) continue;
 
         const bool need = tmax > m_ref + kOvershoot;
         // A row's first reference takes more headroom: its running max keeps
@@ -767,15 +788,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               pl[i >> 1] = l2;
             }
           }
-          // A operand of P V in TMEM, over S(cur): lane 32q + rl (hi row) and
+          // A operand of P V in TMEM, P tile pb: lane 32q + rl (hi row) and
           // lane 32q + 16 + rl (lo row) take the e4m3 bytes of keys
           // [64 kh, +64) at columns [16 kh, +16). This thread holds keys
           // [32 qtr, +32) of both: two 16-lane stores, its hi bytes into the
           // hi row and its lo bytes into the lo row, threads 16-31 at +8.
-          // The quadrant's other warp read its S columns before the exchange.
           tc_fence_after();
-          tmem_st_16x32bx2_x8<8>(tmem + lane_base + kColS + b * kT + 16 * kh, ph);
-          tmem_st_16x32bx2_x8<8>(tmem + lane_base + (16u << 16) + kColS + b * kT + 16 * kh, pl);
+          tmem_st_16x32bx2_x8<8>(tmem + lane_base + kColP + pb * (kT / 4) + 16 * kh, ph);
+          tmem_st_16x32bx2_x8<8>(tmem + lane_base + (16u << 16) + kColP + pb * (kT / 4) + 16 * kh, pl);
           tmem_wait_st();
         } else {
           uint32_t pw[8];
@@ -808,8 +828,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // FullV(vs) alternates between the tiles that share slot vs, so its
           // parity names tile cur only once the slot's previous tile
           // (cur - kVSlots) has been consumed by P V. The softmax at tile cur
-          // only knows P V(cur - kPBufs) done (its P buffer, or for a TMEM P
-          // the S buffer Q K^T waited for); if that is not enough, wait.
+          // only knows P V(cur - kPBufs) done (its P buffer's wait above); if
+          // that is not enough, wait.
           if constexpr (kPBufs > C::kVSlots) {
             const int xv = cur - C::kVSlots;
             if (xv >= 0 && !wait_or_fail(kBarPFree + (xv & (kPBufs - 1)), (xv / kPBufs) & 1, 2049)) continue;
