@@ -29,8 +29,10 @@
 //    Q K^T and P V take their A operands (Q, P) from TMEM: Q is staged there
 //    by the softmax warps, P written there beside the one S tile, which is
 //    free again once the softmax has loaded it. The shared memory this
-//    leaves to the rings holds 4 K + 3 V slots. K and V are never
-//    dequantised.
+//    leaves to the rings holds 4 K + 3 V slots. The variant kernel, whose
+//    soft cap can make the softmax the bottleneck, keeps Q in shared memory
+//    and two S tiles, each P written over its S (3 K + 3 V). K and V are
+//    never dequantised.
 //  * BF16 cache, kind::f16, M=64 (packed row 16q + i in lane 32q + i); P goes
 //    through four smem buffers; rings 3 K + 2 V.
 // V is the MN-major B operand of O += P V. The k/v descales fold into the
@@ -79,12 +81,22 @@ namespace {
 
 using namespace ptx;
 
-template <bool FP8>
+template <bool FP8, bool VAR>
 struct Cfg {
   static constexpr int kT = FP8 ? kTcTileKeysFp8 : kTcTileKeysBf16;  // keys per tile: 128 / 64
   static constexpr int kPagesPerTile = kT / kPageSize;
   static constexpr int kKpt = kT / 4;                      // keys per softmax thread per tile
-  static constexpr int kSBufs = FP8 ? 1 : 4;               // S tiles in TMEM (128 / 256 columns)
+  // FP8 has two TMEM layouts. The plain kernel takes Q and P from TMEM
+  // (one S tile, two P tiles of their own) and spends the shared memory on
+  // a fourth K ring slot. The variant kernel keeps Q in shared memory and
+  // two S tiles, with P written over its S tile: a soft cap makes the
+  // softmax the bottleneck, and with one S tile every tile's Q K^T waits on
+  // the softmax's load of the previous S, its MMA issue slowed by the
+  // softmax warps' ALU work on the same sub-partitions (soft cap 30 on
+  // long_context_fp8: 146.3 us against 137.0 us with two S tiles).
+  static constexpr bool kQInTmem = FP8 && !VAR;
+  static constexpr bool kPOverS = FP8 && VAR;
+  static constexpr int kSBufs = FP8 ? (kQInTmem ? 1 : 2) : 4;  // S tiles in TMEM
   static constexpr int kPBufs = FP8 ? 2 : 4;               // P buffers: TMEM (fp8) / smem (bf16)
   static constexpr int kEsize = FP8 ? 1 : 2;               // bytes per KV element
   static constexpr int kChunks = kHeadDim * kEsize / 128;  // 128-byte d chunks (2 or 4)
@@ -93,15 +105,14 @@ struct Cfg {
   // Separate K and V rings of 32 KB tiles (a K slot is free again once Q K^T
   // has read it, a V slot only after P V). A slot turns over in about DRAM
   // latency + hold + producer reaction (~3500 + 1500 + 500 cycles at full HBM
-  // load), so the tile rate is slots / that. FP8 keeps Q, S and P in TMEM and
-  // spends the shared memory on 4 K + 3 V slots (224 KB): with one S tile,
-  // Q K^T of a tile waits for the softmax to load the previous S, which
-  // lengthens a K slot's hold (measured: 4 K + 3 V beats 3 K + 4 V by 1.8 us
-  // on a 128 us call). BF16 keeps Q and its P buffers in shared memory and
-  // has room for 3 K + 2 V (160 KB).
+  // load), so the tile rate is slots / that. FP8 with Q in TMEM has room for
+  // 4 K + 3 V slots (224 KB): with one S tile, Q K^T of a tile waits for the
+  // softmax to load the previous S, which lengthens a K slot's hold
+  // (measured: 4 K + 3 V beats 3 K + 4 V by 1.8 us on a 128 us call); with
+  // Q in shared memory, 3 K + 3 V (192 KB). BF16 keeps Q and its P buffers in
+  // shared memory and has room for 3 K + 2 V (160 KB).
   static constexpr bool kPInTmem = FP8;
-  static constexpr bool kQInTmem = FP8;
-  static constexpr int kKSlots = FP8 ? 4 : 3;
+  static constexpr int kKSlots = kQInTmem ? 4 : 3;
   static constexpr int kVSlots = FP8 ? 3 : 2;
   static constexpr int kRingBytes = (kKSlots + kVSlots) * 32768;
   // Producer warps: one streams K, two alternate on V's tiles. A producer's
@@ -135,8 +146,9 @@ struct Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kChunks * kQRegion == 32768, "Q size");
   static_assert(kPInTmem || kPBufs * kPBuf == 32768, "P buffers");
-  static_assert(kSBufs * kT == (FP8 ? 128 : 256), "S buffers");
-  static_assert(kPInTmem == kQInTmem, "the TMEM layout below");
+  static_assert(kSBufs * kT == (kQInTmem ? 128 : 256), "S buffers");
+  static_assert(!kPOverS || kSBufs == kPBufs, "a P over its S tile shares that tile's index and barriers");
+  static_assert(!kQInTmem || kPInTmem, "the TMEM layout below");
   static_assert(kPagesPerTile * kChunks <= 32, "one TMA box per lane");
 };
 
@@ -145,14 +157,15 @@ constexpr int kMaxPBufs = 4;
 constexpr int kThreads = 416;  // 13 warps
 constexpr int kSoftmaxThreads = 256;
 
-// TMEM columns. BF16: O [0, 256), four 64-column S tiles [256, 512). FP8: O,
-// one 128-column S tile, two P tiles of 32 columns (128 keys of e4m3, hi row
-// in lane 32q + i, lo row in lane 32q + 16 + i, as S) and the Q A operand
-// (64 columns: 256 e4m3 bytes of each hi and lo row).
+// TMEM columns. O [0, 256), then BF16: four 64-column S tiles; FP8 with Q
+// in shared memory: two 128-column S tiles, each P (32 columns) written over
+// its S; FP8 with Q in TMEM: one 128-column S tile, two P tiles of 32 columns
+// (128 keys of e4m3, hi row in lane 32q + i, lo row in lane 32q + 16 + i, as
+// S) and the Q A operand (64 columns: 256 e4m3 bytes of each hi and lo row).
 constexpr uint32_t kColO = 0;    // 256 fp32 columns
 constexpr uint32_t kColS = 256;
-constexpr uint32_t kColP = 384;  // FP8
-constexpr uint32_t kColQ = 448;  // FP8
+constexpr uint32_t kColP = 384;  // FP8, Q in TMEM
+constexpr uint32_t kColQ = 448;  // FP8, Q in TMEM
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -196,7 +209,7 @@ template <bool FP8, bool VAR>
 __global__ void __launch_bounds__(kThreads, 1)
     va_main_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v) {
-  using C = Cfg<FP8>;
+  using C = Cfg<FP8, VAR>;
   constexpr int kT = C::kT;
   constexpr int kSBufs = C::kSBufs;
   constexpr int kPBufs = C::kPBufs;
@@ -408,8 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = cur % C::kKSlots;
             const int b = cur & (kSBufs - 1);
             if (!wait_or_fail(kBarFullK + s, (cur / C::kKSlots) & 1, 32)) break;
-            // S buffer b is free once the softmax has read S(cur - kSBufs)
-            if (cur >= kSBufs && !wait_or_fail(kBarSFree + b, ((cur - kSBufs) / kSBufs) & 1, 64)) break;
+            // S buffer b is free once the softmax has read S(cur - kSBufs) or,
+            // with P written over it, once P V(cur - kSBufs) has read that P
+            if (cur >= kSBufs &&
+                !wait_or_fail(C::kPOverS ? kBarPFree + b : kBarSFree + b, ((cur - kSBufs) / kSBufs) & 1, 64))
+              break;
             tc_fence_after();
             const uint32_t kst = sbase + s * C::kTensorBytes;
 #pragma unroll
@@ -446,8 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                1024, kLayoutSw128);
               const uint32_t acc = (i == 0 && kk == 0) ? 0u : 1u;
               if constexpr (C::kPInTmem) {
-                // P(x) sits in P tile pb, 8 columns per K-step
-                mma_f8f6f4_ta(tmem + kColO, tmem + kColP + pb * (kT / 4) + 8 * kk, bdesc, C::kIdPV, acc);
+                // P(x) sits in P tile pb (or over S buffer pb), 8 columns per K-step
+                const uint32_t pcol = C::kPOverS ? kColS + pb * kT : kColP + pb * (kT / 4);
+                mma_f8f6f4_ta(tmem + kColO, tmem + pcol + 8 * kk, bdesc, C::kIdPV, acc);
               } else {
                 const uint64_t a = smem_desc(pbuf + kk * 256, 128, C::kPSbo, kLayoutNone);
                 mma<FP8>(tmem + kColO, a, bdesc, C::kIdPV, acc);
@@ -556,35 +573,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float up = __uint_as_float((uint32_t)(e + 127) << 23) * (q_neg ? -1.f : 1.f);
           const float down = __uint_as_float((uint32_t)(127 - e) << 23);
           rs = cscale * down;  // rows past R stage zeros: their logits are 0
-          // d [64 qtr, +64): 16 words of each term, the TMEM A operand's
-          // columns [16 qtr, +16) of lane 32q + rl (hi) and lane 32q + 16 + rl
-          // (lo): per half of them two 16-lane stores, threads 16-31 (sub 1)
-          // at +16
-          if (ok) {
+          // d [64 qtr, +64) of row 16q + rl: 16 words of each term, four per
+          // 16-byte piece cc (raw[2 cc], raw[2 cc + 1])
+          auto split_piece = [&](int cc, uint32_t* hw, uint32_t* lw) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t hw[8], lw[8];
-#pragma unroll
-              for (int c2 = 0; c2 < 2; ++c2) {
-                const int cc = 2 * h + c2;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const uint4 a = raw[2 * cc + (k >> 1)];
-                  const uint32_t wa = (k & 1) ? a.z : a.x;
-                  const uint32_t wb = (k & 1) ? a.w : a.y;
-                  const float x0 = __uint_as_float(wa << 16) * up, x1 = __uint_as_float(wa & 0xFFFF0000u) * up;
-                  const float x2 = __uint_as_float(wb << 16) * up, x3 = __uint_as_float(wb & 0xFFFF0000u) * up;
-                  const uint32_t h01 = pack_fp8x2(x0, x1), h23 = pack_fp8x2(x2, x3);
-                  const float2 f01 = unpack_fp8x2(h01), f23 = unpack_fp8x2(h23);
-                  const uint32_t l01 = pack_fp8x2(x0 - f01.x, x1 - f01.y), l23 = pack_fp8x2(x2 - f23.x, x3 - f23.y);
-                  hw[4 * c2 + k] = h01 | (h23 << 16);
-                  lw[4 * c2 + k] = l01 | (l23 << 16);
-                }
-              }
-              tmem_st_16x32bx2_x8<16>(tmem + lane_base + kColQ + 32 * kh + 8 * h, hw);
-              tmem_st_16x32bx2_x8<16>(tmem + lane_base + (16u << 16) + kColQ + 32 * kh + 8 * h, lw);
+            for (int k = 0; k < 4; ++k) {
+              const uint4 a = raw[2 * cc + (k >> 1)];
+              const uint32_t wa = (k & 1) ? a.z : a.x;
+              const uint32_t wb = (k & 1) ? a.w : a.y;
+              const float x0 = __uint_as_float(wa << 16) * up, x1 = __uint_as_float(wa & 0xFFFF0000u) * up;
+              const float x2 = __uint_as_float(wb << 16) * up, x3 = __uint_as_float(wb & 0xFFFF0000u) * up;
+              const uint32_t h01 = pack_fp8x2(x0, x1), h23 = pack_fp8x2(x2, x3);
+              const float2 f01 = unpack_fp8x2(h01), f23 = unpack_fp8x2(h23);
+              const uint32_t l01 = pack_fp8x2(x0 - f01.x, x1 - f01.y), l23 = pack_fp8x2(x2 - f23.x, x3 - f23.y);
+              hw[k] = h01 | (h23 << 16);
+              lw[k] = l01 | (l23 << 16);
             }
-            tmem_wait_st();
+          };
+          if (ok) {
+            if constexpr (C::kQInTmem) {
+              // the A operand's columns [16 qtr, +16) of lane 32q + rl (hi) and
+              // lane 32q + 16 + rl (lo): per half two 16-lane stores, threads
+              // 16-31 (sub 1) at +16
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t hw[8], lw[8];
+                split_piece(2 * h, hw, lw);
+                split_piece(2 * h + 1, hw + 4, lw + 4);
+                tmem_st_16x32bx2_x8<16>(tmem + lane_base + kColQ + 32 * kh + 8 * h, hw);
+                tmem_st_16x32bx2_x8<16>(tmem + lane_base + (16u << 16) + kColQ + 32 * kh + 8 * h, lw);
+              }
+              tmem_wait_st();
+            } else {
+              // region kh, 16-byte pieces 4 sub .. 4 sub + 3 of A rows 32q + rl
+              // (hi) and 32q + 16 + rl (lo)
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) {
+                uint32_t hw[4], lw[4];
+                split_piece(cc, hw, lw);
+                const int swz = ((4 * sub + cc) ^ (rl & 7)) << 4;
+                const int ahi = 32 * q + rl, alo = ahi + 16;
+                *reinterpret_cast<uint4*>(qs + kh * C::kQRegion + ahi * 128 + swz) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(qs + kh * C::kQRegion + alo * 128 + swz) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+              }
+            }
           }
         } else {
           rs = cscale;  // rows past R stage zeros: their logits are 0
@@ -675,15 +707,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the hi and lo partials of row 16q + rl, keys [64 kh + 32 sub,
             // +32): two 16-lane loads (hi rows in lanes 32q.., lo rows in
             // lanes 32q + 16..) whose second halves go to threads 16-31, so
-            // every thread gets both terms of its own keys; S buffer b is then
-            // free for Q K^T of the next tile
+            // every thread gets both terms of its own keys. S buffer b is then
+            // free for Q K^T of a later tile, or is overwritten by P(cur) and
+            // freed by P V's commit.
             uint32_t vh[32], vl[32];
             tmem_ld_16x32bx2_x32<32>(tmem + lane_base + kColS + b * kT + 64 * kh, vh);
             tmem_ld_16x32bx2_x32<32>(tmem + lane_base + (16u << 16) + kColS + b * kT + 64 * kh, vl);
             tmem_wait_ld();
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarSFree + b));
+            if constexpr (!C::kPOverS) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(kBarSFree + b));
+            }
 #pragma unroll
             for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(vh[i]) + __uint_as_float(vl[i]);
           } else {
@@ -726,8 +761,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmax = exchange(tmax * xs, true);  // log2 units (xs > 0 keeps the order)
         if (!ok) continue;
 
-        // P buffer pb was last read by PV(cur - kPBufs)
-        if (cur >= kPBufs && !wait_or_fail(kBarPFree + pb, ((cur - kPBufs) / kPBufs) & 1, 512)) continue;
+        // P buffer pb was last read by PV(cur - kPBufs). (A P over S(cur):
+        // Q K^T(cur) already waited for that.)
+        if (!C::kPOverS && cur >= kPBufs &&
+            !wait_or_fail(kBarPFree + pb, ((cur - kPBufs) / kPBufs) & 1, 512))
+          continue;
 
         const bool need = tmax > m_ref + kOvershoot;
         // A row's first reference takes more headroom: its running max keeps
@@ -788,14 +826,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               pl[i >> 1] = l2;
             }
           }
-          // A operand of P V in TMEM, P tile pb: lane 32q + rl (hi row) and
+          // A operand of P V in TMEM, P tile pb or over S(cur) (pb == b
+          // then): lane 32q + rl (hi row) and
           // lane 32q + 16 + rl (lo row) take the e4m3 bytes of keys
           // [64 kh, +64) at columns [16 kh, +16). This thread holds keys
           // [32 qtr, +32) of both: two 16-lane stores, its hi bytes into the
           // hi row and its lo bytes into the lo row, threads 16-31 at +8.
+          // Over S, the quadrant's other warp read its S columns before the
+          // exchange.
+          const uint32_t pcol = C::kPOverS ? kColS + pb * kT : kColP + pb * (kT / 4);
           tc_fence_after();
-          tmem_st_16x32bx2_x8<8>(tmem + lane_base + kColP + pb * (kT / 4) + 16 * kh, ph);
-          tmem_st_16x32bx2_x8<8>(tmem + lane_base + (16u << 16) + kColP + pb * (kT / 4) + 16 * kh, pl);
+          tmem_st_16x32bx2_x8<8>(tmem + lane_base + pcol + 16 * kh, ph);
+          tmem_st_16x32bx2_x8<8>(tmem + lane_base + (16u << 16) + pcol + 16 * kh, pl);
           tmem_wait_st();
         } else {
           uint32_t pw[8];
@@ -828,8 +870,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // FullV(vs) alternates between the tiles that share slot vs, so its
           // parity names tile cur only once the slot's previous tile
           // (cur - kVSlots) has been consumed by P V. The softmax at tile cur
-          // only knows P V(cur - kPBufs) done (its P buffer's wait above); if
-          // that is not enough, wait.
+          // only knows P V(cur - kPBufs) done (its P buffer's wait above, or
+          // for a P over S the S buffer Q K^T waited for); if that is not
+          // enough, wait.
           if constexpr (kPBufs > C::kVSlots) {
             const int xv = cur - C::kVSlots;
             if (xv >= 0 && !wait_or_fail(kBarPFree + (xv & (kPBufs - 1)), (xv / kPBufs) & 1, 2049)) continue;
@@ -940,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool FP8, bool VAR>
 cudaError_t set_smem() {
   return cudaFuncSetAttribute(va_main_tc_kernel<FP8, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<FP8>::kSmemBytes);
+                              Cfg<FP8, VAR>::kSmemBytes);
 }
 
 cudaError_t prepare_main_tc() {
@@ -959,7 +1002,8 @@ cudaError_t launch_main_tc(const Params& p, const CUtensorMap& tm_k, const CUten
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_splits);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = p.kv_fp8 ? Cfg<true>::kSmemBytes : Cfg<false>::kSmemBytes;
+  cfg.dynamicSmemBytes = p.kv_fp8 ? (var ? Cfg<true, true>::kSmemBytes : Cfg<true, false>::kSmemBytes)
+                                  : (var ? Cfg<false, true>::kSmemBytes : Cfg<false, false>::kSmemBytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
