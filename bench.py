@@ -33,7 +33,11 @@ METRIC = "verify-attn µs/call and achieved HBM GB/s (fraction of ~8 TB/s) on 1 
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-MAIN_KERNEL = {"fp8_e4m3": "va_main_tc_kernel<true, false>", "bf16": "va_main_tc_kernel<false, false>",
+# main kernel by KV dtype and, for the GQA kernel, the layout the plan picks
+# (verify_attn_plan's `kernel`: 2 = FP8 with Q in tensor memory)
+MAIN_KERNEL = {("fp8_e4m3", 1): "va_main_tc_kernel<true, false, false>",
+               ("fp8_e4m3", 2): "va_main_tc_kernel<true, false, true>",
+               ("bf16", 1): "va_main_tc_kernel<false, false, false>",
                "mla": "va_mla_tc_kernel", "mla_bf16": "va_mla_bf16_tc_kernel"}
 
 
@@ -496,7 +500,9 @@ def run_ours(args):
         out = torch.empty_like(w.q)
         n_ws = va.workspace_size(w.q, w.k_cache, w.seqused_k, w.max_seqlen_q, w.max_seqlen_k)
         inputs = ("q", "k_cache", "v_cache", "block_table", "cu_seqlens_q", "seqused_k")
-        kernel = MAIN_KERNEL[w.kv_dtype]
+        layout = va.plan(w.num_seqs, w.k_cache.shape[2], w.q.shape[1], w.max_seqlen_q, w.max_seqlen_k,
+                         w.kv_dtype, torch.cuda.get_device_properties(dev).multi_processor_count)["kernel"]
+        kernel = MAIN_KERNEL[(w.kv_dtype, layout)]
     alg = w.algorithmic_bytes()
     ws = torch.zeros(n_ws + 256, dtype=torch.uint8, device=dev)
 

@@ -81,7 +81,10 @@ typedef struct va_plan {
                               of the batch's key tiles (its KV segments) */
   int32_t max_rows;        /* packed rows per (sequence, KV head) = G * max_seqlen_q */
   int32_t num_work;        /* B * Hkv (sequence, KV head) pairs */
-  int32_t kernel;          /* main-kernel variant the launch will use */
+  int32_t kernel;          /* main-kernel layout the launch will use: 1 = Q in
+                              shared memory (BF16; FP8 batches of fewer than 16
+                              tiles per CTA; any variant option), 2 = FP8 with
+                              Q and P in tensor memory and a deeper K ring */
   int32_t reserved;
   int64_t workspace_bytes; /* scratch the split-KV partials need */
 } va_plan;

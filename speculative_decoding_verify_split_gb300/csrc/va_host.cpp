@@ -177,7 +177,12 @@ va_status make_plan(int64_t B, int64_t hkv, int64_t hq, int32_t max_q, int32_t m
   plan->num_splits = (int32_t)splits;
   plan->max_rows = (int32_t)(G * max_q);
   plan->num_work = (int32_t)J;
-  plan->kernel = kKernelTc;
+  // Q in TMEM and the deeper K ring pay off when CTAs stream many tiles; a
+  // small batch's CTAs hold a few tiles each, whose latency the single S tile
+  // lengthens (gqa_32q2kv: 27.3 against 26.3 us per call)
+  plan->kernel = kv_dtype == VA_FP8_E4M3 && window_left < 0 && tiles_bound >= kSmallSplitTiles * splits
+                     ? kKernelTcQTmem
+                     : kKernelTc;
   plan->workspace_bytes = (int64_t)workspace_layout(J, splits, G * max_q).total;
   return VA_OK;
 }
@@ -328,6 +333,7 @@ va_status launch(const va_tensor* q, const va_tensor* k, const va_tensor* v, con
   p.num_work = plan.num_work;
   p.piece_cost = piece_cost_for(
       plan, tiles_upper_bound(sh.num_seqs, sh.hkv, max_q, max_k, plan.tile_keys, p.window_left));
+  p.q_in_tmem = plan.kernel == kKernelTcQTmem ? 1 : 0;
   p.dv = kHeadDim;
   p.wait_limit_ns = wait_limit_ns();
   if (part) {

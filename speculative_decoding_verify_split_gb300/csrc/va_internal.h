@@ -72,6 +72,7 @@ struct Params {
   // epilogue and pipeline refill), so a CTA that starts an item gets fewer
   // tiles.
   int32_t tile_keys, num_splits, max_rows, num_work, piece_cost;
+  int32_t q_in_tmem;   // 1: the plan chose kKernelTcQTmem (used unless a variant option is set)
   int32_t dv;          // output (value) columns: kHeadDim, or kMlaNope over a latent cache
   // Limit of every bounded wait of the main kernels, in ns (kDefaultWaitLimitNs
   // unless a test shortened it to make waits run out).
@@ -109,8 +110,13 @@ inline WorkspaceLayout workspace_layout(int64_t num_work, int64_t num_splits, in
   return w;
 }
 
-// Main kernel (tensor cores) and its key-tile sizes.
-enum Kernel : int32_t { kKernelTc = 1 };
+// Main kernel (tensor cores) and its key-tile sizes. kKernelTc keeps Q in
+// shared memory (FP8: two S tiles, each P written over its S); kKernelTcQTmem,
+// the FP8 kernel for batches of at least kSmallSplitTiles tiles per CTA,
+// takes Q and P from TMEM (one S tile) and spends the shared memory on a
+// fourth K ring slot. The variant options (window, soft cap, sinks) always
+// run the first layout.
+enum Kernel : int32_t { kKernelTc = 1, kKernelTcQTmem = 2 };
 constexpr int kTcTileKeysFp8 = 128;  // keys per tile, FP8 KV
 constexpr int kTcTileKeysBf16 = 64;  // keys per tile, BF16 KV
 // Split cost of starting a work item, in tiles: a CTA's boundary between two

@@ -81,21 +81,24 @@ namespace {
 
 using namespace ptx;
 
-template <bool FP8, bool VAR>
+template <bool FP8, bool VAR, bool QTM>
 struct Cfg {
   static constexpr int kT = FP8 ? kTcTileKeysFp8 : kTcTileKeysBf16;  // keys per tile: 128 / 64
   static constexpr int kPagesPerTile = kT / kPageSize;
   static constexpr int kKpt = kT / 4;                      // keys per softmax thread per tile
-  // FP8 has two TMEM layouts. The plain kernel takes Q and P from TMEM
-  // (one S tile, two P tiles of their own) and spends the shared memory on
-  // a fourth K ring slot. The variant kernel keeps Q in shared memory and
-  // two S tiles, with P written over its S tile: a soft cap makes the
-  // softmax the bottleneck, and with one S tile every tile's Q K^T waits on
-  // the softmax's load of the previous S, its MMA issue slowed by the
-  // softmax warps' ALU work on the same sub-partitions (soft cap 30 on
+  // FP8 has two TMEM layouts. QTM (the plain kernel on batches of many
+  // tiles per CTA) takes Q and P from TMEM (one S tile, two P tiles of their
+  // own) and spends the shared memory on a fourth K ring slot. Otherwise Q
+  // stays in shared memory with two S tiles, P written over its S tile: with
+  // one S tile every tile's Q K^T waits on the softmax's load of the
+  // previous S, which a CTA of few tiles pays as latency, and which a soft
+  // cap (the softmax then the bottleneck, its ALU work slowing the MMA issue
+  // on the same sub-partitions) pays per tile (soft cap 30 on
   // long_context_fp8: 146.3 us against 137.0 us with two S tiles).
-  static constexpr bool kQInTmem = FP8 && !VAR;
-  static constexpr bool kPOverS = FP8 && VAR;
+  static_assert(FP8 || !QTM, "Q in TMEM is an FP8 layout");
+  static_assert(!(VAR && QTM), "the variant kernel keeps Q in shared memory");
+  static constexpr bool kQInTmem = QTM;
+  static constexpr bool kPOverS = FP8 && !QTM;
   static constexpr int kSBufs = FP8 ? (kQInTmem ? 1 : 2) : 4;  // S tiles in TMEM
   static constexpr int kPBufs = FP8 ? 2 : 4;               // P buffers: TMEM (fp8) / smem (bf16)
   static constexpr int kEsize = FP8 ? 1 : 2;               // bytes per KV element
@@ -204,12 +207,12 @@ __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t
 }
 
 // VAR: compiled with the sliding-window / soft-cap / sink code (the plain path
-// is compiled without it).
-template <bool FP8, bool VAR>
+// is compiled without it). QTM: the FP8 layout with Q and P in TMEM (Cfg).
+template <bool FP8, bool VAR, bool QTM>
 __global__ void __launch_bounds__(kThreads, 1)
     va_main_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v) {
-  using C = Cfg<FP8, VAR>;
+  using C = Cfg<FP8, VAR, QTM>;
   constexpr int kT = C::kT;
   constexpr int kSBufs = C::kSBufs;
   constexpr int kPBufs = C::kPBufs;
@@ -980,18 +983,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <bool FP8, bool VAR>
+template <bool FP8, bool VAR, bool QTM>
 cudaError_t set_smem() {
-  return cudaFuncSetAttribute(va_main_tc_kernel<FP8, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<FP8, VAR>::kSmemBytes);
+  return cudaFuncSetAttribute(va_main_tc_kernel<FP8, VAR, QTM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<FP8, VAR, QTM>::kSmemBytes);
 }
 
 cudaError_t prepare_main_tc() {
-  cudaError_t e = set_smem<true, false>();
-  if (e == cudaSuccess) e = set_smem<false, false>();
-  if (e == cudaSuccess) e = set_smem<true, true>();
-  if (e == cudaSuccess) e = set_smem<false, true>();
+  cudaError_t e = set_smem<true, false, true>();
+  if (e == cudaSuccess) e = set_smem<true, false, false>();
+  if (e == cudaSuccess) e = set_smem<false, false, false>();
+  if (e == cudaSuccess) e = set_smem<true, true, false>();
+  if (e == cudaSuccess) e = set_smem<false, true, false>();
   return e;
+}
+
+template <bool FP8, bool VAR, bool QTM>
+static cudaError_t launch_one(cudaLaunchConfig_t& cfg, const Params& p, const CUtensorMap& tm_k,
+                              const CUtensorMap& tm_v) {
+  cfg.dynamicSmemBytes = Cfg<FP8, VAR, QTM>::kSmemBytes;
+  return cudaLaunchKernelEx(&cfg, va_main_tc_kernel<FP8, VAR, QTM>, p, tm_k, tm_v);
 }
 
 cudaError_t launch_main_tc(const Params& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
@@ -1002,19 +1013,19 @@ cudaError_t launch_main_tc(const Params& p, const CUtensorMap& tm_k, const CUten
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_splits);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = p.kv_fp8 ? (var ? Cfg<true, true>::kSmemBytes : Cfg<true, false>::kSmemBytes)
-                                  : (var ? Cfg<false, true>::kSmemBytes : Cfg<false, false>::kSmemBytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.kv_fp8)
-    return var ? cudaLaunchKernelEx(&cfg, va_main_tc_kernel<true, true>, p, tm_k, tm_v)
-               : cudaLaunchKernelEx(&cfg, va_main_tc_kernel<true, false>, p, tm_k, tm_v);
-  return var ? cudaLaunchKernelEx(&cfg, va_main_tc_kernel<false, true>, p, tm_k, tm_v)
-             : cudaLaunchKernelEx(&cfg, va_main_tc_kernel<false, false>, p, tm_k, tm_v);
+  if (p.kv_fp8) {
+    if (var) return launch_one<true, true, false>(cfg, p, tm_k, tm_v);
+    return p.q_in_tmem ? launch_one<true, false, true>(cfg, p, tm_k, tm_v)
+                       : launch_one<true, false, false>(cfg, p, tm_k, tm_v);
+  }
+  return var ? launch_one<false, true, false>(cfg, p, tm_k, tm_v)
+             : launch_one<false, false, false>(cfg, p, tm_k, tm_v);
 }
 
 }  // namespace va

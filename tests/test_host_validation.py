@@ -116,6 +116,21 @@ def test_plan_force_and_clamp():
     assert va.plan(3, 1, 16, 4, 0, "fp8_e4m3", 152)["num_splits"] == 1
 
 
+def test_plan_picks_the_layout():
+    """FP8 batches of at least 16 key tiles per CTA run the kernel with Q and
+    P in tensor memory (plan kernel 2); BF16 and small FP8 batches the one
+    with Q in shared memory (1)."""
+    assert va.plan(16, 1, 16, 4, 131072, "fp8_e4m3", 152)["kernel"] == 2
+    assert va.plan(64, 1, 16, 3, 32768, "fp8_e4m3", 152)["kernel"] == 2
+    assert va.plan(2, 1, 16, 4, 1024, "fp8_e4m3", 152)["kernel"] == 1
+    assert va.plan(8, 2, 32, 4, 4096, "fp8_e4m3", 152)["kernel"] == 1
+    assert va.plan(16, 1, 16, 4, 131072, "bf16", 152)["kernel"] == 1
+    # the boundary: 16 tiles per CTA
+    assert va.plan(1, 1, 16, 4, 16 * 128, "fp8_e4m3", 152, force_splits=1)["kernel"] == 2
+    assert va.plan(1, 1, 16, 4, 16 * 128 - 128, "fp8_e4m3", 152, force_splits=1)["kernel"] == 1
+    assert va.plan(2, 1, 16, 4, 1024, "fp8_e4m3", 152, force_splits=1)["kernel"] == 2
+
+
 def test_plan_rejects():
     for bad in [(1, 1, 16, 5, 100, "fp8_e4m3", 152), (1, 3, 16, 1, 100, "fp8_e4m3", 152),
                 (1, 1, 16, 1, 100, "fp8_e4m3", 0), (1, 1, 16, 0, 100, "bf16", 152)]:
