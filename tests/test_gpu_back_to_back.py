@@ -63,14 +63,17 @@ def _run_alternating(a, b, names, call, n_calls=8):
 
 
 class _Gqa:
-    @staticmethod
-    def workspace_size(w):
-        return va.workspace_size(w.q, w.k_cache, w.seqused_k, w.max_seqlen_q, w.max_seqlen_k)
+    def __init__(self, splits=0):
+        self.splits = splits
+
+    def workspace_size(self, w):
+        return va.workspace_size(w.q, w.k_cache, w.seqused_k, w.max_seqlen_q, w.max_seqlen_k, self.splits)
 
     def __call__(self, w, out, ws):
         return va.verify_attn_ex(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q,
                                  w.seqused_k, w.max_seqlen_q, w.max_seqlen_k, w.softmax_scale,
-                                 w.k_descale, w.v_descale, out=out, workspace=ws)
+                                 w.k_descale, w.v_descale, out=out, workspace=ws,
+                                 num_splits=self.splits)
 
 
 class _Mla:
@@ -84,13 +87,19 @@ class _Mla:
                                   w.v_descale, out=out, workspace=ws)
 
 
-@pytest.mark.parametrize("dt", ["fp8_e4m3", "bf16"])
-def test_back_to_back_gqa(dt):
+# (KV dtype, forced split count): FP8 with 8 splits runs the kernel with Q in
+# tensor memory (at least 16 key tiles per CTA), the others Q in shared memory
+@pytest.mark.parametrize("dt,splits", [("fp8_e4m3", 0), ("bf16", 0), ("fp8_e4m3", 8)])
+def test_back_to_back_gqa(dt, splits):
     fp8 = dt == "fp8_e4m3"
     a, b = _batches(lambda seed: make_workload(Q_LENS, KV_LENS, 16, 2, dt, seed=seed,
                                                k_descale=1.1 if fp8 else None,
                                                v_descale=0.8 if fp8 else None))
-    outs, refs = _run_alternating(a, b, ["q", "k_cache", "v_cache", "block_table", "seqused_k"], _Gqa())
+    if splits:
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert va.plan(a.num_seqs, 2, 16, a.max_seqlen_q, a.max_seqlen_k, dt, sms, splits)["kernel"] == 2
+    outs, refs = _run_alternating(a, b, ["q", "k_cache", "v_cache", "block_table", "seqused_k"],
+                                  _Gqa(splits))
     assert not torch.equal(refs[0], refs[1])
     for i, o in enumerate(outs):
         assert torch.equal(o.view(torch.int16), refs[i % 2].view(torch.int16)), f"call {i}"
@@ -101,6 +110,7 @@ class _Variants(_Gqa):
     kernel and the SINKS merge)."""
 
     def __init__(self, hq):
+        super().__init__()
         self.sinks = torch.linspace(-1.5, 1.5, hq, device="cuda")
 
     def __call__(self, w, out, ws):
