@@ -106,7 +106,9 @@ def _gpu_rank(rank, world, port, ci, q):
     out = dcp_verify_attn(w.q, w.k_cache, w.v_cache, bt, w.cu_seqlens_q, su, ext, w.max_seqlen_q,
                           bt.shape[1] * 16, w.softmax_scale, w.k_descale, w.v_descale)
     torch.cuda.synchronize()
-    q.put((rank, out.cpu()))
+    # by value (the bf16 bits as a numpy array): a torch tensor would go
+    # through a file descriptor this process shares, gone if it exits first
+    q.put((rank, out.cpu().view(torch.int16).numpy().copy()))
     dist.barrier()
     dist.destroy_process_group()
 
@@ -117,6 +119,6 @@ def test_dcp_two_processes_on_one_gpu(ci):
     from gpu_util import compare
     from oracle.attention_fp64 import oracle_from_torch
     res = _run(_gpu_rank, 2, ci)
-    a, b = res[0][1], res[1][1]
+    a, b = (torch.from_numpy(r[1]).view(torch.bfloat16) for r in res)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16)), "ranks disagree"
     print("dcp", ci, compare(a, oracle_from_torch(_workload(ci))))
